@@ -1,0 +1,189 @@
+"""WKV-7 oracle: the plain double-precision CPU reference.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, the package's ``smoke()`` check and
+the benchmark's CPU-baseline leg may import this package.  The product path
+(``rwkv_wkv_gb300`` and its C-ABI library) never imports, links or calls it,
+and the two share no code: this side is plain C in ``wkv7_oracle.c`` plus the
+array plumbing below.
+
+The recurrence (RWKV-X Architecture, "WKV-7 Kernel (Generalized Delta Rule)"),
+per head with state S[i][j] (i value index, j key index):
+
+    h = S a ;  S <- S diag(w) + h b^T + v k^T ;  o = S r
+
+Pool-level helpers follow the state-slot model of "wkvm: state-slot inference
+for RWKV, GDN and Mamba hybrids" ("The allocation unit wkvm changes"): a slot is
+a fixed-size block holding one state per (layer, head); decode advances each
+listed slot by one token, prefill advances each listed slot by its sequence.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "wkv7_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile wkv7_oracle.c with gcc into oracle/_build/liboracle.so."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-pthread",
+           "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            dp = ctypes.POINTER(ctypes.c_double)
+            ll = ctypes.c_longlong
+            for name in ("wkv7_oracle_sequential", "wkv7_oracle_matprod"):
+                f = getattr(lib, name)
+                f.restype = ctypes.c_int
+                f.argtypes = [ctypes.c_int, ctypes.c_int, dp, ll, ll] + [dp] * 7
+            f = lib.wkv7_oracle_chunked
+            f.restype = ctypes.c_int
+            f.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, dp, ll, ll] + [dp] * 7
+            f = lib.wkv7_oracle_sequential_batch
+            f.restype = ctypes.c_int
+            f.argtypes = [ctypes.c_int, ctypes.c_int, dp, ctypes.POINTER(ll),
+                          ctypes.POINTER(ctypes.c_int), ll] + [dp] * 7 + [ctypes.c_int]
+            _lib = lib
+    return _lib
+
+
+def _f64(x) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(x: np.ndarray):
+    return x.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _one_head(fn_name, S0, r, w, k, v, a, b, extra=()):
+    """Run one head over T tokens; inputs are [T, N], S0 is [N, N]."""
+    S = _f64(S0).copy()
+    ins = [_f64(x) for x in (r, w, k, v, a, b)]
+    T, N = ins[0].shape
+    for x in ins:
+        if x.shape != (T, N):
+            raise ValueError("inputs must all be [T, N]")
+    if S.shape != (N, N):
+        raise ValueError("state must be [N, N]")
+    o = np.zeros((T, N), dtype=np.float64)
+    fn = getattr(_load(), fn_name)
+    args = [N, T] + list(extra) + [_ptr(S), 0, N] + [_ptr(x) for x in ins] + [_ptr(o)]
+    rc = fn(*args)
+    if rc:
+        raise RuntimeError(f"{fn_name} failed with code {rc}")
+    return o, S
+
+
+def sequential(S0, r, w, k, v, a, b):
+    """Sequential recurrence on one head. Returns (o [T,N], S_T [N,N])."""
+    return _one_head("wkv7_oracle_sequential", S0, r, w, k, v, a, b)
+
+
+def matprod(S0, r, w, k, v, a, b):
+    """Matrix-product form on one head (tiny inputs only). Returns (o, S_T)."""
+    return _one_head("wkv7_oracle_matprod", S0, r, w, k, v, a, b)
+
+
+def chunked(S0, r, w, k, v, a, b, L: int = 64):
+    """Chunked WY/UT form on one head, chunks of L from the first token."""
+    fn = _load().wkv7_oracle_chunked
+    S = _f64(S0).copy()
+    ins = [_f64(x) for x in (r, w, k, v, a, b)]
+    T, N = ins[0].shape
+    o = np.zeros((T, N), dtype=np.float64)
+    rc = fn(N, T, int(L), _ptr(S), 0, N, *[_ptr(x) for x in ins], _ptr(o))
+    if rc:
+        raise RuntimeError(f"wkv7_oracle_chunked failed with code {rc}")
+    return o, S
+
+
+def run_units(S, base, T, tok_stride, inputs, n_threads: int = 1):
+    """Sequential recurrence on many independent heads at once.
+
+    S: [n_units, N, N] float64, updated in place.  base[u], T[u]: first element
+    offset and token count of unit u; token t of unit u, channel j is at
+    x[base[u] + t*tok_stride + j] for every x in inputs = (r, w, k, v, a, b)
+    (flat float64 arrays).  Returns o with the same flat layout as the inputs.
+    """
+    S = np.ascontiguousarray(S, dtype=np.float64)
+    n_units, N, _ = S.shape
+    base = np.ascontiguousarray(base, dtype=np.int64)
+    T = np.ascontiguousarray(T, dtype=np.int32)
+    ins = [_f64(x).reshape(-1) for x in inputs]
+    o = np.zeros_like(ins[0])
+    rc = _load().wkv7_oracle_sequential_batch(
+        N, n_units, _ptr(S), base.ctypes.data_as(ctypes.POINTER(ctypes.c_longlong)),
+        T.ctypes.data_as(ctypes.POINTER(ctypes.c_int)), int(tok_stride),
+        *[_ptr(x) for x in ins], _ptr(o), int(n_threads))
+    if rc:
+        raise RuntimeError(f"wkv7_oracle_sequential_batch failed with code {rc}")
+    return o, S
+
+
+def decode_step(states, r, w, k, v, a, b, n_threads: int = 1):
+    """One decode token for B rows of H heads.
+
+    states: [B, H, N, N] (the gathered slot states of one layer); inputs
+    [B, H, N].  Returns (o [B, H, N], new states [B, H, N, N]) in float64.
+    """
+    st = _f64(states)
+    B, H, N, _ = st.shape
+    S = st.reshape(B * H, N, N).copy()
+    base = np.arange(B * H, dtype=np.int64) * N
+    T = np.ones(B * H, dtype=np.int32)
+    o, S = run_units(S, base, T, N, (r, w, k, v, a, b), n_threads)
+    return o.reshape(B, H, N), S.reshape(B, H, N, N)
+
+
+def prefill(states, cu_seqlens, r, w, k, v, a, b, n_threads: int = 1):
+    """Ragged prefill: sequence s covers tokens cu_seqlens[s]..cu_seqlens[s+1].
+
+    states: [S, H, N, N] start states; inputs [Ttot, H, N].
+    Returns (o [Ttot, H, N], final states [S, H, N, N]) in float64.
+    """
+    st = _f64(states)
+    nS, H, N, _ = st.shape
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    S = st.reshape(nS * H, N, N).copy()
+    base = np.empty(nS * H, dtype=np.int64)
+    T = np.empty(nS * H, dtype=np.int32)
+    for s in range(nS):
+        for h in range(H):
+            base[s * H + h] = cu[s] * H * N + h * N
+            T[s * H + h] = cu[s + 1] - cu[s]
+    o, S = run_units(S, base, T, H * N, (r, w, k, v, a, b), n_threads)
+    Ttot = np.asarray(r).shape[0]
+    return o.reshape(Ttot, H, N), S.reshape(nS, H, N, N)
+
+
+def rel_err(x, ref) -> float:
+    """Normwise-max relative error: max|x - ref| / max|ref| (0 when both are 0)."""
+    x = np.asarray(x, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    den = float(np.max(np.abs(ref))) if ref.size else 0.0
+    num = float(np.max(np.abs(x - ref))) if ref.size else 0.0
+    if den == 0.0:
+        return num
+    return num / den
