@@ -1,0 +1,733 @@
+#!/usr/bin/env python3
+"""Benchmark of the WKV-7 state-slot hot path on one GB300 (or N replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload mixed|decode12|prefill|sweep] [--batch B] [--graph]
+
+Default workload ("mixed", one step = every part of the hot path): on a
+4096-slot pool of 32 heads x 64 (1 layer) -- create 64 fresh slots, snapshot
+64 slots, decode 1024 slots at permuted ids, chunked prefill of 64 ragged
+sequences (lengths uniform on 1..2048) into the fresh slots, fork 64 slots,
+restore the 64 snapshots.  Throughput = (decode tokens + prefill tokens) per
+second; one decode slot-step and one prefill token are each one token through
+one layer.  Other workloads: "decode12" (12 layers x 12 heads, 256 of 1024
+slots), "prefill" (8 x 4096 tokens, 32 heads), "sweep" (32 layers x 64 heads,
+--batch of a 4096-slot pool).
+
+Prints ONE JSON line (rank 0).  Timing: W untimed steps, then K steps between
+CUDA events on the launching stream, bracketed by a barrier and a device
+synchronisation, max over ranks.  Each step moves more bytes than the 129 MB L2
+holds (inputs larger than L2), so no explicit flush is used.
+--impl reference times the CPU oracle (the only reference this method has) on
+a bounded sample of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as wl  # noqa: E402
+
+METRIC = "WKV-7 decode slot-steps/s + GB/s (% HBM peak); prefill tokens/s (% roofline)"
+HEAD_BYTES_STATE = 64 * 64 * 4
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+# --------------------------------------------------------------------------- env
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", choices=["mixed", "decode12", "prefill", "sweep"],
+                   default="mixed")
+    p.add_argument("--batch", type=int, default=4096, help="sweep batch size")
+    p.add_argument("--graph", action="store_true", help="replay each step as a CUDA graph")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args(argv)
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS)
+
+
+def aggregate(elapsed_s: float, units: float, world: int, device=None):
+    """Whole-job figures over ranks: max of the elapsed times, sum of the units."""
+    if world <= 1:
+        return elapsed_s, units
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=device)
+    u = torch.tensor([units], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", gpu_id], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def wait_first(self, timeout=5.0):
+        t0 = time.time()
+        while self.proc and not self.samples and time.time() - t0 < timeout:
+            time.sleep(0.02)
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        rows = [s for ts, s in self.samples if t0 - 0.1 <= ts <= t1 + 0.1 and len(s) >= 9]
+        if not rows:
+            rows = [s for _, s in self.samples if len(s) >= 9][-3:]
+        if not rows:
+            return None
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        reasons = sorted({name for r in rows for name, val in zip(self.REASONS, r[5:9])
+                          if val.strip().lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- workloads
+class Workload:
+    """One benchmark workload on one GPU.  Subclasses set self.phases (ordered
+    names), self.phase_bytes (algorithmic bytes per phase per step),
+    self.tokens_per_step, self.dominant and implement setup/step/host_io."""
+    name = ""
+    description = ""
+    dominant = ""
+
+    def config(self) -> dict:
+        return {}
+
+
+class Mixed(Workload):
+    name = wl.MIXED.name
+
+    def __init__(self, torch, device, seed=wl.MIXED.seed):
+        from rwkv_wkv_gb300 import Pool
+        W = wl.MIXED
+        self.torch, self.device = torch, device
+        self.H, self.N = W.H, W.N
+        plan = wl.mixed_plan(seed)
+        self.plan = plan
+        self.lengths = plan["lengths"].astype(np.int64)
+        self.total = int(self.lengths.sum())
+        self.pool = Pool(1, W.H, W.n_slots, n_snapshots=wl.MIXED_VERB_N, device=device)
+        g = torch.Generator(device=device).manual_seed(seed)
+        self.pool.states.normal_(0.0, 0.1, generator=g)
+        # slot table: every id in use except the prefill targets, which each
+        # step creates (zeroed) and returns at the end.
+        self.pool.alloc(W.n_slots)
+        self.pool.free(list(plan["prefill"][::-1]))
+        self.snap_ids_host = self.pool.snapshot_alloc(wl.MIXED_VERB_N)
+        i32 = lambda x: torch.as_tensor(np.asarray(x, dtype=np.int32), device=device)  # noqa: E731
+        self.dec_ids = i32(plan["decode"])
+        self.pre_ids = i32(plan["prefill"])
+        self.cu = i32(wl.cu_seqlens(self.lengths))
+        self.fork_src, self.fork_dst = i32(plan["fork_src"]), i32(plan["fork_dst"])
+        self.snap_src, self.snap_ids = i32(plan["snap_src"]), i32(self.snap_ids_host)
+        B = wl.MIXED_DECODE_B
+        self.dec_in = wl.token_inputs_device(seed, B, W.H, W.N, device, generator_offset=1)
+        self.pre_in = wl.token_inputs_device(seed, self.total, W.H, W.N, device,
+                                             generator_offset=2)
+        self.o_dec = torch.empty(B, W.H, W.N, dtype=torch.float32, device=device)
+        self.o_pre = torch.empty(self.total, W.H, W.N, dtype=torch.float32, device=device)
+        slot_bytes = self.pool.slot_bytes
+        nv = wl.MIXED_VERB_N
+        in_row = W.H * W.N * 2 * 6
+        out_row = W.H * W.N * 4
+        self.phases = ["create", "snapshot", "decode", "prefill", "fork", "restore"]
+        self.phase_bytes = {
+            "create": wl.MIXED_PREFILL_SEQS * slot_bytes,
+            "snapshot": 2 * nv * slot_bytes,
+            "decode": B * (W.H * 2 * HEAD_BYTES_STATE + in_row + out_row),
+            "prefill": self.total * (in_row + out_row)
+            + wl.MIXED_PREFILL_SEQS * W.H * 2 * HEAD_BYTES_STATE,
+            "fork": 2 * nv * slot_bytes,
+            "restore": 2 * nv * slot_bytes,
+        }
+        self.tokens_per_step = B + self.total
+        self.dominant = "prefill"
+        self.launches_per_step = 6
+        self.check_ids = True
+
+    def step(self, ev=None):
+        pool = self.pool
+        rec = (lambda name: ev[name].record()) if ev else (lambda name: None)
+        rec("start")
+        created = pool.create(wl.MIXED_PREFILL_SEQS)
+        if self.check_ids:
+            assert created == [int(x) for x in self.plan["prefill"]], "slot table order"
+            self.check_ids = False
+        rec("create")
+        pool.snapshot(self.snap_src, self.snap_ids)
+        rec("snapshot")
+        pool.decode_step(0, self.dec_ids, *self.dec_in, o=self.o_dec)
+        rec("decode")
+        pool.prefill(0, self.pre_ids, self.cu, *self.pre_in, o=self.o_pre,
+                     max_seqlen=wl.MIXED_MAX_LEN)
+        rec("prefill")
+        pool.fork(self.fork_src, self.fork_dst)
+        rec("fork")
+        pool.restore(self.snap_ids, self.snap_src)
+        rec("restore")
+        pool.free(created[::-1])
+
+    def host_io(self):
+        """(inputs to upload each step, outputs to read back each step)."""
+        ins = [self.dec_ids, self.pre_ids, self.cu, self.fork_src, self.fork_dst,
+               self.snap_src, self.snap_ids] + self.dec_in + self.pre_in
+        return ins, [self.o_dec, self.o_pre]
+
+    def config(self):
+        return {"workload": wl.MIXED.description, "pool_slots": wl.MIXED.n_slots,
+                "layers": 1, "heads": self.H, "head_size": self.N,
+                "decode_slots": wl.MIXED_DECODE_B, "prefill_seqs": wl.MIXED_PREFILL_SEQS,
+                "prefill_tokens": self.total, "verb_slots": wl.MIXED_VERB_N,
+                "state_dtype": "f32", "input_dtype": "bf16", "output_dtype": "f32"}
+
+    def oracle_sample(self, frac_target: float):
+        """Sample of the step for the CPU oracle: every decode row and prefill
+        sequence on a subset of the (independent) heads; below one head, also
+        the first rows and sequences only."""
+        return _head_sample(self.H, frac_target, wl.MIXED_DECODE_B, self.lengths,
+                            self.tokens_per_step)
+
+
+def _head_sample(H, frac_target, n_rows, lengths, tokens_per_step, layers=1):
+    n_heads = int(min(H, max(1, round(frac_target * H))))
+    sub = min(1.0, frac_target * H) if n_heads == 1 else 1.0
+    n_dec = int(max(1 if n_rows else 0, round(n_rows * sub))) if n_rows else 0
+    lens = np.asarray(lengths if lengths is not None else [], dtype=np.int64)
+    if len(lens) and sub < 1.0:
+        budget = max(1.0, lens.sum() * sub)
+        csum = np.cumsum(lens)
+        n_seq = max(1, int(np.searchsorted(csum, budget, side="right")))
+        lens = lens[:n_seq]
+    toks = n_dec * layers + int(lens.sum())
+    frac = (toks / float(tokens_per_step)) * (n_heads / float(H))
+    desc = (f"{n_heads} of {H} heads; {n_dec} of {n_rows} decode rows"
+            + (f" x {layers} layers" if layers > 1 else "")
+            + (f"; {len(lens)} prefill sequences ({int(lens.sum())} tokens)" if len(lens) else "")
+            + f"; step time scaled by the work fraction {frac:.5f}")
+    return {"heads": n_heads, "decode_rows": n_dec, "layers": layers,
+            "prefill_lengths": lens, "frac": frac, "desc": desc}
+
+
+class Decode12(Workload):
+    name = wl.DECODE_12L.name
+
+    def __init__(self, torch, device):
+        from rwkv_wkv_gb300 import Pool
+        W = wl.DECODE_12L
+        self.torch, self.W = torch, W
+        self.H, self.N, self.L = W.H, W.N, W.n_layers
+        self.B = 256
+        self.pool = Pool(W.n_layers, W.H, W.n_slots, device=device)
+        g = torch.Generator(device=device).manual_seed(W.seed)
+        self.pool.states.normal_(0.0, 0.1, generator=g)
+        slots = wl.distinct_slots(W.seed, "decode/slots", self.B, W.n_slots)
+        self.ids = torch.as_tensor(slots.astype(np.int32), device=device)
+        self.ins = [wl.token_inputs_device(W.seed, self.B, W.H, W.N, device, generator_offset=l)
+                    for l in range(self.L)]
+        self.o = [torch.empty(self.B, W.H, W.N, dtype=torch.float32, device=device)
+                  for _ in range(self.L)]
+        self.phases = ["decode"]
+        row = W.H * (2 * HEAD_BYTES_STATE + W.N * 2 * 6 + W.N * 4)
+        self.phase_bytes = {"decode": self.L * self.B * row}
+        self.tokens_per_step = self.L * self.B  # slot-steps (one slot, one layer)
+        self.dominant = "decode"
+        self.launches_per_step = self.L
+
+    def step(self, ev=None):
+        if ev:
+            ev["start"].record()
+        for l in range(self.L):
+            self.pool.decode_step(l, self.ids, *self.ins[l], o=self.o[l])
+        if ev:
+            ev["decode"].record()
+
+    def host_io(self):
+        return [self.ids] + [t for x in self.ins for t in x], list(self.o)
+
+    def config(self):
+        return {"workload": self.W.description, "pool_slots": self.W.n_slots, "layers": self.L,
+                "heads": self.H, "head_size": self.N, "decode_slots": self.B,
+                "state_dtype": "f32", "input_dtype": "bf16", "output_dtype": "f32"}
+
+    def oracle_sample(self, frac_target):
+        return _head_sample(self.H, frac_target, self.B, None, self.tokens_per_step,
+                            layers=self.L)
+
+
+class Sweep(Workload):
+    name = wl.SWEEP_32L.name
+
+    def __init__(self, torch, device, batch):
+        from rwkv_wkv_gb300 import Pool
+        W = wl.SWEEP_32L
+        self.torch, self.W = torch, W
+        self.H, self.N, self.L, self.B = W.H, W.N, W.n_layers, batch
+        self.pool = Pool(W.n_layers, W.H, W.n_slots, device=device)
+        g = torch.Generator(device=device).manual_seed(W.seed)
+        self.pool.states.normal_(0.0, 0.1, generator=g)
+        slots = wl.distinct_slots(W.seed, f"sweep/slots{batch}", batch, W.n_slots)
+        self.ids = torch.as_tensor(slots.astype(np.int32), device=device)
+        self.ins = wl.token_inputs_device(W.seed, batch, W.H, W.N, device)
+        self.o = torch.empty(batch, W.H, W.N, dtype=torch.float32, device=device)
+        self.phases = ["decode"]
+        row = W.H * (2 * HEAD_BYTES_STATE + W.N * 2 * 6 + W.N * 4)
+        self.phase_bytes = {"decode": self.L * self.B * row}
+        self.tokens_per_step = self.L * self.B
+        self.dominant = "decode"
+        self.launches_per_step = self.L
+
+    def step(self, ev=None):
+        if ev:
+            ev["start"].record()
+        for l in range(self.L):
+            self.pool.decode_step(l, self.ids, *self.ins, o=self.o)
+        if ev:
+            ev["decode"].record()
+
+    def host_io(self):
+        return [self.ids] + list(self.ins), [self.o]
+
+    def config(self):
+        return {"workload": self.W.description + f"; batch {self.B}", "pool_slots": self.W.n_slots,
+                "layers": self.L, "heads": self.H, "head_size": self.N, "decode_slots": self.B,
+                "state_bytes_per_slot_layer": self.H * HEAD_BYTES_STATE,
+                "state_dtype": "f32", "input_dtype": "bf16", "output_dtype": "f32"}
+
+    def oracle_sample(self, frac_target):
+        return _head_sample(self.H, frac_target, self.B, None, self.tokens_per_step,
+                            layers=self.L)
+
+
+class Prefill(Workload):
+    name = wl.PREFILL_8x4096.name
+
+    def __init__(self, torch, device):
+        from rwkv_wkv_gb300 import Pool
+        W = wl.PREFILL_8x4096
+        self.torch, self.W = torch, W
+        self.H, self.N = W.H, W.N
+        self.S, self.T = 8, 4096
+        self.total = self.S * self.T
+        self.pool = Pool(1, W.H, W.n_slots, device=device)
+        self.pool.alloc(W.n_slots)
+        self.pool.free(list(range(W.n_slots))[::-1])
+        self.ids = torch.arange(self.S, dtype=torch.int32, device=device)
+        self.cu = torch.as_tensor(wl.cu_seqlens([self.T] * self.S), device=device)
+        self.ins = wl.token_inputs_device(W.seed, self.total, W.H, W.N, device)
+        self.o = torch.empty(self.total, W.H, W.N, dtype=torch.float32, device=device)
+        self.phases = ["create", "prefill"]
+        self.phase_bytes = {"create": self.S * self.pool.slot_bytes,
+                            "prefill": self.total * W.H * (W.N * 2 * 6 + W.N * 4)
+                            + self.S * W.H * 2 * HEAD_BYTES_STATE}
+        self.tokens_per_step = self.total
+        self.dominant = "prefill"
+        self.launches_per_step = 2
+
+    def step(self, ev=None):
+        rec = (lambda name: ev[name].record()) if ev else (lambda name: None)
+        rec("start")
+        created = self.pool.create(self.S)
+        rec("create")
+        self.pool.prefill(0, self.ids, self.cu, *self.ins, o=self.o, max_seqlen=self.T)
+        rec("prefill")
+        self.pool.free(created[::-1])
+
+    def host_io(self):
+        return [self.ids, self.cu] + list(self.ins), [self.o]
+
+    def config(self):
+        return {"workload": self.W.description, "layers": 1, "heads": self.H,
+                "head_size": self.N, "prefill_seqs": self.S, "prefill_tokens": self.total,
+                "chunk": 64, "state_dtype": "f32", "input_dtype": "bf16", "output_dtype": "f32"}
+
+    def oracle_sample(self, frac_target):
+        return _head_sample(self.H, frac_target, 0, np.array([self.T] * self.S),
+                            self.tokens_per_step)
+
+
+def make_workload(args, torch, device):
+    if args.workload == "mixed":
+        return Mixed(torch, device)
+    if args.workload == "decode12":
+        return Decode12(torch, device)
+    if args.workload == "prefill":
+        return Prefill(torch, device)
+    return Sweep(torch, device, args.batch)
+
+
+# ------------------------------------------------------------- oracle timing
+def prepare_oracle_sample(wk, sample, seed=12345):
+    """Seeded host inputs of one oracle sample (drawn once, reused per step)."""
+    H, N, nh = wk.H, wk.N, sample["heads"]
+    heads = list(range(nh))
+    work = []
+    n = sample.get("decode_rows", 0)
+    for l in range(sample.get("layers", 1) if n else 0):
+        ins = wl.token_inputs(seed, f"oracle/dec{l}", n, H, N, dtype="bf16", heads=heads)
+        st = wl.slot_states(seed, "oracle/state", range(n), 1, nh, N)[:, 0]
+        work.append(("decode", st, [ins[k].astype(np.float64) for k in wl.INPUT_NAMES]))
+    lens = sample.get("prefill_lengths")
+    if lens is not None and len(lens):
+        cu = wl.cu_seqlens(lens)
+        ins = wl.token_inputs(seed, "oracle/pre", int(cu[-1]), H, N, dtype="bf16", heads=heads)
+        work.append(("prefill", cu, [ins[k].astype(np.float64) for k in wl.INPUT_NAMES],
+                     np.zeros((len(lens), nh, N, N))))
+    return work
+
+
+def time_oracle_sample(work):
+    """Time the CPU oracle on one prepared sample; returns (seconds, threads)."""
+    import oracle
+    n_threads = os.cpu_count() or 1
+    t_total = 0.0
+    for item in work:
+        t0 = time.perf_counter()
+        if item[0] == "decode":
+            oracle.decode_step(item[1], *item[2], n_threads=n_threads)
+        else:
+            oracle.prefill(item[3], item[1], *item[2], n_threads=n_threads)
+        t_total += time.perf_counter() - t0
+    return t_total, n_threads
+
+
+def sized_sample(wk, seconds):
+    """A sample whose oracle time is about `seconds` (from a one-head probe)."""
+    probe = wk.oracle_sample(1.0 / wk.H)
+    t, _ = time_oracle_sample(prepare_oracle_sample(wk, probe))
+    frac = min(1.0, probe["frac"] * seconds / max(t, 1e-3))
+    sample = wk.oracle_sample(frac)
+    return sample, prepare_oracle_sample(wk, sample)
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args):
+    import torch
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    import rwkv_wkv_gb300 as rw
+    rw.load_library()
+    wk = make_workload(args, torch, device)
+    stream = torch.cuda.current_stream(device)
+    peaks = load_peaks()
+
+    graph = None
+    if args.graph:
+        if args.workload not in ("decode12", "sweep"):
+            raise SystemExit("--graph is offered for the decode-only workloads")
+        wk.step()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            wk.step()
+        torch.cuda.synchronize()
+
+    def one_step(ev=None):
+        if graph is not None:
+            if ev:
+                ev["start"].record()
+            graph.replay()
+            if ev:
+                ev[wk.phases[-1]].record()
+        else:
+            wk.step(ev)
+
+    for _ in range(max(3, args.warmup)):
+        one_step()
+    torch.cuda.synchronize()
+
+    props = torch.cuda.get_device_properties(device)
+    uuid = str(getattr(props, "uuid", "") or "")
+    gpu_id = uuid if uuid.startswith("GPU-") else (f"GPU-{uuid}" if uuid else str(local))
+    clocks = ClockSampler(gpu_id)
+    clocks.wait_first()
+
+    names = ["start"] + wk.phases
+    events = [{n: torch.cuda.Event(enable_timing=True) for n in names}
+              for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    launches0 = rw.launch_count()
+    t_wall0 = time.time()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for k in range(args.steps):
+        one_step(events[k])
+    end.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    launches = rw.launch_count() - launches0
+    if graph is not None:
+        launches = wk.launches_per_step * args.steps
+    clk = clocks.summary(t_wall0, t_wall1)
+    clocks.stop()
+    elapsed = start.elapsed_time(end) / 1e3
+    phase_ms = {}
+    prev = "start"
+    for n in wk.phases:
+        phase_ms[n] = statistics.mean(e[prev].elapsed_time(e[n]) for e in events)
+        prev = n
+    if graph is not None:
+        phase_ms = {wk.phases[-1]: statistics.mean(e["start"].elapsed_time(e[wk.phases[-1]])
+                                                   for e in events)}
+    units = wk.tokens_per_step * args.steps
+    elapsed_max, units_all = aggregate(elapsed, units, world, device)
+    value = units_all / elapsed_max
+
+    hbm = peaks["hbm_gbs"]
+    dom = wk.dominant
+    dom_ms = phase_ms.get(dom, elapsed * 1e3 / args.steps)
+    achieved = wk.phase_bytes[dom] / (dom_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
+                "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                "peak_source": peaks["source"] + " (hbm copy)",
+                "bytes_per_launch": wk.phase_bytes[dom], "ms_per_launch": round(dom_ms, 4),
+                "traffic": None}
+    phases = {}
+    for n in wk.phases:
+        ms = phase_ms.get(n)
+        if ms is None:
+            continue
+        gbs = wk.phase_bytes[n] / (ms / 1e3) / 1e9
+        phases[n] = {"ms": round(ms, 4), "GB_per_s": round(gbs, 1),
+                     "hbm_frac": round(gbs / hbm, 4)}
+    extra = {}
+    if "decode" in phase_ms:
+        rows = wk.phase_bytes["decode"]
+        per_row = wk.H * (2 * HEAD_BYTES_STATE + wk.N * 2 * 6 + wk.N * 4)
+        n_slot_steps = rows // per_row
+        extra["decode"] = {"slot_steps_per_s": round(n_slot_steps / (phase_ms["decode"] / 1e3), 1),
+                           "GB_per_s": phases["decode"]["GB_per_s"],
+                           "hbm_frac": phases["decode"]["hbm_frac"]}
+    if "prefill" in phase_ms:
+        extra["prefill"] = {"tokens_per_s": round(wk.total / (phase_ms["prefill"] / 1e3), 1),
+                            "GB_per_s": phases["prefill"]["GB_per_s"],
+                            "roofline_frac": phases["prefill"]["hbm_frac"],
+                            "bound": "hbm"}
+
+    e2e = None
+    if not args.no_e2e and graph is None:
+        e2e = run_e2e(torch, wk, args, world, device)
+
+    cpu_base = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu_base = cpu_baseline(wk, target_seconds=8.0)
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": max(3, args.warmup),
+        "ms_per_step": round(elapsed_max * 1e3 / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32+bf16", "data": "synthetic",
+        "config": dict(wk.config(), parallelism=f"replicas x{world}" if world > 1 else "1 gpu",
+                       l2="inputs larger than L2 (every step moves > 129 MB)",
+                       graph=bool(graph)),
+        "roofline": roofline, "phases": phases, **extra,
+        "e2e": e2e, "gpu_launches": int(launches), "clocks": clk,
+        "cpu_baseline": cpu_base,
+        "dtype_note": "state, decode arithmetic and outputs float32; prefill contractions "
+                      "bf16 tensor-core operands with float32 accumulation; inputs bf16",
+    }
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return line if rank == 0 else None
+
+
+def run_e2e(torch, wk, args, world, device):
+    """Same steps through the public API with pinned host buffers: every step
+    copies its inputs host->device and its outputs device->host."""
+    ins, outs = wk.host_io()
+    h_ins = [t.cpu().pin_memory() for t in ins]
+    h_outs = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    h2d = sum(t.numel() * t.element_size() for t in ins)
+    d2h = sum(t.numel() * t.element_size() for t in outs)
+    steps = max(3, min(args.steps, 20))
+
+    def step():
+        for d, h in zip(ins, h_ins):
+            d.copy_(h, non_blocking=True)
+        wk.step()
+        for h, d in zip(h_outs, outs):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        step()
+    e.record()
+    torch.cuda.synchronize()
+    elapsed = s.elapsed_time(e) / 1e3
+    elapsed_max, units = aggregate(elapsed, wk.tokens_per_step * steps, world, device)
+    return {"value": round(units / elapsed_max, 1), "unit": "tokens/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "steps": steps, "ms_per_step": round(elapsed_max * 1e3 / steps, 3)}
+
+
+def cpu_baseline(wk, target_seconds=12.0):
+    """The oracle timed on the host cores on a bounded sample of the workload."""
+    sample, work = sized_sample(wk, target_seconds)
+    t, threads = time_oracle_sample(work)
+    step_s = t / sample["frac"]
+    return {"value": round(wk.tokens_per_step / step_s, 1), "unit": "tokens/s",
+            "cores": threads, "kind": "oracle", "seconds": round(t, 2),
+            "sample": sample["desc"]}
+
+
+# ------------------------------------------------------------ reference arm
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    # The oracle needs the workload's shapes only: built without a GPU.
+    wk = _shapes_only(args)
+    per_step = min(5.0, 90.0 / max(1, args.steps + args.warmup))
+    sample, work = sized_sample(wk, per_step)
+    for _ in range(args.warmup):
+        time_oracle_sample(work)
+    runs = [time_oracle_sample(work) for _ in range(args.steps)]
+    times = [t for t, _ in runs]
+    threads = runs[0][1] if runs else (os.cpu_count() or 1)
+    step_s = statistics.mean(times) / sample["frac"]
+    value = wk.tokens_per_step / step_s
+    cfg = wk.config()
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 1),
+            "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(step_s * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": dict(cfg, parallelism="1 host"),
+            "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": threads,
+                             "kind": "oracle", "sample": sample["desc"]},
+            "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def _shapes_only(args):
+    """A workload object carrying shapes and sample plans, with no device state."""
+    class S(Workload):
+        pass
+    s = S()
+    if args.workload == "mixed":
+        plan = wl.mixed_plan()
+        s.H, s.N = wl.MIXED.H, wl.MIXED.N
+        s.lengths = plan["lengths"].astype(np.int64)
+        s.total = int(s.lengths.sum())
+        s.tokens_per_step = wl.MIXED_DECODE_B + s.total
+        s.oracle_sample = lambda f: Mixed.oracle_sample(s, f)
+        s.config = lambda: {"workload": wl.MIXED.description, "pool_slots": wl.MIXED.n_slots,
+                            "layers": 1, "heads": s.H, "head_size": s.N,
+                            "decode_slots": wl.MIXED_DECODE_B,
+                            "prefill_seqs": wl.MIXED_PREFILL_SEQS, "prefill_tokens": s.total,
+                            "verb_slots": wl.MIXED_VERB_N}
+    elif args.workload == "decode12":
+        W = wl.DECODE_12L
+        s.H, s.N, s.L, s.B, s.W = W.H, W.N, W.n_layers, 256, W
+        s.tokens_per_step = s.L * s.B
+        s.oracle_sample = lambda f: Decode12.oracle_sample(s, f)
+        s.config = lambda: {"workload": W.description}
+    elif args.workload == "prefill":
+        W = wl.PREFILL_8x4096
+        s.H, s.N, s.S, s.T, s.W = W.H, W.N, 8, 4096, W
+        s.total = s.S * s.T
+        s.tokens_per_step = s.total
+        s.oracle_sample = lambda f: Prefill.oracle_sample(s, f)
+        s.config = lambda: {"workload": W.description}
+    else:
+        W = wl.SWEEP_32L
+        s.H, s.N, s.L, s.B, s.W = W.H, W.N, W.n_layers, args.batch, W
+        s.tokens_per_step = s.L * s.B
+        s.oracle_sample = lambda f: Sweep.oracle_sample(s, f)
+        s.config = lambda: {"workload": W.description + f"; batch {s.B}"}
+    return s
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

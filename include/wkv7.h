@@ -1,0 +1,247 @@
+/*
+ * libwkv7 -- WKV-7 state-slot engine for one NVIDIA GB300 GPU (sm_103a).
+ *
+ * What it computes.  RWKV-X Architecture, "WKV-7 Kernel (Generalized Delta
+ * Rule)": per layer and head a [head_size x head_size] recurrent state S
+ * ("State is a [head_size, head_size] matrix per head per RWKV-7 layer --
+ * fixed size regardless of sequence length").  With S[i][j] (i = value index,
+ * j = key index) every token does
+ *
+ *     h = S a;   S <- S diag(w) + h b^T + v k^T;   o = S r
+ *
+ * (decay, delta-rule term, key-value write, readout after the update).  The
+ * delta term uses h = S a on the state before the decay and the vector b,
+ * i.e. S <- S (diag(w) + a b^T) + v k^T.
+ *
+ * How state is held.  "wkvm: state-slot inference for RWKV, GDN and Mamba
+ * hybrids", section "The allocation unit wkvm changes": the allocation unit is
+ * a fixed-size per-request state slot, and the verbs are create, snapshot,
+ * fork and resume (restore).  A pool owns n_slots live slots and n_snapshots
+ * parked copies.  One slot holds the states of every layer and head:
+ *
+ *     slot layout  [layer][head][i][j]  float32, row-major, contiguous
+ *     slot bytes   n_layers * n_heads * head_size^2 * 4
+ *     pool layout  [slot][layer][head][i][j]; snapshots use the same layout
+ *
+ * Token inputs are packed [rows][n_heads][head_size] (row = batch entry for
+ * decode, token for prefill), contiguous, float32 or bf16; outputs o are
+ * float32 with the same shape.
+ *
+ * Conventions for every call.
+ *   - All pointers named *_dev and every tensor argument are device pointers
+ *     owned by the caller; the library never frees them.  The pool owns its
+ *     state buffer unless the caller supplied one at creation.
+ *   - Calls that take a cudaStream_t are asynchronous on that stream and never
+ *     synchronise, except wkv7_get_device_status.
+ *   - Host-checkable faults (NULL pointers, counts, layer range, dtype, head
+ *     size) return an error before anything is launched; the pool is left
+ *     untouched.
+ *   - Faults only the device can see (a slot id out of range inside a device
+ *     array, inconsistent cu_seqlens) make the kernel skip that unit and
+ *     record a code in the pool's sticky device status word (WKV7_DEV_*),
+ *     read with wkv7_get_device_status.  Kernels never trap or assert.
+ *   - Slot ids within one call must be distinct, and a call's source and
+ *     destination sets must not overlap; violating this is a data race whose
+ *     result is undefined (not detected on the fast path).
+ *   - Only head_size == 64 is implemented; other sizes return
+ *     WKV7_ERR_UNSUPPORTED.
+ */
+#ifndef WKV7_H
+#define WKV7_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define WKV7_VERSION 1
+
+typedef struct wkv7_pool wkv7_pool; /* opaque, owned by the library */
+
+typedef enum {
+    WKV7_OK = 0,
+    WKV7_ERR_INVALID_ARG = 1,   /* NULL pointer, negative count, bad layer/dtype */
+    WKV7_ERR_BAD_SLOT = 2,      /* host-side id not in range or not allocated */
+    WKV7_ERR_DUP_SLOT = 3,      /* the same id twice in one host-side list */
+    WKV7_ERR_POOL_FULL = 4,     /* fewer free slots/snapshots than requested */
+    WKV7_ERR_BAD_SEQLENS = 5,   /* host-checkable sequence sizes are inconsistent */
+    WKV7_ERR_CUDA = 6,          /* a CUDA runtime call failed; see wkv7_last_error */
+    WKV7_ERR_UNSUPPORTED = 7,   /* head_size != 64, or dtype not offered by this call */
+    WKV7_ERR_DEVICE_STATUS = 8, /* a kernel recorded a fault; code in *code_out */
+    WKV7_ERR_TIMEOUT = 9,       /* the stream did not finish within the limit */
+    WKV7_ERR_NO_MEMORY = 10     /* host or device allocation failed */
+} wkv7_status;
+
+typedef enum { WKV7_F32 = 0, WKV7_BF16 = 1 } wkv7_dtype;
+
+/* Codes of the sticky device status word (first fault wins). */
+#define WKV7_DEV_OK 0
+#define WKV7_DEV_BAD_SLOT 1     /* a device slot/snapshot id was out of range */
+#define WKV7_DEV_BAD_SEQLENS 2  /* cu_seqlens not monotone, out of range or longer than max_seqlen */
+#define WKV7_DEV_WAIT_TIMEOUT 3 /* a bounded in-kernel wait gave up; outputs of that unit are invalid */
+#define WKV7_DEV_DECAY_RANGE 4  /* chunked prefill: decay over half a chunk beyond the float range */
+
+typedef struct {
+    int32_t n_layers;    /* >= 1 */
+    int32_t n_heads;     /* >= 1 */
+    int32_t head_size;   /* must be 64 */
+    int32_t n_slots;     /* >= 1, live slots */
+    int32_t n_snapshots; /* >= 0, parked copies */
+    void *device_buffer; /* NULL: the library allocates (cudaMalloc) and frees.
+                            Else a caller-owned device buffer of at least
+                            wkv7_pool_required_bytes() bytes, 256-byte aligned,
+                            that must outlive the pool. */
+    size_t buffer_bytes; /* size of device_buffer (ignored when it is NULL) */
+} wkv7_pool_desc;
+
+/* ---------------------------------------------------------------- pool ---- */
+
+/* Bytes of device memory a pool with this description needs: a 256-byte
+ * header (the device status word) followed by the slot and snapshot states.
+ * Returns 0 for an invalid description. */
+size_t wkv7_pool_required_bytes(const wkv7_pool_desc *desc);
+
+/* Create a pool.  With a caller buffer no CUDA call is made (slot contents are
+ * whatever the buffer holds until wkv7_slot_create zeroes them) except that
+ * the caller must have zeroed the first 256 bytes (the status word).  With
+ * device_buffer == NULL the library allocates on the current device and zeroes
+ * the status word.  Every slot and snapshot starts free.
+ * Errors: INVALID_ARG, UNSUPPORTED (head_size), NO_MEMORY, CUDA. */
+wkv7_status wkv7_pool_create(const wkv7_pool_desc *desc, wkv7_pool **out);
+
+/* Destroy a pool; frees the device buffer only if the library allocated it.
+ * The caller must make sure no work using the pool is still in flight. */
+wkv7_status wkv7_pool_destroy(wkv7_pool *pool);
+
+/* Copy the pool's description (device_buffer = the buffer actually used). */
+wkv7_status wkv7_pool_get_desc(const wkv7_pool *pool, wkv7_pool_desc *out);
+
+/* Bytes of one slot (and of one snapshot): n_layers*n_heads*head_size^2*4. */
+size_t wkv7_slot_bytes(const wkv7_pool *pool);
+
+/* Device address of the float32 [n_heads][head_size][head_size] state of
+ * (slot, layer), or of a snapshot.  For tests and for initialising states.
+ * Errors: INVALID_ARG, BAD_SLOT (index out of range; allocation state is not
+ * checked). */
+wkv7_status wkv7_pool_state_ptr(wkv7_pool *pool, int32_t slot, int32_t layer, float **dev_ptr);
+wkv7_status wkv7_pool_snapshot_ptr(wkv7_pool *pool, int32_t snap, int32_t layer, float **dev_ptr);
+
+/* ------------------------------------------------ slot table (host only) -- */
+/* The slot table is host bookkeeping: which ids are handed out.  These calls
+ * launch nothing.  Recurrent-state slots are reserved up front, separately
+ * from anything else ("Virtual Memory for KV Cache and Model Weights": hybrid
+ * recurrent-state slots are reserved separately and must be available at
+ * admission), so running out is reported, never grown. */
+
+/* Hand out n free slot ids into ids_out[n] (host array).  All or nothing:
+ * POOL_FULL if fewer than n are free. */
+wkv7_status wkv7_slot_alloc(wkv7_pool *pool, int32_t n, int32_t *ids_out);
+/* Return n slot ids.  All or nothing: BAD_SLOT if any id is out of range or
+ * not allocated, DUP_SLOT if an id repeats. */
+wkv7_status wkv7_slot_free(wkv7_pool *pool, int32_t n, const int32_t *ids);
+wkv7_status wkv7_snapshot_alloc(wkv7_pool *pool, int32_t n, int32_t *ids_out);
+wkv7_status wkv7_snapshot_free(wkv7_pool *pool, int32_t n, const int32_t *ids);
+/* Number of free slots / snapshots (or -1 for a NULL pool). */
+int32_t wkv7_slot_count_free(const wkv7_pool *pool);
+int32_t wkv7_snapshot_count_free(const wkv7_pool *pool);
+/* *out = 1 if the slot id is allocated, else 0.  BAD_SLOT if out of range. */
+wkv7_status wkv7_slot_is_allocated(const wkv7_pool *pool, int32_t slot, int32_t *out);
+
+/* ------------------------------------------------------------ verbs ----- */
+
+/* create: hand out n free slots (ids_out, host array) and zero their state on
+ * `stream` -- the verb "create" of the state-slot engine ("The allocation
+ * unit wkvm changes"), with the zeroing of a fresh state as in RWKV-X
+ * Architecture, "Dual State" (the reset zeros the recurrent state).
+ * Errors: INVALID_ARG, POOL_FULL (nothing allocated), CUDA (ids are returned
+ * to the free list). */
+wkv7_status wkv7_slot_create(wkv7_pool *pool, int32_t n, int32_t *ids_out, cudaStream_t stream);
+
+/* reset: zero the states of n slots given as a device id array (no table
+ * change).  Out-of-range ids are skipped and flagged WKV7_DEV_BAD_SLOT. */
+wkv7_status wkv7_slot_reset(wkv7_pool *pool, const int32_t *slot_ids_dev, int32_t n,
+                            cudaStream_t stream);
+
+/* snapshot: copy slot slot_ids_dev[i] -> snapshot snap_ids_dev[i], i < n, bit
+ * for bit.  restore (the verb "resume"): snapshot -> slot.  fork: slot
+ * src_ids_dev[i] -> slot dst_ids_dev[i].  ("The allocation unit wkvm
+ * changes": a fixed-size slot can be copied, parked and restored cheaply.)
+ * Whole-slot copies of every layer and head.  Out-of-range ids are skipped and
+ * flagged WKV7_DEV_BAD_SLOT.  n == 0 is a no-op. */
+wkv7_status wkv7_slot_snapshot(wkv7_pool *pool, const int32_t *slot_ids_dev,
+                               const int32_t *snap_ids_dev, int32_t n, cudaStream_t stream);
+wkv7_status wkv7_slot_restore(wkv7_pool *pool, const int32_t *snap_ids_dev,
+                              const int32_t *slot_ids_dev, int32_t n, cudaStream_t stream);
+wkv7_status wkv7_slot_fork(wkv7_pool *pool, const int32_t *src_ids_dev,
+                           const int32_t *dst_ids_dev, int32_t n, cudaStream_t stream);
+
+/* --------------------------------------------------------- recurrence ---- */
+
+/* decode: one token for each of n slots at one layer.  For b < n and every
+ * head h, the state at (slot_ids_dev[b], layer, h) takes one step of the
+ * recurrence with inputs x[b][h][:] (x = r, w, k, v, a, b; [n][n_heads][64],
+ * dtype in_dtype) and o[b][h][:] (float32) receives the readout.  The state is
+ * read once and written once.  Errors: INVALID_ARG (including n > n_slots),
+ * UNSUPPORTED, CUDA.  Device: WKV7_DEV_BAD_SLOT for an out-of-range id (that
+ * row's state and o are untouched). */
+wkv7_status wkv7_decode_step(wkv7_pool *pool, int32_t layer, const int32_t *slot_ids_dev,
+                             int32_t n, wkv7_dtype in_dtype, const void *r, const void *w,
+                             const void *k, const void *v, const void *a, const void *b,
+                             float *o, cudaStream_t stream);
+
+/* prefill: n_seqs sequences packed back to back (RWKV-X Architecture, "What
+ * Was Stripped": the batch forward is the prefill path).  Sequence s holds
+ * tokens cu_seqlens_dev[s] .. cu_seqlens_dev[s+1]-1 of the packed inputs
+ * [total_tokens][n_heads][64] (bf16) and starts from the state at
+ * (slot_ids_dev[s], layer); the slot receives the state after its last token
+ * and o[t][h][:] (float32) the readout of every token.  The result equals
+ * the token-by-token recurrence up to rounding; it is computed in chunks of
+ * 64 tokens anchored at each sequence's first token, with bf16 tensor-core
+ * operands and a float32 state carried between chunks.  max_seqlen bounds
+ * every sequence length.  Errors: INVALID_ARG, UNSUPPORTED (in_dtype must be
+ * WKV7_BF16), CUDA.  Device: WKV7_DEV_BAD_SLOT, WKV7_DEV_BAD_SEQLENS (that
+ * sequence is skipped), WKV7_DEV_DECAY_RANGE, WKV7_DEV_WAIT_TIMEOUT. */
+wkv7_status wkv7_prefill(wkv7_pool *pool, int32_t layer, const int32_t *slot_ids_dev,
+                         const int32_t *cu_seqlens_dev, int32_t n_seqs, int32_t total_tokens,
+                         int32_t max_seqlen, wkv7_dtype in_dtype, const void *r,
+                         const void *w, const void *k, const void *v, const void *a,
+                         const void *b, float *o, cudaStream_t stream);
+
+/* prefill_sequential: the same contract as wkv7_prefill, computed token by
+ * token in float32 on the CUDA cores (no chunking, no tensor cores; accepts
+ * WKV7_F32 or WKV7_BF16 inputs).  Slower; exact to float32 rounding. */
+wkv7_status wkv7_prefill_sequential(wkv7_pool *pool, int32_t layer,
+                                    const int32_t *slot_ids_dev,
+                                    const int32_t *cu_seqlens_dev, int32_t n_seqs,
+                                    int32_t total_tokens, int32_t max_seqlen,
+                                    wkv7_dtype in_dtype, const void *r, const void *w,
+                                    const void *k, const void *v, const void *a,
+                                    const void *b, float *o, cudaStream_t stream);
+
+/* ------------------------------------------------------------- status ---- */
+
+/* Wait (at most timeout_ms, polling; <= 0 means 10000) for the work queued on
+ * `stream`, then read and clear the pool's device status word into *code_out
+ * (WKV7_DEV_*).  Returns WKV7_ERR_DEVICE_STATUS when the code is non-zero,
+ * WKV7_ERR_TIMEOUT when the stream did not finish in time (the word is left
+ * as it is), WKV7_ERR_CUDA on a CUDA error. */
+wkv7_status wkv7_get_device_status(wkv7_pool *pool, cudaStream_t stream, int32_t timeout_ms,
+                                   int32_t *code_out);
+
+/* Static text for a status code. */
+const char *wkv7_status_string(wkv7_status status);
+/* Text of the last CUDA error seen by this thread inside the library. */
+const char *wkv7_last_error(void);
+/* Number of kernels this process has launched through the library. */
+uint64_t wkv7_launch_count(void);
+int32_t wkv7_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WKV7_H */

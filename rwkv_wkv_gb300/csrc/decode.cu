@@ -1,0 +1,101 @@
+// Batched single-token WKV-7 decode over indirected state slots.
+//
+// RWKV-X Architecture, "WKV-7 Kernel (Generalized Delta Rule)": per head and
+// token, h = S a; S <- S diag(w) + h b^T + v k^T; o = S r.  One CTA advances
+// one (batch row, head) unit: it streams that head's 64x64 float32 state
+// (16 KiB) from HBM into registers once, applies the step, streams it back and
+// writes the 64 readouts.  The kernel is bound by HBM bandwidth: per unit it
+// moves 32 KiB of state against ~37 kFLOP.
+//
+// Thread mapping (256 threads): thread t holds the float4 at byte offset
+// 16*t + 4096*m (m = 0..3) of the state, i.e. key columns 4*(t%16)..+3 of
+// value rows t/16 + 16*m.  Each load/store instruction of the CTA covers 4 KiB
+// of contiguous memory.  A row's 64 columns sit in one half-warp, so both
+// row reductions (S a before the update, S' r after it) are 4-level xor
+// shuffles inside the half-warp, and the state never touches shared memory.
+#include "device_common.cuh"
+#include "wkv7_internal.h"
+
+namespace wkv7 {
+namespace {
+
+template <bool BF16>
+__global__ void __launch_bounds__(256) decode_kernel(DecodeArgs p) {
+    const int H = p.lv.n_heads;
+    const int unit = blockIdx.x;
+    const int bi = unit / H;
+    const int h = unit - bi * H;
+    const int slot = __ldg(p.slot_ids + bi);
+    if (slot < 0 || slot >= p.lv.n_slots) {
+        if (threadIdx.x == 0) flag_status(p.lv.status, WKV7_DEV_BAD_SLOT);
+        return;
+    }
+    float *S = p.lv.states + static_cast<size_t>(slot) * p.lv.slot_stride + p.lv.layer_off +
+               static_cast<size_t>(h) * kHeadFloats;
+    const int tid = threadIdx.x;
+    const int c = (tid & 15) * 4;  // first key column held by this thread
+    const int row0 = tid >> 4;     // value rows row0 + 16*m
+
+    float4 s[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+        s[m] = __ldcs(reinterpret_cast<const float4 *>(S + (row0 + 16 * m) * kHeadSize + c));
+
+    const size_t io = static_cast<size_t>(unit) * kHeadSize;
+    const float4 a4 = load4<BF16>(p.in.a, io + c);
+    const float4 w4 = load4<BF16>(p.in.w, io + c);
+    const float4 b4 = load4<BF16>(p.in.b, io + c);
+    const float4 k4 = load4<BF16>(p.in.k, io + c);
+    const float4 r4 = load4<BF16>(p.in.r, io + c);
+    float vv[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) vv[m] = load1<BF16>(p.in.v, io + row0 + 16 * m);
+
+    // delta read on the old state: h_i = sum_j S_ij a_j
+    float hs[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) hs[m] = dot4(s[m], a4);
+#pragma unroll
+    for (int off = 8; off >= 1; off >>= 1)
+#pragma unroll
+        for (int m = 0; m < 4; ++m) hs[m] += __shfl_xor_sync(0xffffffffu, hs[m], off);
+
+    // decay, delta write, kv write; then the readout on the new state
+    float os[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        s[m].x = fmaf(s[m].x, w4.x, fmaf(hs[m], b4.x, vv[m] * k4.x));
+        s[m].y = fmaf(s[m].y, w4.y, fmaf(hs[m], b4.y, vv[m] * k4.y));
+        s[m].z = fmaf(s[m].z, w4.z, fmaf(hs[m], b4.z, vv[m] * k4.z));
+        s[m].w = fmaf(s[m].w, w4.w, fmaf(hs[m], b4.w, vv[m] * k4.w));
+        os[m] = dot4(s[m], r4);
+    }
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+        __stcs(reinterpret_cast<float4 *>(S + (row0 + 16 * m) * kHeadSize + c), s[m]);
+#pragma unroll
+    for (int off = 8; off >= 1; off >>= 1)
+#pragma unroll
+        for (int m = 0; m < 4; ++m) os[m] += __shfl_xor_sync(0xffffffffu, os[m], off);
+    if ((tid & 15) == 0) {
+#pragma unroll
+        for (int m = 0; m < 4; ++m) p.in.o[io + row0 + 16 * m] = os[m];
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s, int *launches) {
+    const long long units = static_cast<long long>(a.n) * a.lv.n_heads;
+    if (units <= 0) return cudaSuccess;
+    if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
+    dim3 grid(static_cast<unsigned>(units));
+    if (a.in.bf16)
+        decode_kernel<true><<<grid, 256, 0, s>>>(a);
+    else
+        decode_kernel<false><<<grid, 256, 0, s>>>(a);
+    ++*launches;
+    return cudaGetLastError();
+}
+
+}  // namespace wkv7

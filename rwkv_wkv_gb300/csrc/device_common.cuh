@@ -1,0 +1,63 @@
+// Small device helpers shared by the WKV-7 kernels.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "wkv7.h"
+
+namespace wkv7 {
+
+// Record a device fault in the sticky status word; the first fault wins.
+__device__ __forceinline__ void flag_status(int *status, int code) {
+    atomicCAS(status, 0, code);
+}
+
+// bf16 bits -> float (exact).
+__device__ __forceinline__ float bf16_lo(uint32_t pair) { return __uint_as_float(pair << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t pair) { return __uint_as_float(pair & 0xFFFF0000u); }
+
+// Load 4 consecutive input values at element offset `off` as floats.
+template <bool BF16>
+__device__ __forceinline__ float4 load4(const void *p, size_t off) {
+    if constexpr (BF16) {
+        uint2 u = __ldg(reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(p) + off));
+        return make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
+    } else {
+        return __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(p) + off));
+    }
+}
+
+// Load one input value at element offset `off` as float.
+template <bool BF16>
+__device__ __forceinline__ float load1(const void *p, size_t off) {
+    if constexpr (BF16) {
+        uint16_t u = __ldg(static_cast<const unsigned short *>(p) + off);
+        return __uint_as_float(static_cast<uint32_t>(u) << 16);
+    } else {
+        return __ldg(static_cast<const float *>(p) + off);
+    }
+}
+
+// Load 8 consecutive input values at element offset `off` (16-byte aligned for
+// bf16, 32-byte for float) as floats.
+template <bool BF16>
+__device__ __forceinline__ void load8(const void *p, size_t off, float *x) {
+    if constexpr (BF16) {
+        uint4 u = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p) + off));
+        x[0] = bf16_lo(u.x); x[1] = bf16_hi(u.x); x[2] = bf16_lo(u.y); x[3] = bf16_hi(u.y);
+        x[4] = bf16_lo(u.z); x[5] = bf16_hi(u.z); x[6] = bf16_lo(u.w); x[7] = bf16_hi(u.w);
+    } else {
+        const float4 *q = reinterpret_cast<const float4 *>(static_cast<const float *>(p) + off);
+        float4 a = __ldg(q), b = __ldg(q + 1);
+        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+        x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+    }
+}
+
+__device__ __forceinline__ float dot4(float4 a, float4 b) {
+    return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
+}
+
+}  // namespace wkv7

@@ -1,0 +1,77 @@
+// Internal interface between the C-ABI layer (capi.cpp) and the kernels.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace wkv7 {
+
+constexpr int kHeadSize = 64;
+constexpr int kHeadFloats = kHeadSize * kHeadSize;
+
+// One layer of a pool, as the recurrence kernels see it.
+struct LayerView {
+    float *states;          // pool state base (slot 0, layer 0, head 0)
+    long long slot_stride;  // floats per slot
+    long long layer_off;    // floats from a slot's start to this layer
+    int n_slots;
+    int n_heads;
+    int *status;            // sticky device status word
+};
+
+struct TokenInputs {
+    const void *r, *w, *k, *v, *a, *b;
+    bool bf16;
+    float *o;
+};
+
+struct DecodeArgs {
+    LayerView lv;
+    const int *slot_ids;
+    int n;
+    TokenInputs in;
+};
+
+struct PrefillArgs {
+    LayerView lv;
+    const int *slot_ids;
+    const int *cu_seqlens;
+    int n_seqs;
+    int total_tokens;
+    int max_seqlen;
+    TokenInputs in;
+};
+
+// Whole-slot copies: dst[dst_ids[i]] <- src[src_ids[i]], slot_floats each.
+struct CopyArgs {
+    float *dst;
+    const float *src;
+    const int *dst_ids;
+    const int *src_ids;
+    int n;
+    int n_dst;
+    int n_src;
+    long long slot_floats;
+    int *status;
+};
+
+constexpr int kZeroIdsPerLaunch = 512;
+struct ZeroIds {
+    int ids[kZeroIdsPerLaunch];
+};
+
+cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s, int *launches);
+cudaError_t launch_prefill_sequential(const PrefillArgs &a, cudaStream_t s, int *launches);
+cudaError_t launch_prefill_chunked(const PrefillArgs &a, cudaStream_t s, int *launches);
+cudaError_t launch_slot_copy(const CopyArgs &a, cudaStream_t s, int *launches);
+// Zero slots listed in a device id array.
+cudaError_t launch_slot_zero_dev(float *states, int n_slots, long long slot_floats,
+                                 const int *ids_dev, int n, int *status, cudaStream_t s,
+                                 int *launches);
+// Zero slots listed on the host (ids passed by value, in batches).
+cudaError_t launch_slot_zero_host(float *states, int n_slots, long long slot_floats,
+                                  const int *ids_host, int n, int *status, cudaStream_t s,
+                                  int *launches);
+
+}  // namespace wkv7

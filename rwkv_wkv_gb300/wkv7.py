@@ -1,0 +1,306 @@
+"""Python binding of libwkv7 (ctypes).  Argument marshalling only: every step
+of the recurrence and of the slot verbs runs in the library's CUDA kernels.
+PyTorch supplies device memory (the pool buffer, the caller's tensors) and the
+current CUDA stream; nothing here computes.
+
+The C contract (layouts, ownership, errors) is documented in include/wkv7.h.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libwkv7.so")
+
+F32, BF16 = 0, 1
+DEV_OK, DEV_BAD_SLOT, DEV_BAD_SEQLENS, DEV_WAIT_TIMEOUT, DEV_DECAY_RANGE = 0, 1, 2, 3, 4
+HEAD_SIZE = 64
+_HEADER_BYTES = 256
+
+STATUS_NAMES = {
+    0: "OK", 1: "ERR_INVALID_ARG", 2: "ERR_BAD_SLOT", 3: "ERR_DUP_SLOT", 4: "ERR_POOL_FULL",
+    5: "ERR_BAD_SEQLENS", 6: "ERR_CUDA", 7: "ERR_UNSUPPORTED", 8: "ERR_DEVICE_STATUS",
+    9: "ERR_TIMEOUT", 10: "ERR_NO_MEMORY",
+}
+
+
+class Wkv7Error(RuntimeError):
+    def __init__(self, status: int, what: str, detail: str = ""):
+        self.status = status
+        self.name = STATUS_NAMES.get(status, str(status))
+        msg = f"{what}: {self.name}"
+        if detail:
+            msg += f" ({detail})"
+        super().__init__(msg)
+
+
+class PoolDesc(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int32), ("n_heads", ctypes.c_int32),
+                ("head_size", ctypes.c_int32), ("n_slots", ctypes.c_int32),
+                ("n_snapshots", ctypes.c_int32), ("device_buffer", ctypes.c_void_p),
+                ("buffer_bytes", ctypes.c_size_t)]
+
+
+# name -> (restype, argtypes)
+_P, _I32, _VP = ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p
+_I32P = ctypes.POINTER(ctypes.c_int32)
+_SIGS = {
+    "wkv7_pool_required_bytes": (ctypes.c_size_t, [ctypes.POINTER(PoolDesc)]),
+    "wkv7_pool_create": (ctypes.c_int, [ctypes.POINTER(PoolDesc), ctypes.POINTER(ctypes.c_void_p)]),
+    "wkv7_pool_destroy": (ctypes.c_int, [_P]),
+    "wkv7_pool_get_desc": (ctypes.c_int, [_P, ctypes.POINTER(PoolDesc)]),
+    "wkv7_slot_bytes": (ctypes.c_size_t, [_P]),
+    "wkv7_pool_state_ptr": (ctypes.c_int, [_P, _I32, _I32, ctypes.POINTER(ctypes.c_void_p)]),
+    "wkv7_pool_snapshot_ptr": (ctypes.c_int, [_P, _I32, _I32, ctypes.POINTER(ctypes.c_void_p)]),
+    "wkv7_slot_alloc": (ctypes.c_int, [_P, _I32, _I32P]),
+    "wkv7_slot_free": (ctypes.c_int, [_P, _I32, _I32P]),
+    "wkv7_snapshot_alloc": (ctypes.c_int, [_P, _I32, _I32P]),
+    "wkv7_snapshot_free": (ctypes.c_int, [_P, _I32, _I32P]),
+    "wkv7_slot_count_free": (ctypes.c_int32, [_P]),
+    "wkv7_snapshot_count_free": (ctypes.c_int32, [_P]),
+    "wkv7_slot_is_allocated": (ctypes.c_int, [_P, _I32, _I32P]),
+    "wkv7_slot_create": (ctypes.c_int, [_P, _I32, _I32P, _VP]),
+    "wkv7_slot_reset": (ctypes.c_int, [_P, _VP, _I32, _VP]),
+    "wkv7_slot_snapshot": (ctypes.c_int, [_P, _VP, _VP, _I32, _VP]),
+    "wkv7_slot_restore": (ctypes.c_int, [_P, _VP, _VP, _I32, _VP]),
+    "wkv7_slot_fork": (ctypes.c_int, [_P, _VP, _VP, _I32, _VP]),
+    "wkv7_decode_step": (ctypes.c_int, [_P, _I32, _VP, _I32, ctypes.c_int] + [_VP] * 7 + [_VP]),
+    "wkv7_prefill": (ctypes.c_int, [_P, _I32, _VP, _VP, _I32, _I32, _I32, ctypes.c_int]
+                     + [_VP] * 7 + [_VP]),
+    "wkv7_prefill_sequential": (ctypes.c_int, [_P, _I32, _VP, _VP, _I32, _I32, _I32, ctypes.c_int]
+                                + [_VP] * 7 + [_VP]),
+    "wkv7_get_device_status": (ctypes.c_int, [_P, _VP, _I32, _I32P]),
+    "wkv7_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "wkv7_last_error": (ctypes.c_char_p, []),
+    "wkv7_launch_count": (ctypes.c_uint64, []),
+    "wkv7_version": (ctypes.c_int32, []),
+}
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libwkv7.so; raises if it has not been built.  There is no fallback."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with `python -m rwkv_wkv_gb300.build` "
+                          "(there is no fallback implementation)")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGS.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = lib
+    return lib
+
+
+def exported_symbols() -> list[str]:
+    return list(_SIGS)
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        detail = ""
+        if status == 6:
+            detail = load_library().wkv7_last_error().decode(errors="replace")
+        raise Wkv7Error(status, what, detail)
+
+
+def launch_count() -> int:
+    return int(load_library().wkv7_launch_count())
+
+
+def _stream_handle(stream, device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return int(stream.cuda_stream)
+
+
+def _ids_host(ids) -> ctypes.Array:
+    vals = [int(x) for x in ids]
+    return (ctypes.c_int32 * max(1, len(vals)))(*vals), len(vals)
+
+
+def _dev_i32(t: torch.Tensor, name: str, device) -> int:
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.int32 or not t.is_cuda:
+        raise TypeError(f"{name} must be an int32 CUDA tensor")
+    if t.device != device or not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous on {device}")
+    return t.data_ptr()
+
+
+class Pool:
+    """A pool of fixed-size WKV-7 state slots on one GPU.
+
+    States live in one torch-allocated device buffer: ``states`` is a float32
+    view [n_slots, n_layers, n_heads, 64, 64] and ``snapshots`` the same for
+    the parked copies (S[i][j]: i = value row, j = key column).
+    """
+
+    def __init__(self, n_layers: int, n_heads: int, n_slots: int, n_snapshots: int = 0,
+                 head_size: int = HEAD_SIZE, device=None):
+        self._lib = load_library()
+        self.device = torch.device("cuda", torch.cuda.current_device()) if device is None \
+            else torch.device(device)
+        self.n_layers, self.n_heads, self.head_size = n_layers, n_heads, head_size
+        self.n_slots, self.n_snapshots = n_slots, n_snapshots
+        desc = PoolDesc(n_layers, n_heads, head_size, n_slots, n_snapshots, None, 0)
+        nbytes = self._lib.wkv7_pool_required_bytes(ctypes.byref(desc))
+        if nbytes == 0:
+            raise Wkv7Error(1, "Pool", "invalid description")
+        self.buffer = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+        self.buffer[:_HEADER_BYTES].zero_()
+        desc.device_buffer = self.buffer.data_ptr()
+        desc.buffer_bytes = nbytes
+        handle = ctypes.c_void_p()
+        _check(self._lib.wkv7_pool_create(ctypes.byref(desc), ctypes.byref(handle)), "pool_create")
+        self._h = handle
+        self.slot_bytes = int(self._lib.wkv7_slot_bytes(self._h))
+        per_slot = self.slot_bytes // 4
+        body = self.buffer[_HEADER_BYTES:].view(torch.float32)
+        shape = (n_layers, n_heads, head_size, head_size)
+        self.states = body[: n_slots * per_slot].view(n_slots, *shape)
+        self.snapshots = body[n_slots * per_slot:(n_slots + n_snapshots) * per_slot].view(
+            n_snapshots, *shape)
+
+    # -------------------------------------------------------------- lifetime
+    def close(self):
+        if getattr(self, "_h", None):
+            _check(self._lib.wkv7_pool_destroy(self._h), "pool_destroy")
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    # ------------------------------------------------------------ slot table
+    def alloc(self, n: int) -> list[int]:
+        arr = (ctypes.c_int32 * max(1, n))()
+        _check(self._lib.wkv7_slot_alloc(self._h, n, arr), "slot_alloc")
+        return list(arr[:n])
+
+    def free(self, ids) -> None:
+        arr, n = _ids_host(ids)
+        _check(self._lib.wkv7_slot_free(self._h, n, arr), "slot_free")
+
+    def snapshot_alloc(self, n: int) -> list[int]:
+        arr = (ctypes.c_int32 * max(1, n))()
+        _check(self._lib.wkv7_snapshot_alloc(self._h, n, arr), "snapshot_alloc")
+        return list(arr[:n])
+
+    def snapshot_free(self, ids) -> None:
+        arr, n = _ids_host(ids)
+        _check(self._lib.wkv7_snapshot_free(self._h, n, arr), "snapshot_free")
+
+    def n_free(self) -> int:
+        return int(self._lib.wkv7_slot_count_free(self._h))
+
+    def n_snapshots_free(self) -> int:
+        return int(self._lib.wkv7_snapshot_count_free(self._h))
+
+    def is_allocated(self, slot: int) -> bool:
+        out = ctypes.c_int32()
+        _check(self._lib.wkv7_slot_is_allocated(self._h, slot, ctypes.byref(out)), "is_allocated")
+        return bool(out.value)
+
+    def state_ptr(self, slot: int, layer: int) -> int:
+        p = ctypes.c_void_p()
+        _check(self._lib.wkv7_pool_state_ptr(self._h, slot, layer, ctypes.byref(p)), "state_ptr")
+        return int(p.value)
+
+    # ----------------------------------------------------------------- verbs
+    def create(self, n: int, stream=None) -> list[int]:
+        arr = (ctypes.c_int32 * max(1, n))()
+        _check(self._lib.wkv7_slot_create(self._h, n, arr, _stream_handle(stream, self.device)),
+               "slot_create")
+        return list(arr[:n])
+
+    def reset(self, slot_ids: torch.Tensor, stream=None) -> None:
+        _check(self._lib.wkv7_slot_reset(self._h, _dev_i32(slot_ids, "slot_ids", self.device),
+                                         slot_ids.numel(), _stream_handle(stream, self.device)),
+               "slot_reset")
+
+    def snapshot(self, slot_ids: torch.Tensor, snap_ids: torch.Tensor, stream=None) -> None:
+        self._pairs("wkv7_slot_snapshot", slot_ids, snap_ids, stream)
+
+    def restore(self, snap_ids: torch.Tensor, slot_ids: torch.Tensor, stream=None) -> None:
+        self._pairs("wkv7_slot_restore", snap_ids, slot_ids, stream)
+
+    def fork(self, src_ids: torch.Tensor, dst_ids: torch.Tensor, stream=None) -> None:
+        self._pairs("wkv7_slot_fork", src_ids, dst_ids, stream)
+
+    def _pairs(self, fn, first, second, stream):
+        if first.numel() != second.numel():
+            raise ValueError("id arrays differ in length")
+        _check(getattr(self._lib, fn)(self._h, _dev_i32(first, "ids", self.device),
+                                      _dev_i32(second, "ids", self.device), first.numel(),
+                                      _stream_handle(stream, self.device)), fn)
+
+    # ------------------------------------------------------------ recurrence
+    def _inputs(self, xs, rows):
+        dt = xs[0].dtype
+        if dt not in (torch.float32, torch.bfloat16):
+            raise TypeError("inputs must be float32 or bfloat16")
+        for x in xs:
+            if x.dtype != dt or x.device != self.device or not x.is_contiguous():
+                raise ValueError("inputs must share one dtype and be contiguous on the pool device")
+            if tuple(x.shape) != (rows, self.n_heads, self.head_size):
+                raise ValueError(f"inputs must be [{rows}, {self.n_heads}, {self.head_size}]")
+        return (BF16 if dt == torch.bfloat16 else F32), [x.data_ptr() for x in xs]
+
+    def _out(self, o, rows):
+        if o is None:
+            return torch.empty(rows, self.n_heads, self.head_size, dtype=torch.float32,
+                               device=self.device)
+        if (o.dtype != torch.float32 or o.device != self.device or not o.is_contiguous()
+                or tuple(o.shape) != (rows, self.n_heads, self.head_size)):
+            raise ValueError("o must be a contiguous float32 [rows, n_heads, 64] tensor")
+        return o
+
+    def decode_step(self, layer: int, slot_ids: torch.Tensor, r, w, k, v, a, b, o=None,
+                    stream=None) -> torch.Tensor:
+        n = slot_ids.numel()
+        dt, ptrs = self._inputs((r, w, k, v, a, b), n)
+        o = self._out(o, n)
+        _check(self._lib.wkv7_decode_step(self._h, layer, _dev_i32(slot_ids, "slot_ids", self.device),
+                                          n, dt, *ptrs, o.data_ptr(),
+                                          _stream_handle(stream, self.device)), "decode_step")
+        return o
+
+    def prefill(self, layer: int, slot_ids: torch.Tensor, cu_seqlens: torch.Tensor, r, w, k, v,
+                a, b, o=None, max_seqlen: int | None = None, stream=None,
+                sequential: bool = False) -> torch.Tensor:
+        total = r.shape[0]
+        dt, ptrs = self._inputs((r, w, k, v, a, b), total)
+        o = self._out(o, total)
+        if cu_seqlens.numel() != slot_ids.numel() + 1:
+            raise ValueError("cu_seqlens must have n_seqs + 1 entries")
+        fn = self._lib.wkv7_prefill_sequential if sequential else self._lib.wkv7_prefill
+        _check(fn(self._h, layer, _dev_i32(slot_ids, "slot_ids", self.device),
+                  _dev_i32(cu_seqlens, "cu_seqlens", self.device), slot_ids.numel(), total,
+                  total if max_seqlen is None else int(max_seqlen), dt, *ptrs, o.data_ptr(),
+                  _stream_handle(stream, self.device)),
+               "prefill_sequential" if sequential else "prefill")
+        return o
+
+    # ---------------------------------------------------------------- status
+    def device_status(self, stream=None, timeout_ms: int = 10000) -> int:
+        code = ctypes.c_int32()
+        st = self._lib.wkv7_get_device_status(self._h, _stream_handle(stream, self.device),
+                                              timeout_ms, ctypes.byref(code))
+        if st not in (0, 8):
+            _check(st, "get_device_status")
+        return int(code.value)

@@ -1,0 +1,44 @@
+"""Shared plumbing for the GPU parity tests: move seeded inputs to the device and
+gather what the oracle needs.  Nothing here computes the recurrence."""
+import numpy as np
+import torch
+
+import workloads as wl
+
+NAMES = wl.INPUT_NAMES  # r, w, k, v, a, b
+
+DECODE_TOL = 1e-4    # float32 decode path, normwise-max relative error
+PREFILL_TOL = 2e-2   # chunked prefill with bf16 tensor-core operands
+SEQ_PREFILL_TOL = 1e-4  # float32 token-by-token prefill
+
+
+def dev_inputs(ins: dict, dtype: str, device="cuda"):
+    """Seeded float32 arrays (exact in dtype) -> list of device tensors r..b."""
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    return [torch.from_numpy(np.ascontiguousarray(ins[n])).to(device).to(tdt) for n in NAMES]
+
+
+def host_inputs(ins: dict):
+    return [np.asarray(ins[n], dtype=np.float64) for n in NAMES]
+
+
+def i32(x, device="cuda"):
+    return torch.as_tensor(np.asarray(x, dtype=np.int32), device=device)
+
+
+def rel(x, ref):
+    import oracle
+    return oracle.rel_err(np.asarray(x, dtype=np.float64), ref)
+
+
+def sampled_head_inputs(seed: int, tag: str, n_tok: int, H: int, N: int, heads,
+                        device="cuda"):
+    """Full-size bf16 device inputs whose `heads` carry seeded host values (also
+    returned, [n_tok, len(heads), N], for the oracle); the other heads are
+    drawn with torch's device generator from the same recipe."""
+    dev = wl.token_inputs_device(seed, n_tok, H, N, device)
+    host = wl.token_inputs(seed, tag, n_tok, H, N, dtype="bf16", heads=heads)
+    hidx = torch.as_tensor(list(heads), dtype=torch.long, device=device)
+    for t, name in zip(dev, NAMES):
+        t[:, hidx] = torch.from_numpy(host[name]).to(device).to(torch.bfloat16)
+    return dev, host

@@ -1,0 +1,149 @@
+"""GPU parity of the prefill paths against the oracle.
+
+wkv7_prefill (chunked, bf16 tensor-core operands, float32 carry): normwise-max
+relative error <= 2e-2 on outputs and final states.  wkv7_prefill_sequential
+(float32 token by token): <= 1e-4.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from gpu_helpers import (PREFILL_TOL, SEQ_PREFILL_TOL, dev_inputs, host_inputs, i32, rel,
+                         sampled_head_inputs)
+from rwkv_wkv_gb300 import DEV_BAD_SEQLENS, DEV_BAD_SLOT, Pool
+
+pytestmark = pytest.mark.gpu
+
+PATHS = [("chunked", False, PREFILL_TOL), ("sequential", True, SEQ_PREFILL_TOL)]
+
+
+def _run(pool, slots, cu, ins, sequential, layer=0):
+    dev = ins if isinstance(ins, list) else dev_inputs(ins, "bf16")
+    o = pool.prefill(layer, i32(slots), i32(cu), *dev,
+                     max_seqlen=int(np.max(np.diff(cu))) if len(cu) > 1 else 0,
+                     sequential=sequential)
+    code = pool.device_status()
+    return o.cpu().numpy(), code
+
+
+def _check(pool, slots, cu, ins, S0, sequential, tol, heads=None, host=None):
+    """ins: host dict (all heads) or a list of device tensors with `host`
+    holding the seeded values of `heads` only."""
+    o_gpu, code = _run(pool, slots, cu, ins, sequential)
+    assert code == 0
+    S_gpu = pool.states[torch.as_tensor(slots, dtype=torch.long), 0].cpu().numpy()
+    H = S0.shape[1]
+    heads = list(range(H)) if heads is None else heads
+    if host is None:
+        sub = [x[:, heads] for x in host_inputs(ins)]
+    else:
+        sub = host_inputs(host)
+    o_ref, S_ref = oracle.prefill(S0[:, heads], cu, *sub, n_threads=8)
+    e_o = rel(o_gpu[:, heads], o_ref)
+    e_s = rel(S_gpu[:, heads], S_ref)
+    assert e_o < tol and e_s < tol, (e_o, e_s)
+    return e_o, e_s
+
+
+@pytest.mark.parametrize("name,sequential,tol", PATHS)
+def test_single_layer_as_one_prefill(name, sequential, tol):
+    """1 layer, 4 heads, 2 slots, T = 64 per slot, zero start (bf16-rounded
+    copy of the decode inputs)."""
+    W = wl.SINGLE_LAYER
+    T = 64
+    ins = wl.token_inputs(W.seed, "tokens", T * W.n_slots, W.H, W.N, dtype="bf16")
+    # token-major [T][slot] -> sequence-major [slot][T]
+    ins = {k: np.ascontiguousarray(v.reshape(T, W.n_slots, W.H, W.N).transpose(1, 0, 2, 3)
+                                   .reshape(T * W.n_slots, W.H, W.N)) for k, v in ins.items()}
+    cu = wl.cu_seqlens([T] * W.n_slots)
+    with Pool(1, W.H, W.n_slots) as pool:
+        slots = pool.create(W.n_slots)
+        _check(pool, slots, cu, ins, np.zeros((W.n_slots, W.H, W.N, W.N)), sequential, tol)
+
+
+@pytest.mark.parametrize("name,sequential,tol", PATHS)
+def test_ragged_lengths_around_chunk_boundaries(name, sequential, tol):
+    """Lengths 1, 63, 64, 65, 129, 0 (empty), 200 from N(0, 0.1) start states."""
+    H, N = 3, 64
+    lengths = [1, 63, 64, 65, 129, 0, 200]
+    cu = wl.cu_seqlens(lengths)
+    ins = wl.token_inputs(21, "ragged", int(cu[-1]), H, N, dtype="bf16")
+    S0 = wl.slot_states(21, "state", range(len(lengths)), 1, H, N)[:, 0]
+    with Pool(1, H, 16) as pool:
+        slots = [3, 0, 9, 15, 7, 2, 11]
+        pool.states[torch.as_tensor(slots, dtype=torch.long), 0] = torch.from_numpy(S0).cuda()
+        _check(pool, slots, cu, ins, S0.astype(np.float64), sequential, tol)
+
+
+@pytest.mark.parametrize("name,sequential,tol", PATHS)
+def test_prefill_8x4096_32_heads_sampled_heads(name, sequential, tol):
+    """8 sequences x 4096 tokens, 32 heads, zero start state, chunk 64; every
+    output and final state of heads 0, 7, 19, 31 checked against the oracle."""
+    W = wl.PREFILL_8x4096
+    T = 4096
+    cu = wl.cu_seqlens([T] * 8)
+    heads = [0, 7, 19, 31]
+    dev, host = sampled_head_inputs(W.seed, "tokens", T * 8, W.H, W.N, heads)
+    with Pool(1, W.H, W.n_slots) as pool:
+        slots = pool.create(8)
+        _check(pool, slots, cu, dev, np.zeros((8, W.H, W.N, W.N)), sequential, tol,
+               heads=heads, host=host)
+
+
+@pytest.mark.parametrize("name,sequential,tol", PATHS)
+def test_prefill_ragged_64_sequences_sampled(name, sequential, tol):
+    """64 sequences with lengths uniform on 1..2048, 32 heads, into created
+    slots of a 4096-slot pool; heads 0, 13, 31 checked."""
+    W = wl.MIXED
+    plan = wl.mixed_plan()
+    lengths = plan["lengths"]
+    cu = wl.cu_seqlens(lengths)
+    heads = [0, 13, 31]
+    dev, host = sampled_head_inputs(W.seed, "prefill", int(cu[-1]), W.H, W.N, heads)
+    with Pool(1, W.H, W.n_slots) as pool:
+        slots = pool.create(len(lengths))
+        _check(pool, slots, cu, dev, np.zeros((len(lengths), W.H, W.N, W.N)), sequential, tol,
+               heads=heads, host=host)
+
+
+@pytest.mark.parametrize("sequential", [False, True])
+def test_bad_sequence_metadata_is_flagged(sequential):
+    H, N = 2, 64
+    ins = wl.token_inputs(5, "bad", 10, H, N, dtype="bf16")
+    with Pool(1, H, 4) as pool:
+        pool.states.fill_(1.5)
+        # second sequence runs backwards: skipped and flagged
+        o = pool.prefill(0, i32([0, 1]), i32([0, 6, 4]), *dev_inputs(ins, "bf16"),
+                         max_seqlen=10, sequential=sequential)
+        assert pool.device_status() == DEV_BAD_SEQLENS
+        assert bool((pool.states[1] == 1.5).all())
+        # slot id out of range
+        pool.prefill(0, i32([2, 99]), i32([0, 5, 10]), *dev_inputs(ins, "bf16"),
+                     max_seqlen=5, sequential=sequential)
+        assert pool.device_status() == DEV_BAD_SLOT
+        # a sequence longer than max_seqlen
+        pool.prefill(0, i32([3]), i32([0, 10]), *dev_inputs(ins, "bf16"), max_seqlen=4,
+                     sequential=sequential)
+        assert pool.device_status() == DEV_BAD_SEQLENS
+        assert bool((pool.states[3] == 1.5).all())
+        del o
+
+
+def test_chunked_and_sequential_agree():
+    """The two GPU paths on the same inputs (ragged, random start states)."""
+    H, N = 4, 64
+    lengths = [300, 64, 5, 1000]
+    cu = wl.cu_seqlens(lengths)
+    ins = wl.token_inputs(8, "agree", int(cu[-1]), H, N, dtype="bf16")
+    S0 = torch.from_numpy(wl.slot_states(8, "state", range(4), 1, H, N)[:, 0]).cuda()
+    outs = []
+    with Pool(1, H, 4) as pool:
+        for sequential in (False, True):
+            pool.states[:, 0] = S0
+            o, code = _run(pool, [0, 1, 2, 3], cu, ins, sequential)
+            assert code == 0
+            outs.append((o, pool.states[:, 0].cpu().numpy()))
+    assert rel(outs[0][0], outs[1][0]) < PREFILL_TOL
+    assert rel(outs[0][1], outs[1][1]) < PREFILL_TOL

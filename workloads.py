@@ -63,6 +63,13 @@ def words(key: np.uint64, start: int, n: int) -> np.ndarray:
         return _mix(key + i * _G)
 
 
+def words_at(key: np.uint64, idx: np.ndarray) -> np.ndarray:
+    """Words at arbitrary stream positions idx (same values as words())."""
+    i = np.asarray(idx, dtype=np.uint64) + np.uint64(1)
+    with np.errstate(over="ignore"):
+        return _mix(key + i * _G)
+
+
 def uniforms(key: np.uint64, start: int, n: int) -> np.ndarray:
     wds = words(key, start, n)
     return ((wds >> np.uint64(11)).astype(np.float64) + 1.0) * (2.0 ** -53)
@@ -79,6 +86,24 @@ def normals(seed: int, tag: str, n: int, mean: float = 0.0, std: float = 1.0,
         u1, u2 = u[0::2], u[1::2]
         out[b0:b0 + m] = np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * math.pi * u2)
     return mean + std * out
+
+
+def normals_at(seed: int, tag: str, idx: np.ndarray, mean: float = 0.0,
+               std: float = 1.0) -> np.ndarray:
+    """Normals of stream (seed, tag) at element positions idx (any shape);
+    normals_at(s, t, arange(a, b)) == normals(s, t, b - a, start=a)."""
+    key = stream_key(seed, tag)
+    idx = np.asarray(idx, dtype=np.int64)
+    flat = idx.reshape(-1)
+    out = np.empty(flat.size, dtype=np.float64)
+    for b0 in range(0, flat.size, _BLOCK):
+        e = flat[b0:b0 + _BLOCK].astype(np.uint64)
+        w1 = words_at(key, 2 * e)
+        w2 = words_at(key, 2 * e + np.uint64(1))
+        u1 = ((w1 >> np.uint64(11)).astype(np.float64) + 1.0) * (2.0 ** -53)
+        u2 = ((w2 >> np.uint64(11)).astype(np.float64) + 1.0) * (2.0 ** -53)
+        out[b0:b0 + e.size] = np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * math.pi * u2)
+    return (mean + std * out).reshape(idx.shape)
 
 
 # --------------------------------------------------------------------------
@@ -115,16 +140,29 @@ INPUT_NAMES = ("r", "w", "k", "v", "a", "b")
 
 
 def token_inputs(seed: int, tag: str, n_tok: int, H: int, N: int,
-                 dtype: str = "bf16") -> dict:
+                 dtype: str = "bf16", heads=None) -> dict:
     """Inputs r, w, k, v, a, b of shape [n_tok, H, N] as float32 arrays whose
-    values are exactly representable in `dtype` ("bf16" or "f32")."""
-    shape = (n_tok, H, N)
-    n = n_tok * H * N
-    r = normals(seed, tag + "/r", n).reshape(shape)
-    k = normals(seed, tag + "/k", n).reshape(shape)
-    v = normals(seed, tag + "/v", n).reshape(shape)
-    g = normals(seed, tag + "/b_gate", n).reshape(shape)
-    x = normals(seed, tag + "/w", n, mean=-0.6, std=0.3).reshape(shape)
+    values are exactly representable in `dtype` ("bf16" or "f32").  With
+    `heads`, only those heads are produced ([n_tok, len(heads), N]), with the
+    same values they have in the full tensor."""
+    if heads is None:
+        shape = (n_tok, H, N)
+        n = n_tok * H * N
+
+        def draw(t, mean=0.0, std=1.0):
+            return normals(seed, tag + t, n, mean=mean, std=std).reshape(shape)
+    else:
+        hs = np.asarray(list(heads), dtype=np.int64)
+        idx = ((np.arange(n_tok, dtype=np.int64)[:, None, None] * H + hs[None, :, None]) * N
+               + np.arange(N, dtype=np.int64)[None, None, :])
+
+        def draw(t, mean=0.0, std=1.0):
+            return normals_at(seed, tag + t, idx, mean=mean, std=std)
+    r = draw("/r")
+    k = draw("/k")
+    v = draw("/v")
+    g = draw("/b_gate")
+    x = draw("/w", mean=-0.6, std=0.3)
     norm = np.sqrt(np.sum(k * k, axis=-1, keepdims=True))
     norm = np.where(norm > 0.0, norm, 1.0)
     khat = k / norm
@@ -223,3 +261,25 @@ def mixed_plan(seed: int = MIXED.seed, n_slots: int = MIXED.n_slots,
     lengths = ragged_lengths(seed, "mixed/lengths", n_seqs, 1, max_len)
     return {"decode": decode, "prefill": prefill, "fork_src": fork_src,
             "fork_dst": fork_dst, "snap_src": snap_src, "lengths": lengths}
+
+
+def token_inputs_device(seed: int, n_tok: int, H: int, N: int, device, dtype=None,
+                        generator_offset: int = 0):
+    """The same recipe drawn with torch's seeded device generator (Philox), for
+    inputs too large to draw on the host.  Values differ from token_inputs();
+    only shapes and distributions match.  Returns [r, w, k, v, a, b] tensors
+    [n_tok, H, N] of `dtype` (default bfloat16) on `device`."""
+    import torch
+    dtype = torch.bfloat16 if dtype is None else dtype
+    g = torch.Generator(device=device).manual_seed(int(seed) * 1000003 + generator_offset)
+    shape = (n_tok, H, N)
+    r = torch.randn(shape, device=device, generator=g)
+    k = torch.randn(shape, device=device, generator=g)
+    v = torch.randn(shape, device=device, generator=g)
+    gate = torch.randn(shape, device=device, generator=g)
+    x = torch.randn(shape, device=device, generator=g) * 0.3 - 0.6
+    khat = k / k.norm(dim=-1, keepdim=True).clamp_min(1e-30)
+    a = -khat
+    b = khat * torch.sigmoid(gate)
+    w = torch.exp(-torch.exp(x))
+    return [t.to(dtype).contiguous() for t in (r, w, k, v, a, b)]
