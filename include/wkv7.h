@@ -203,8 +203,11 @@ wkv7_status wkv7_decode_step(wkv7_pool *pool, int32_t layer, const int32_t *slot
  * 64 tokens anchored at each sequence's first token, with bf16 tensor-core
  * operands and a float32 state carried between chunks.  max_seqlen bounds
  * every sequence length.  Errors: INVALID_ARG, UNSUPPORTED (in_dtype must be
- * WKV7_BF16), CUDA.  Device: WKV7_DEV_BAD_SLOT, WKV7_DEV_BAD_SEQLENS (that
- * sequence is skipped), WKV7_DEV_DECAY_RANGE, WKV7_DEV_WAIT_TIMEOUT. */
+ * WKV7_BF16; the six input bases must be 16-byte aligned), CUDA.  Device:
+ * WKV7_DEV_BAD_SLOT, WKV7_DEV_BAD_SEQLENS (that sequence is skipped),
+ * WKV7_DEV_DECAY_RANGE (the decay over half a chunk, 32 tokens, exceeds
+ * 2^120 in some channel: that sequence's results are not reliable),
+ * WKV7_DEV_WAIT_TIMEOUT. */
 wkv7_status wkv7_prefill(wkv7_pool *pool, int32_t layer, const int32_t *slot_ids_dev,
                          const int32_t *cu_seqlens_dev, int32_t n_seqs, int32_t total_tokens,
                          int32_t max_seqlen, wkv7_dtype in_dtype, const void *r,

@@ -375,6 +375,11 @@ static wkv7_status prefill_common(wkv7_pool *pool, int32_t layer, const int32_t 
     if (!slot_ids_dev || !cu_seqlens_dev) return WKV7_ERR_INVALID_ARG;
     if (total_tokens > 0 && !inputs_present(r, w, k, v, a, b, o)) return WKV7_ERR_INVALID_ARG;
     if (chunked && in_dtype != WKV7_BF16) return WKV7_ERR_UNSUPPORTED;
+    if (chunked && total_tokens > 0) {  // tensor-map loads need 16-byte aligned bases
+        const void *ins[6] = {r, w, k, v, a, b};
+        for (const void *x : ins)
+            if (reinterpret_cast<uintptr_t>(x) % 16 != 0) return WKV7_ERR_UNSUPPORTED;
+    }
     wkv7::PrefillArgs pa;
     pa.lv = layer_view(pool, layer);
     pa.slot_ids = slot_ids_dev;
