@@ -17,10 +17,14 @@
 //
 // One CTA (4 warps) owns one (sequence, head) and walks its chunks in order,
 // anchored at the sequence's first token; the last chunk is padded with
-// identity tokens (w = 1, other inputs 0).  Per chunk:
-//   E   TMA-loaded bf16 inputs -> log2-decay prefix sums (one warp per 16
-//       tokens, two channels per lane) -> scaled bf16 operands in 128-byte
-//       swizzled K-major tiles.  Decays inside the Gram products are taken
+// identity tokens (w = 1, other inputs 0).  Two CTAs share an SM (about 106 KB
+// of shared memory and 256 tensor-memory columns each), so one CTA's MMA
+// waits and load latencies are covered by the other's CUDA-core phases.
+// Per chunk:
+//   E   bf16 inputs read from global memory (the chunk's six boxes were
+//       prefetched into L2 by TMA one chunk earlier) -> log2-decay prefix
+//       sums (one warp per 16 tokens, two channels per lane) -> scaled bf16
+//       operands in 128-byte swizzled K-major tiles.  Decays inside the Gram products are taken
 //       relative to the chunk midpoint (token 31), so no factor exceeds
 //       2^(half-chunk decay); factors that meet S0 are relative to the start.
 //   G1  [Bbar;Kbar] x Am^T  -> Mab, Mak rows        (M=128, N=64,  K=64)
@@ -50,39 +54,46 @@ constexpr int kL = 64;
 constexpr int kThreads = 128;
 constexpr long long kWaitCycles = 4000000000LL;  // about 2 s at 2 GHz
 constexpr float kMaxLog2Range = 120.0f;           // |G - Gm| limit (float exponent range)
-constexpr int kMS = 68;                           // float stride of the 64x64 fp32 scratch
 
-// Shared-memory map (bytes from a 1024-aligned base).
+// Shared-memory map.  Small items first (from the raw base), then the tiles
+// from the next 1024-byte boundary.  Region R1 is reused through the chunk:
+// G1A | G1B (E -> G1)  ->  MT | TT fp32 (inverse)  ->  G2B (over MT, -> G2)
+// ->  OPZ (-> G34)  ->  OPY | OPA2 (-> G5).
 constexpr uint32_t kTile64 = 8192;    // 64 rows x 128 B (bf16, K = 64)
 constexpr uint32_t kTile128 = 16384;  // 128 rows
-constexpr uint32_t OFF_IN = 0;        // six TMA tiles: r, w, k, v, a, b (plain [t][j] bf16)
-constexpr uint32_t OFF_R1 = OFF_IN + 6 * kTile64;   // G1A | G1B, later OPZ, later OPY | OPA2
+constexpr uint32_t SOFF_TOT = 0;                    // per-warp log2-decay totals [4][64] fp32
+constexpr uint32_t SOFF_GAM = SOFF_TOT + 4 * 64 * 4;  // D(0,L] per channel [64]
+constexpr uint32_t SOFF_BAR = SOFF_GAM + 64 * 4;    // one mbarrier (8 B)
+constexpr uint32_t SOFF_HOLD = SOFF_BAR + 8;        // tensor-memory base
+constexpr uint32_t SOFF_FLAG = SOFF_HOLD + 4;       // abort flag
+constexpr uint32_t kSmallBytes = SOFF_FLAG + 4;
+constexpr uint32_t OFF_R1 = 0;                      // tile offsets from the aligned base
 constexpr uint32_t OFF_G1A = OFF_R1;
 constexpr uint32_t OFF_G1B = OFF_R1 + kTile128;
+constexpr uint32_t OFF_MT = OFF_R1;                 // fp32 64x64, swizzled
+constexpr uint32_t OFF_TT = OFF_R1 + kTile128;      // fp32 64x64, swizzled
+constexpr uint32_t OFF_G2B = OFF_R1;                // T (rows s, K = t)
 constexpr uint32_t OFF_OPZ = OFF_R1;
 constexpr uint32_t OFF_OPY = OFF_R1;
 constexpr uint32_t OFF_OPA2 = OFF_R1 + kTile128;
 constexpr uint32_t OFF_G2A = OFF_R1 + 2 * kTile128;  // [Bhat^T; Qb^T]
-constexpr uint32_t OFF_G2B = OFF_G2A + kTile128;     // T (rows s, K = t)
-constexpr uint32_t OFF_G34B = OFF_G2B + kTile64;     // [A0^T; Mak]
+constexpr uint32_t OFF_G34B = OFF_G2A + kTile128;    // [A0^T; Mak]
 constexpr uint32_t OFF_V = OFF_G34B + kTile128;      // V^T (rows i, K = s)
 constexpr uint32_t OFF_KHT = OFF_V + kTile64;        // Khat^T (rows j, K = s)
 constexpr uint32_t OFF_R0 = OFF_KHT + kTile64;       // R0 (rows t, K = j)
 constexpr uint32_t OFF_SHI = OFF_R0 + kTile64;       // S0 hi (rows i, K = j)
 constexpr uint32_t OFF_SLO = OFF_SHI + kTile64;      // S0 lo
-constexpr uint32_t OFF_MT = OFF_SLO + kTile64;       // Mab fp32 [64][kMS]; lower blocks: temps
-constexpr uint32_t OFF_TT = OFF_MT + 64 * kMS * 4;   // T fp32 [64][kMS]
-constexpr uint32_t OFF_TOT = OFF_TT + 64 * kMS * 4;  // per-warp log2-decay totals [4][64]
-constexpr uint32_t OFF_GAM = OFF_TOT + 4 * 64 * 4;   // D(0,L] per channel [64]
-constexpr uint32_t OFF_BAR = OFF_GAM + 64 * 4;       // two mbarriers
-constexpr uint32_t OFF_HOLD = OFF_BAR + 16;          // tensor-memory base
-constexpr uint32_t OFF_FLAG = OFF_HOLD + 4;          // abort flag
-constexpr uint32_t kSmemUsed = OFF_FLAG + 4;
-constexpr uint32_t kSmemBytes = kSmemUsed + 1024;    // + alignment slack
-static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+constexpr uint32_t kTileBytes = OFF_SLO + kTile64;
+constexpr uint32_t kSmemBytes = kSmallBytes + 1024 + kTileBytes;  // + worst-case alignment
+static_assert(2 * (kSmemBytes + 1024) <= 228 * 1024, "two CTAs per SM");
 constexpr uint32_t kTmemCols = 256;
 
-enum { IN_R = 0, IN_W = 1, IN_K = 2, IN_V = 3, IN_A = 4, IN_B = 5 };
+// Index of element (r, c) of a 64x64 fp32 scratch matrix: 4-float groups of a
+// row are permuted by XOR with (r % 16), so row-wise float4 access and
+// column-wise scalar access both spread over the banks.
+__device__ __forceinline__ int mt_idx(int r, int c) {
+    return r * 64 + ((((c >> 2) ^ (r & 15)) << 2) | (c & 3));
+}
 
 struct InputMaps {
     CUtensorMap m[6];  // r, w, k, v, a, b
@@ -91,6 +102,19 @@ struct InputMaps {
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&p);
+}
+
+// Hardware base-2 exponential and logarithm (MUFU, ~2 ulp, denormals flushed);
+// the decay factors they produce are rounded to bf16 right after.
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float lg2_approx(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 __device__ __forceinline__ float bf16_to_f(uint16_t u) {
@@ -110,6 +134,31 @@ __device__ __forceinline__ void store_row32(uint8_t *tile, int row, int col0, co
     }
 }
 
+// Write 16 floats as bf16 into columns col0..col0+15 of `row` of a swizzled tile.
+__device__ __forceinline__ void store_row16(uint8_t *tile, int row, int col0, const float *v) {
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        uint4 u;
+        u.x = pack_bf16(v[8 * q + 0], v[8 * q + 1]);
+        u.y = pack_bf16(v[8 * q + 2], v[8 * q + 3]);
+        u.z = pack_bf16(v[8 * q + 4], v[8 * q + 5]);
+        u.w = pack_bf16(v[8 * q + 6], v[8 * q + 7]);
+        *reinterpret_cast<uint4 *>(tile + sw128_off(row, col0 + 8 * q)) = u;
+    }
+}
+
+// Read 16 bf16 of `row` (columns col0..) of a swizzled tile as floats.
+__device__ __forceinline__ void load_row16(const uint8_t *tile, int row, int col0, float *v) {
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        uint4 u = *reinterpret_cast<const uint4 *>(tile + sw128_off(row, col0 + 8 * q));
+        v[8 * q + 0] = bf16_lo(u.x); v[8 * q + 1] = bf16_hi(u.x);
+        v[8 * q + 2] = bf16_lo(u.y); v[8 * q + 3] = bf16_hi(u.y);
+        v[8 * q + 4] = bf16_lo(u.z); v[8 * q + 5] = bf16_hi(u.z);
+        v[8 * q + 6] = bf16_lo(u.w); v[8 * q + 7] = bf16_hi(u.w);
+    }
+}
+
 // Read 32 bf16 of `row` (columns col0..) of a swizzled tile as floats.
 __device__ __forceinline__ void load_row32(const uint8_t *tile, int row, int col0, float *v) {
 #pragma unroll
@@ -122,31 +171,72 @@ __device__ __forceinline__ void load_row32(const uint8_t *tile, int row, int col
     }
 }
 
-// C (2x4 micro-tile at rows r0, r0+1, cols c0..c0+3) += A[rows][k] * B[k][cols]
-// over k = 0..15, A and B 16x16 blocks of kMS-strided float matrices.
-__device__ __forceinline__ void micro_2x4(const float *A, const float *B, int r0, int c0,
-                                          float (&acc)[2][4]) {
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+// d += a (16x8, tf32) * b (8x8, tf32), float accumulators; warp-wide.
+__device__ __forceinline__ void mma_tf32_16x8x8(float (&d)[4], uint32_t a0, uint32_t a1,
+                                                uint32_t a2, uint32_t a3, uint32_t b0,
+                                                uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// acc[n] (16 x 8 tile n of a 16x16 block) += A[ar.., ac..] (16x16) * B[br.., bc..]
+// (16x16) for the n-tiles nt0 .. nt0+ntc-1, on swizzled fp32 scratch; warp-wide.
+// Fragments: A (g, t), (g+8, t), (g, t+4), (g+8, t+4); B (t, g), (t+4, g);
+// accumulator (g, 2t), (g, 2t+1), (g+8, 2t), (g+8, 2t+1), g = lane/4, t = lane%4.
+__device__ __forceinline__ void block_mma(const float *A, int ar, int ac, const float *B, int br,
+                                          int bc, int nt0, int ntc, float (&acc)[2][4],
+                                          int lane) {
+    const int g = lane >> 2, t = lane & 3;
 #pragma unroll
-    for (int kk = 0; kk < 16; ++kk) {
-        const float a0 = A[r0 * kMS + kk];
-        const float a1 = A[(r0 + 1) * kMS + kk];
-        const float4 b = *reinterpret_cast<const float4 *>(B + kk * kMS + c0);
-        acc[0][0] = fmaf(a0, b.x, acc[0][0]); acc[0][1] = fmaf(a0, b.y, acc[0][1]);
-        acc[0][2] = fmaf(a0, b.z, acc[0][2]); acc[0][3] = fmaf(a0, b.w, acc[0][3]);
-        acc[1][0] = fmaf(a1, b.x, acc[1][0]); acc[1][1] = fmaf(a1, b.y, acc[1][1]);
-        acc[1][2] = fmaf(a1, b.z, acc[1][2]); acc[1][3] = fmaf(a1, b.w, acc[1][3]);
+    for (int kk = 0; kk < 16; kk += 8) {
+        const uint32_t a0 = to_tf32(A[mt_idx(ar + g, ac + kk + t)]);
+        const uint32_t a1 = to_tf32(A[mt_idx(ar + g + 8, ac + kk + t)]);
+        const uint32_t a2 = to_tf32(A[mt_idx(ar + g, ac + kk + t + 4)]);
+        const uint32_t a3 = to_tf32(A[mt_idx(ar + g + 8, ac + kk + t + 4)]);
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+            if (n < ntc) {
+                const int col = bc + 8 * (nt0 + n) + g;
+                const uint32_t b0 = to_tf32(B[mt_idx(br + kk + t, col)]);
+                const uint32_t b1 = to_tf32(B[mt_idx(br + kk + t + 4, col)]);
+                mma_tf32_16x8x8(acc[n], a0, a1, a2, a3, b0, b1);
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void block_store(float *C, int cr, int cc, int nt0, int ntc,
+                                            const float (&acc)[2][4], int lane) {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int n = 0; n < 2; ++n) {
+        if (n < ntc) {
+            const int col = cc + 8 * (nt0 + n) + 2 * t;
+            *reinterpret_cast<float2 *>(C + mt_idx(cr + g, col)) = make_float2(acc[n][0], acc[n][1]);
+            *reinterpret_cast<float2 *>(C + mt_idx(cr + g + 8, col)) = make_float2(acc[n][2], acc[n][3]);
+        }
     }
 }
 
 // T = (I - M)^-1 for the strictly upper triangular 64x64 M in MT (fp32),
 // result in TT (upper triangle and 16x16 diagonal blocks), blocked by 16:
-// diagonal blocks by substitution, then T_pq = T_pp sum_{p<u<=q} M_pu T_uq
-// level by level (q - p = 1, 2, 3).  The lower 16x16 blocks of MT hold the
-// sums.  All 128 threads take part; ends with the block synchronised.
+// diagonal blocks by substitution in float32, then T_pq = T_pp sum_{p<u<=q}
+// M_pu T_uq level by level (q - p = 1, 2, 3) with warp-level tf32 MMAs (the
+// blocks are 16x16; T is rounded to bf16 afterwards).  The lower 16x16
+// blocks of MT hold the sums.  All 128 threads take part; ends synchronised.
 __device__ __forceinline__ void invert_unit_upper(float *MT, float *TT, int tid) {
     if (tid < 64) {
         const int p = tid >> 4, c = tid & 15;
-        const float *M = MT + (16 * p) * kMS + 16 * p;
+        const int o = 16 * p;
         float x[16];
 #pragma unroll
         for (int r = 0; r < 16; ++r) x[r] = (r == c) ? 1.f : 0.f;
@@ -155,44 +245,51 @@ __device__ __forceinline__ void invert_unit_upper(float *MT, float *TT, int tid)
             if (r < c) {
                 float acc = 0.f;
 #pragma unroll
-                for (int u = r + 1; u < 16; ++u) acc = fmaf(M[r * kMS + u], x[u], acc);
+                for (int u = r + 1; u < 16; ++u) acc = fmaf(MT[mt_idx(o + r, o + u)], x[u], acc);
                 x[r] = acc;
             }
         }
-        float *Tb = TT + (16 * p) * kMS + 16 * p;
 #pragma unroll
-        for (int r = 0; r < 16; ++r) Tb[r * kMS + c] = x[r];
+        for (int r = 0; r < 16; ++r) TT[mt_idx(o + r, o + c)] = x[r];
     }
     __syncthreads();
-#pragma unroll 1
-    for (int d = 1; d <= 3; ++d) {
-        const int nblk = 4 - d;  // blocks (p, p+d), p = 0..nblk-1
-        const int mt = tid & 31, blk = tid >> 5;
-        const int r0 = 2 * (mt >> 2), c0 = 4 * (mt & 3);
-        if (blk < nblk) {  // X_pq = sum_{u=p+1..q} M_pu T_uq -> lower block (q, p) of MT
-            const int p = blk, q = blk + d;
-            float acc[2][4] = {};
-            for (int u = p + 1; u <= q; ++u)
-                micro_2x4(MT + (16 * p) * kMS + 16 * u, TT + (16 * u) * kMS + 16 * q, r0, c0, acc);
-            float *X = MT + (16 * q) * kMS + 16 * p;
-#pragma unroll
-            for (int i = 0; i < 2; ++i)
-                *reinterpret_cast<float4 *>(X + (r0 + i) * kMS + c0) =
-                    make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
-        }
-        __syncthreads();
-        if (blk < nblk) {  // T_pq = T_pp X_pq
-            const int p = blk, q = blk + d;
-            float acc[2][4] = {};
-            micro_2x4(TT + (16 * p) * kMS + 16 * p, MT + (16 * q) * kMS + 16 * p, r0, c0, acc);
-            float *Tq = TT + (16 * p) * kMS + 16 * q;
-#pragma unroll
-            for (int i = 0; i < 2; ++i)
-                *reinterpret_cast<float4 *>(Tq + (r0 + i) * kMS + c0) =
-                    make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
-        }
-        __syncthreads();
+    const int warp = tid >> 5, lane = tid & 31;
+    // q - p = 1: blocks (0,1), (1,2), (2,3), one warp each
+    if (warp < 3) {
+        const int p = warp, q = warp + 1;
+        float acc[2][4] = {};
+        block_mma(MT, 16 * p, 16 * q, TT, 16 * q, 16 * q, 0, 2, acc, lane);
+        block_store(MT, 16 * q, 16 * p, 0, 2, acc, lane);
+        __syncwarp();
+        float tq[2][4] = {};
+        block_mma(TT, 16 * p, 16 * p, MT, 16 * q, 16 * p, 0, 2, tq, lane);
+        block_store(TT, 16 * p, 16 * q, 0, 2, tq, lane);
     }
+    __syncthreads();
+    {  // q - p = 2: blocks (0,2), (1,3), one 8-column half per warp
+        const int p = warp >> 1, q = p + 2, nt = warp & 1;
+        float acc[2][4] = {};
+        block_mma(MT, 16 * p, 16 * (p + 1), TT, 16 * (p + 1), 16 * q, nt, 1, acc, lane);
+        block_mma(MT, 16 * p, 16 * q, TT, 16 * q, 16 * q, nt, 1, acc, lane);
+        block_store(MT, 16 * q, 16 * p, nt, 1, acc, lane);
+        __syncwarp();
+        float tq[2][4] = {};
+        block_mma(TT, 16 * p, 16 * p, MT, 16 * q, 16 * p, nt, 1, tq, lane);
+        block_store(TT, 16 * p, 16 * q, nt, 1, tq, lane);
+    }
+    __syncthreads();
+    if (warp < 2) {  // q - p = 3: block (0,3), one half per warp
+        const int nt = warp;
+        float acc[2][4] = {};
+#pragma unroll
+        for (int u = 1; u <= 3; ++u) block_mma(MT, 0, 16 * u, TT, 16 * u, 48, nt, 1, acc, lane);
+        block_store(MT, 48, 0, nt, 1, acc, lane);
+        __syncwarp();
+        float tq[2][4] = {};
+        block_mma(TT, 0, 0, MT, 48, 0, nt, 1, tq, lane);
+        block_store(TT, 0, 48, nt, 1, tq, lane);
+    }
+    __syncthreads();
 }
 
 // All threads wait on the barrier; returns false (uniformly) if any gave up.
@@ -202,7 +299,7 @@ __device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, volatile
     return *flag == 0;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     prefill_chunk_kernel(const PrefillArgs p, const __grid_constant__ InputMaps maps) {
     extern __shared__ uint8_t smem_raw[];
     const int seq = blockIdx.x;
@@ -224,21 +321,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int len = t1 - t0;
     if (len == 0) return;
 
+    uint8_t *small = smem_raw;
     uint8_t *base = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const uint32_t bar_tma = smem_addr(base + OFF_BAR);
-    const uint32_t bar_mma = bar_tma + 8;
-    uint32_t *holder = reinterpret_cast<uint32_t *>(base + OFF_HOLD);
-    volatile int *flag = reinterpret_cast<volatile int *>(base + OFF_FLAG);
+        (reinterpret_cast<uintptr_t>(smem_raw + kSmallBytes) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t bar_mma = smem_addr(small + SOFF_BAR);
+    uint32_t *holder = reinterpret_cast<uint32_t *>(small + SOFF_HOLD);
+    volatile int *flag = reinterpret_cast<volatile int *>(small + SOFF_FLAG);
+    float *tot = reinterpret_cast<float *>(small + SOFF_TOT);
+    float *gam = reinterpret_cast<float *>(small + SOFF_GAM);
     float *MT = reinterpret_cast<float *>(base + OFF_MT);
     float *TT = reinterpret_cast<float *>(base + OFF_TT);
-    float *tot = reinterpret_cast<float *>(base + OFF_TOT);
-    float *gam = reinterpret_cast<float *>(base + OFF_GAM);
-    const uint8_t *in = base + OFF_IN;
 
     if (warp == 0) tmem_alloc(smem_addr(holder), kTmemCols);
     if (tid == 0) {
-        mbar_init(bar_tma, 1);
         mbar_init(bar_mma, 1);
         fence_mbar_init();
         *flag = 0;
@@ -270,122 +365,124 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *holder;
     const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
 
+    // inputs as bf16 pairs: token t (absolute), channels 2*lane, 2*lane+1
+    const uint32_t *gR = static_cast<const uint32_t *>(p.in.r);
+    const uint32_t *gW = static_cast<const uint32_t *>(p.in.w);
+    const uint32_t *gK = static_cast<const uint32_t *>(p.in.k);
+    const uint32_t *gV = static_cast<const uint32_t *>(p.in.v);
+    const uint32_t *gA = static_cast<const uint32_t *>(p.in.a);
+    const uint32_t *gB = static_cast<const uint32_t *>(p.in.b);
+    auto goff = [&](int t) -> size_t {
+        return (static_cast<size_t>(t) * H + h) * (kHeadSize / 2) + lane;
+    };
+
     const int n_chunks = (len + kL - 1) / kL;
-    if (tid == 0) {
-        mbar_arrive_expect_tx(bar_tma, 6 * kTile64);
-#pragma unroll
-        for (int x = 0; x < 6; ++x)
-            tma_load_3d(smem_addr(base + OFF_IN + x * kTile64), &maps.m[x], 0, h, t0, bar_tma);
-    }
-    uint32_t ph_tma = 0, ph_mma = 0;
+    uint32_t ph_mma = 0;
     bool range_bad = false;
 
     for (int c = 0; c < n_chunks; ++c) {
         const int tc0 = t0 + c * kL;
         const int Lc = min(kL, t1 - tc0);
         const bool last = (c + 1 == n_chunks);
-        if (!wait_all(bar_tma, ph_tma, flag)) break;
-        ph_tma ^= 1;
-
         // ---------------------------------------------------------- E phase
         {
             const int tb = 16 * warp;  // this warp's 16 tokens; lane: channels 2l, 2l+1
             const int ch = 2 * lane;
-            auto ld2 = [&](int x, int t) -> float2 {
-                const uint32_t u = *reinterpret_cast<const uint32_t *>(in + x * kTile64 + t * 128 + 4 * lane);
-                return make_float2(bf16_lo(u), bf16_hi(u));
-            };
-            float pre0[16], pre1[16];
-            float s0 = 0.f, s1 = 0.f;
+            float s0 = 0.f, s1 = 0.f;  // pass 1: this warp's log2-decay totals
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                const int t = tb + i;
-                if (t < Lc) {
-                    const float2 wv = ld2(IN_W, t);
-                    s0 += __log2f(wv.x);
-                    s1 += __log2f(wv.y);
-                }
-                pre0[i] = s0;
-                pre1[i] = s1;
+                const uint32_t wv = (tb + i < Lc) ? __ldg(gW + goff(tc0 + tb + i)) : 0x3F803F80u;
+                s0 += lg2_approx(bf16_lo(wv));
+                s1 += lg2_approx(bf16_hi(wv));
             }
             tot[warp * 64 + ch] = s0;
             tot[warp * 64 + ch + 1] = s1;
             __syncthreads();
-            float off0 = 0.f, off1 = 0.f;
+            float G0 = 0.f, G1 = 0.f;  // running G (inclusive prefix) of channels ch, ch+1
             for (int w2 = 0; w2 < warp; ++w2) {
-                off0 += tot[w2 * 64 + ch];
-                off1 += tot[w2 * 64 + ch + 1];
+                G0 += tot[w2 * 64 + ch];
+                G1 += tot[w2 * 64 + ch + 1];
             }
             const float Gm0 = tot[ch] + tot[64 + ch], Gm1 = tot[ch + 1] + tot[64 + ch + 1];
             const float G630 = Gm0 + tot[128 + ch] + tot[192 + ch];
             const float G631 = Gm1 + tot[128 + ch + 1] + tot[192 + ch + 1];
             if (warp == 0) {
-                gam[ch] = exp2f(G630);
-                gam[ch + 1] = exp2f(G631);
+                gam[ch] = ex2_approx(G630);
+                gam[ch + 1] = ex2_approx(G631);
             }
-            if (!(fabsf(off0 - Gm0) <= kMaxLog2Range && fabsf(off1 - Gm1) <= kMaxLog2Range))
+            if (!(fabsf(G0 - Gm0) <= kMaxLog2Range && fabsf(G1 - Gm1) <= kMaxLog2Range))
                 range_bad = true;  // G[tb-1] (G[-1] = 0 for the first warp)
-            const float EL0 = exp2f(G630 - Gm0), EL1 = exp2f(G631 - Gm1);
-            float ep0 = exp2f(off0 - Gm0), ep1 = exp2f(off1 - Gm1);  // e_prev at i = 0
-            float dp0 = exp2f(off0), dp1 = exp2f(off1);              // d_prev at i = 0
-            uint32_t cb[4][2][4];  // CT operands: [Bhat, Khat, A0, V][channel][token pair]
+            const float EL0 = ex2_approx(G630 - Gm0), EL1 = ex2_approx(G631 - Gm1);
+            float ep0 = ex2_approx(G0 - Gm0), ep1 = ex2_approx(G1 - Gm1);  // e_prev
+            float dp0 = ex2_approx(G0), dp1 = ex2_approx(G1);              // d_prev
+            // swizzled byte offset of (row tb + i, column ch) = rowbase + row part + xo[i & 7]
+            const uint32_t xl = static_cast<uint32_t>(lane) >> 2;
+            uint8_t *g1a = base + OFF_G1A, *g1b = base + OFF_G1B, *r0t = base + OFF_R0;
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {
+                const int tb8 = tb + 8 * half;
+                const uint32_t rowbase = 1024u * (tb8 >> 3) + 4u * (lane & 3);
+                uint32_t ga[8], gb[8], gk[8], gr[8], gv[8], gw[8];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int t = tb + i;
-                const bool valid = t < Lc;
-                const float G0 = off0 + pre0[i], G1 = off1 + pre1[i];
-                if (valid && !(fabsf(G0 - Gm0) <= kMaxLog2Range && fabsf(G1 - Gm1) <= kMaxLog2Range))
-                    range_bad = true;
-                const float ec0 = exp2f(G0 - Gm0), ec1 = exp2f(G1 - Gm1);
-                const float iv0 = exp2f(Gm0 - G0), iv1 = exp2f(Gm1 - G1);
-                const float dc0 = exp2f(G0), dc1 = exp2f(G1);
-                const float dl0 = EL0 * iv0, dl1 = EL1 * iv1;
-                float2 a = make_float2(0.f, 0.f), b = a, k = a, r = a, v = a;
-                if (valid) {
-                    a = ld2(IN_A, t); b = ld2(IN_B, t); k = ld2(IN_K, t);
-                    r = ld2(IN_R, t); v = ld2(IN_V, t);
+                for (int i = 0; i < 8; ++i) {
+                    const bool valid = tb8 + i < Lc;
+                    const size_t o = goff(tc0 + tb8 + i);
+                    gw[i] = valid ? __ldg(gW + o) : 0x3F803F80u;
+                    ga[i] = valid ? __ldg(gA + o) : 0u;
+                    gb[i] = valid ? __ldg(gB + o) : 0u;
+                    gk[i] = valid ? __ldg(gK + o) : 0u;
+                    gr[i] = valid ? __ldg(gR + o) : 0u;
+                    gv[i] = valid ? __ldg(gV + o) : 0u;
                 }
-                uint8_t *g1a = base + OFF_G1A, *g1b = base + OFF_G1B;
-                *reinterpret_cast<uint32_t *>(g1a + sw128_off(t, ch)) = pack_bf16(b.x * iv0, b.y * iv1);
-                *reinterpret_cast<uint32_t *>(g1a + sw128_off(64 + t, ch)) = pack_bf16(k.x * iv0, k.y * iv1);
-                *reinterpret_cast<uint32_t *>(g1b + sw128_off(t, ch)) = pack_bf16(a.x * ep0, a.y * ep1);
-                *reinterpret_cast<uint32_t *>(g1b + sw128_off(64 + t, ch)) = pack_bf16(r.x * ec0, r.y * ec1);
-                *reinterpret_cast<uint32_t *>(base + OFF_R0 + sw128_off(t, ch)) = pack_bf16(r.x * dc0, r.y * dc1);
-                // channel-major operands, two tokens per 32-bit word
-                const float cv[4][2] = {{b.x * dl0, b.y * dl1}, {k.x * dl0, k.y * dl1},
-                                        {a.x * dp0, a.y * dp1}, {v.x, v.y}};
+                uint32_t cb[4][2][4];  // channel-major operands [Bhat, Khat, A0, V][channel][pair]
+                float prv[4][2];
 #pragma unroll
-                for (int o = 0; o < 4; ++o)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const uint32_t hv = __bfloat16_as_ushort(__float2bfloat16_rn(cv[o][e]));
-                        if ((i & 1) == 0)
-                            cb[o][e][(i >> 1) & 3] = hv;
-                        else
-                            cb[o][e][(i >> 1) & 3] |= hv << 16;
-                    }
-                if ((i & 7) == 7) {  // flush 8 tokens of each channel-major row
-                    const int col = tb + (i & 8);
-                    uint8_t *dst[4] = {base + OFF_G2A, base + OFF_KHT, base + OFF_G34B, base + OFF_V};
+                for (int ii = 0; ii < 8; ++ii) {
+                    G0 += lg2_approx(bf16_lo(gw[ii]));
+                    G1 += lg2_approx(bf16_hi(gw[ii]));
+                    if (tb8 + ii < Lc &&
+                        !(fabsf(G0 - Gm0) <= kMaxLog2Range && fabsf(G1 - Gm1) <= kMaxLog2Range))
+                        range_bad = true;
+                    const float ec0 = ex2_approx(G0 - Gm0), ec1 = ex2_approx(G1 - Gm1);
+                    const float iv0 = ex2_approx(Gm0 - G0), iv1 = ex2_approx(Gm1 - G1);
+                    const float dc0 = ex2_approx(G0), dc1 = ex2_approx(G1);
+                    const float dl0 = EL0 * iv0, dl1 = EL1 * iv1;
+                    const float ax = bf16_lo(ga[ii]), ay = bf16_hi(ga[ii]);
+                    const float bx = bf16_lo(gb[ii]), by = bf16_hi(gb[ii]);
+                    const float kx = bf16_lo(gk[ii]), ky = bf16_hi(gk[ii]);
+                    const float rx = bf16_lo(gr[ii]), ry = bf16_hi(gr[ii]);
+                    const float vx = bf16_lo(gv[ii]), vy = bf16_hi(gv[ii]);
+                    const uint32_t off = rowbase + ii * 128 + ((xl ^ ii) << 4);
+                    *reinterpret_cast<uint32_t *>(g1a + off) = pack_bf16(bx * iv0, by * iv1);
+                    *reinterpret_cast<uint32_t *>(g1a + 8192 + off) = pack_bf16(kx * iv0, ky * iv1);
+                    *reinterpret_cast<uint32_t *>(g1b + off) = pack_bf16(ax * ep0, ay * ep1);
+                    *reinterpret_cast<uint32_t *>(g1b + 8192 + off) = pack_bf16(rx * ec0, ry * ec1);
+                    *reinterpret_cast<uint32_t *>(r0t + off) = pack_bf16(rx * dc0, ry * dc1);
+                    const float cv[4][2] = {{bx * dl0, by * dl1}, {kx * dl0, ky * dl1},
+                                            {ax * dp0, ay * dp1}, {vx, vy}};
 #pragma unroll
                     for (int o = 0; o < 4; ++o)
 #pragma unroll
-                        for (int e = 0; e < 2; ++e)
-                            *reinterpret_cast<uint4 *>(dst[o] + sw128_off(ch + e, col)) =
-                                make_uint4(cb[o][e][0], cb[o][e][1], cb[o][e][2], cb[o][e][3]);
+                        for (int e = 0; e < 2; ++e) {
+                            if ((ii & 1) == 0)
+                                prv[o][e] = cv[o][e];
+                            else
+                                cb[o][e][ii >> 1] = pack_bf16(prv[o][e], cv[o][e]);
+                        }
+                    ep0 = ec0; ep1 = ec1;
+                    dp0 = dc0; dp1 = dc1;
                 }
-                ep0 = ec0; ep1 = ec1;
-                dp0 = dc0; dp1 = dc1;
+                uint8_t *dst[4] = {base + OFF_G2A, base + OFF_KHT, base + OFF_G34B, base + OFF_V};
+#pragma unroll
+                for (int o = 0; o < 4; ++o)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e)  // 8 tokens of channel-major row ch + e
+                        *reinterpret_cast<uint4 *>(dst[o] + sw128_off(ch + e, tb8)) =
+                            make_uint4(cb[o][e][0], cb[o][e][1], cb[o][e][2], cb[o][e][3]);
             }
         }
         fence_proxy_async_smem();
         __syncthreads();
-        if (tid == 0 && !last) {  // the input tiles are free: fetch the next chunk
-            mbar_arrive_expect_tx(bar_tma, 6 * kTile64);
-#pragma unroll
-            for (int x = 0; x < 6; ++x)
-                tma_load_3d(smem_addr(base + OFF_IN + x * kTile64), &maps.m[x], 0, h, tc0 + kL, bar_tma);
-        }
 
         // --------------------------------------------------- G1 and G1'
         if (tid == 0) {
@@ -393,51 +490,50 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_128xNx64(tmem + 0, smem_addr(base + OFF_G1A), smem_addr(base + OFF_G1B), 64, false);
             umma_128xNx64(tmem + 128, smem_addr(base + OFF_G1B), smem_addr(base + OFF_G1A), 128, false);
             umma_commit(bar_mma);
+            if (!last) {  // warm L2 with the next chunk's inputs while the MMAs run
+#pragma unroll
+                for (int x = 0; x < 6; ++x) tma_prefetch_l2_3d(&maps.m[x], 0, h, tc0 + kL);
+            }
         }
         if (!wait_all(bar_mma, ph_mma, flag)) break;
         ph_mma ^= 1;
         tc_fence_after();
         {
-            float v0[32], v1[32];
+            float v[16];
             const int row = 32 * warp + lane;  // TMEM lane
-            tmem_ld32(tmem + lane_base + 0, v0);
-            tmem_ld32(tmem + lane_base + 32, v1);
-            tmem_ld_wait();
             if (warp < 2) {  // Mab row s: keep t > s, float32 for the inverse
                 const int s = row;
-                float *dst = MT + s * kMS;
+#pragma unroll 1
+                for (int g = 0; g < 4; ++g) {
+                    tmem_ld16(tmem + lane_base + 16 * g, v);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    float4 x = make_float4(v0[4 * q], v0[4 * q + 1], v0[4 * q + 2], v0[4 * q + 3]);
-                    const int t = 4 * q;
-                    x.x = (t + 0 > s) ? x.x : 0.f; x.y = (t + 1 > s) ? x.y : 0.f;
-                    x.z = (t + 2 > s) ? x.z : 0.f; x.w = (t + 3 > s) ? x.w : 0.f;
-                    *reinterpret_cast<float4 *>(dst + t) = x;
-                    float4 y = make_float4(v1[4 * q], v1[4 * q + 1], v1[4 * q + 2], v1[4 * q + 3]);
-                    const int u = 32 + 4 * q;
-                    y.x = (u + 0 > s) ? y.x : 0.f; y.y = (u + 1 > s) ? y.y : 0.f;
-                    y.z = (u + 2 > s) ? y.z : 0.f; y.w = (u + 3 > s) ? y.w : 0.f;
-                    *reinterpret_cast<float4 *>(dst + u) = y;
+                    for (int q = 0; q < 4; ++q) {
+                        const int t = 16 * g + 4 * q;
+                        float4 x = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                        x.x = (t + 0 > s) ? x.x : 0.f; x.y = (t + 1 > s) ? x.y : 0.f;
+                        x.z = (t + 2 > s) ? x.z : 0.f; x.w = (t + 3 > s) ? x.w : 0.f;
+                        *reinterpret_cast<float4 *>(MT + mt_idx(s, t)) = x;
+                    }
                 }
             } else {  // Mak row s' (keep s > s'), and Qb^T row t' (keep s <= t')
                 const int s = row - 64;
+#pragma unroll 1
+                for (int g = 0; g < 4; ++g) {
+                    tmem_ld16(tmem + lane_base + 16 * g, v);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int q = 0; q < 32; ++q) {
-                    v0[q] = (q > s) ? v0[q] : 0.f;
-                    v1[q] = (32 + q > s) ? v1[q] : 0.f;
+                    for (int q = 0; q < 16; ++q) v[q] = (16 * g + q > s) ? v[q] : 0.f;
+                    store_row16(base + OFF_G34B, 64 + s, 16 * g, v);
                 }
-                store_row32(base + OFF_G34B, 64 + s, 0, v0);
-                store_row32(base + OFF_G34B, 64 + s, 32, v1);
-                tmem_ld32(tmem + lane_base + 128, v0);
-                tmem_ld32(tmem + lane_base + 160, v1);
-                tmem_ld_wait();
+#pragma unroll 1
+                for (int g = 0; g < 4; ++g) {
+                    tmem_ld16(tmem + lane_base + 128 + 16 * g, v);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int q = 0; q < 32; ++q) {
-                    v0[q] = (q <= s) ? v0[q] : 0.f;
-                    v1[q] = (32 + q <= s) ? v1[q] : 0.f;
+                    for (int q = 0; q < 16; ++q) v[q] = (16 * g + q <= s) ? v[q] : 0.f;
+                    store_row16(base + OFF_G2A, 64 + s, 16 * g, v);
                 }
-                store_row32(base + OFF_G2A, 64 + s, 0, v0);
-                store_row32(base + OFF_G2A, 64 + s, 32, v1);
             }
         }
         tc_fence_before();
@@ -445,12 +541,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // ------------------------------------------------ T = (I - Mab)^-1
         invert_unit_upper(MT, TT, tid);
-        {
+        {  // T (fp32, TT) -> bf16 operand over the dead MT region
             const int s = tid >> 1, c0 = 32 * (tid & 1);
             float x[32];
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
-                const float4 y = *reinterpret_cast<const float4 *>(TT + s * kMS + c0 + 4 * q);
+                const float4 y = *reinterpret_cast<const float4 *>(TT + mt_idx(s, c0 + 4 * q));
                 x[4 * q] = y.x; x[4 * q + 1] = y.y; x[4 * q + 2] = y.z; x[4 * q + 3] = y.w;
             }
 #pragma unroll
@@ -491,47 +587,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         ph_mma ^= 1;
         tc_fence_after();
         {
-            float v[32], add[32];
+            float v[16], add[16];
             if (warp < 2) {  // row j: Phi^T = Phi'^T + diag(gamma); Y_B^T = Y'^T + Khat^T
                 const int j = 32 * warp + lane;
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    tmem_ld32(tmem + lane_base + 32 * half, v);
+                const float gj = gam[j];
+#pragma unroll 1
+                for (int g = 0; g < 4; ++g) {
+                    tmem_ld16(tmem + lane_base + 16 * g, v);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int q = 0; q < 32; ++q)
-                        if (32 * half + q == j) v[q] += gam[j];
-                    store_row32(base + OFF_OPA2, 64 + j, 32 * half, v);
+                    for (int q = 0; q < 16; ++q) v[q] += (16 * g + q == j) ? gj : 0.f;
+                    store_row16(base + OFF_OPA2, 64 + j, 16 * g, v);
                 }
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    tmem_ld32(tmem + lane_base + 64 + 32 * half, v);
+#pragma unroll 1
+                for (int g = 0; g < 4; ++g) {
+                    tmem_ld16(tmem + lane_base + 64 + 16 * g, v);
+                    load_row16(base + OFF_KHT, j, 16 * g, add);
                     tmem_ld_wait();
-                    load_row32(base + OFF_KHT, j, 32 * half, add);
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) v[q] += add[q];
-                    store_row32(base + OFF_OPY, 64 + j, 32 * half, v);
+                    for (int q = 0; q < 16; ++q) v[q] += add[q];
+                    store_row16(base + OFF_OPY, 64 + j, 16 * g, v);
                 }
-            } else {  // row t': R'^T = R''^T + R0; Y_Q^T = Y'^T + Qk^T
+            } else {  // row t': R'^T = R''^T + R0; Y_Q^T = Y'^T + Qk^T (causal: s <= t')
                 const int tq = 32 * warp + lane - 64;
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    tmem_ld32(tmem + lane_base + 32 * half, v);
+#pragma unroll 1
+                for (int g = 0; g < 4; ++g) {
+                    tmem_ld16(tmem + lane_base + 16 * g, v);
+                    load_row16(base + OFF_R0, tq, 16 * g, add);
                     tmem_ld_wait();
-                    load_row32(base + OFF_R0, tq, 32 * half, add);
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) v[q] += add[q];
-                    store_row32(base + OFF_OPA2, tq, 32 * half, v);
+                    for (int q = 0; q < 16; ++q) v[q] += add[q];
+                    store_row16(base + OFF_OPA2, tq, 16 * g, v);
                 }
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    tmem_ld32(tmem + lane_base + 64 + 32 * half, v);
-                    tmem_ld32(tmem + lane_base + 192 + 32 * half, add);
+#pragma unroll 1
+                for (int g = 0; g < 4; ++g) {
+                    tmem_ld16(tmem + lane_base + 64 + 16 * g, v);
+                    tmem_ld16(tmem + lane_base + 192 + 16 * g, add);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int q = 0; q < 32; ++q)  // Qk^T[t'][s] is causal: s <= t'
-                        v[q] += (32 * half + q <= tq) ? add[q] : 0.f;
-                    store_row32(base + OFF_OPY, tq, 32 * half, v);
+                    for (int q = 0; q < 16; ++q) v[q] += (16 * g + q <= tq) ? add[q] : 0.f;
+                    store_row16(base + OFF_OPY, tq, 16 * g, v);
                 }
             }
         }
@@ -550,34 +645,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_all(bar_mma, ph_mma, flag)) break;
         ph_mma ^= 1;
         tc_fence_after();
-        {
-            float v0[32], v1[32];
-            tmem_ld32(tmem + lane_base + 128, v0);
-            tmem_ld32(tmem + lane_base + 160, v1);
-            tmem_ld_wait();
-            if (warp < 2) {  // O row t' -> o[tc0 + t'][h][:]
-                const int tq = 32 * warp + lane;
+        if (warp < 2) {  // O row t' -> o[tc0 + t'][h][:]
+            const int tq = 32 * warp + lane;
+            float *dst = p.in.o + (static_cast<size_t>(tc0 + tq) * H + h) * kHeadSize;
+#pragma unroll 1
+            for (int g = 0; g < 4; ++g) {
+                float v[16];
+                tmem_ld16(tmem + lane_base + 128 + 16 * g, v);
+                tmem_ld_wait();
                 if (tq < Lc) {
-                    float *dst = p.in.o + (static_cast<size_t>(tc0 + tq) * H + h) * kHeadSize;
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        reinterpret_cast<float4 *>(dst)[q] =
-                            make_float4(v0[4 * q], v0[4 * q + 1], v0[4 * q + 2], v0[4 * q + 3]);
-                        reinterpret_cast<float4 *>(dst)[8 + q] =
-                            make_float4(v1[4 * q], v1[4 * q + 1], v1[4 * q + 2], v1[4 * q + 3]);
-                    }
+                    for (int q = 0; q < 4; ++q)
+                        reinterpret_cast<float4 *>(dst + 16 * g)[q] =
+                            make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
                 }
-            } else {  // S_L column j (rows i) -> next chunk's hi/lo operand; last chunk -> slot
-                const int j = 32 * warp + lane - 64;
-                uint8_t *shi = base + OFF_SHI, *slo = base + OFF_SLO;
+            }
+        } else {  // S_L column j (rows i) -> next chunk's hi/lo operand; last chunk -> slot
+            const int j = 32 * warp + lane - 64;
+            uint8_t *shi = base + OFF_SHI, *slo = base + OFF_SLO;
+#pragma unroll 1
+            for (int g = 0; g < 4; ++g) {
+                float v[16];
+                tmem_ld16(tmem + lane_base + 128 + 16 * g, v);
+                tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 64; ++i) {
-                    const float x = i < 32 ? v0[i] : v1[i - 32];
-                    const __nv_bfloat16 hb = __float2bfloat16_rn(x);
-                    const float lo = x - __bfloat162float(hb);
+                for (int q = 0; q < 16; ++q) {
+                    const int i = 16 * g + q;
+                    const __nv_bfloat16 hb = __float2bfloat16_rn(v[q]);
+                    const float lo = v[q] - __bfloat162float(hb);
                     *reinterpret_cast<__nv_bfloat16 *>(shi + sw128_off(i, j)) = hb;
                     *reinterpret_cast<__nv_bfloat16 *>(slo + sw128_off(i, j)) = __float2bfloat16_rn(lo);
-                    if (last) S[i * kHeadSize + j] = x;
+                    if (last) S[i * kHeadSize + j] = v[q];
                 }
             }
         }
@@ -586,9 +684,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncthreads();
     }
 
-    if (*flag) {  // a wait gave up: give in-flight copies a last chance, then leave
+    if (*flag) {  // a wait gave up: give in-flight MMAs a last chance, then leave
         if (tid == 0) flag_status(p.lv.status, WKV7_DEV_WAIT_TIMEOUT);
-        mbar_wait_bounded(bar_tma, ph_tma, kWaitCycles);
         mbar_wait_bounded(bar_mma, ph_mma, kWaitCycles);
     }
     if (range_bad) flag_status(p.lv.status, WKV7_DEV_DECAY_RANGE);
