@@ -15,7 +15,7 @@
 // Khat[s] = k_s D(s,L], Qb[s][t] = <b_s D(s,t], r_t> and Qk likewise (s <= t).
 // Everything except the final "S0 [R' | Phi]" product is independent of S0.
 //
-// One CTA (4 warps) owns one (sequence, head) and walks its chunks in order,
+// One CTA (8 warps) owns one (sequence, head) and walks its chunks in order,
 // anchored at the sequence's first token; the last chunk is padded with
 // identity tokens (w = 1, other inputs 0).  Two CTAs share an SM (about 106 KB
 // of shared memory and 256 tensor-memory columns each), so one CTA's MMA
@@ -23,13 +23,19 @@
 // Per chunk:
 //   E   bf16 inputs read from global memory (the chunk's six boxes were
 //       prefetched into L2 by TMA one chunk earlier) -> log2-decay prefix
-//       sums (one warp per 16 tokens, two channels per lane) -> scaled bf16
-//       operands in 128-byte swizzled K-major tiles.  Decays inside the Gram products are taken
+//       sums (one warp per 8 tokens, two channels per lane) -> scaled bf16
+//       operands in 128-byte swizzled K-major tiles.
+// Tensor-memory readbacks give warps w and w+4 the same 32 lanes (rows) and
+// split the columns between them.  Decays inside the Gram products are taken
 //       relative to the chunk midpoint (token 31), so no factor exceeds
 //       2^(half-chunk decay); factors that meet S0 are relative to the start.
 //   G1  [Bbar;Kbar] x Am^T  -> Mab, Mak rows        (M=128, N=64,  K=64)
 //   G1' [Am;Rm] x [Bbar;Kbar]^T -> Qb^T, Qk^T rows  (M=128, N=128, K=64)
-//   T   (I - Mab)^-1 in float32 on the CUDA cores (16x16 blocked substitution)
+//   T   (I - Mab)^-1: with Mab = D + U (D its 16x16 diagonal blocks),
+//       T = (I + N + N^2 + N^3) Tdiag, Tdiag = (I - D)^-1 (float32 substitution
+//       on the CUDA cores, four 16x16 blocks), N = Tdiag U nilpotent of
+//       index 4; N and the three Horner steps W <- Tdiag + N W are UMMAs
+//       (M=128 with the upper 64 rows unused, B read MN-major)
 //   G2  [Bhat^T; Qb^T] x T^T -> Z^T                  (M=128, N=64)
 //   G34 Z^T x [A0^T; Mak]^T -> Phi'^T, R''^T, Y'^T   (M=128, N=128)
 //   G5  [Y_Q^T; Y_B^T] x V -> O0^T, Psi^T; then += [R'^T; Phi^T] x S0^T with
@@ -51,18 +57,19 @@ namespace {
 using namespace sm100;
 
 constexpr int kL = 64;
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;  // 8 warps; two CTAs per SM
 constexpr long long kWaitCycles = 4000000000LL;  // about 2 s at 2 GHz
 constexpr float kMaxLog2Range = 120.0f;           // |G - Gm| limit (float exponent range)
 
 // Shared-memory map.  Small items first (from the raw base), then the tiles
 // from the next 1024-byte boundary.  Region R1 is reused through the chunk:
-// G1A | G1B (E -> G1)  ->  MT | TT fp32 (inverse)  ->  G2B (over MT, -> G2)
-// ->  OPZ (-> G34)  ->  OPY | OPA2 (-> G5).
+// G1A | G1B (E -> G1)  ->  TD | UT | NT | WT (the inverse; NT first holds the
+// fp32 diagonal blocks of Mab, WT ends as T for G2)  ->  OPZ (-> G34)  ->
+// OPY | OPA2 (-> G5).
 constexpr uint32_t kTile64 = 8192;    // 64 rows x 128 B (bf16, K = 64)
 constexpr uint32_t kTile128 = 16384;  // 128 rows
-constexpr uint32_t SOFF_TOT = 0;                    // per-warp log2-decay totals [4][64] fp32
-constexpr uint32_t SOFF_GAM = SOFF_TOT + 4 * 64 * 4;  // D(0,L] per channel [64]
+constexpr uint32_t SOFF_TOT = 0;                    // per-warp log2-decay totals [8][64] fp32
+constexpr uint32_t SOFF_GAM = SOFF_TOT + 8 * 64 * 4;  // D(0,L] per channel [64]
 constexpr uint32_t SOFF_BAR = SOFF_GAM + 64 * 4;    // one mbarrier (8 B)
 constexpr uint32_t SOFF_HOLD = SOFF_BAR + 8;        // tensor-memory base
 constexpr uint32_t SOFF_FLAG = SOFF_HOLD + 4;       // abort flag
@@ -70,9 +77,12 @@ constexpr uint32_t kSmallBytes = SOFF_FLAG + 4;
 constexpr uint32_t OFF_R1 = 0;                      // tile offsets from the aligned base
 constexpr uint32_t OFF_G1A = OFF_R1;
 constexpr uint32_t OFF_G1B = OFF_R1 + kTile128;
-constexpr uint32_t OFF_MT = OFF_R1;                 // fp32 64x64, swizzled
-constexpr uint32_t OFF_TT = OFF_R1 + kTile128;      // fp32 64x64, swizzled
-constexpr uint32_t OFF_G2B = OFF_R1;                // T (rows s, K = t)
+constexpr uint32_t OFF_TD = OFF_R1;                 // Tdiag rows (bf16, zero off the 16x16 blocks)
+constexpr uint32_t OFF_UT = OFF_R1 + kTile64;       // U = Mab off the diagonal blocks, rows
+constexpr uint32_t OFF_NT = OFF_R1 + 2 * kTile64;   // N = Tdiag U rows
+constexpr uint32_t OFF_MD = OFF_NT;                 // fp32 [64][16]: diagonal blocks of Mab
+constexpr uint32_t OFF_WT = OFF_R1 + 3 * kTile64;   // Horner iterate W, finally T (rows s, K = t)
+constexpr uint32_t OFF_G2B = OFF_WT;
 constexpr uint32_t OFF_OPZ = OFF_R1;
 constexpr uint32_t OFF_OPY = OFF_R1;
 constexpr uint32_t OFF_OPA2 = OFF_R1 + kTile128;
@@ -87,13 +97,6 @@ constexpr uint32_t kTileBytes = OFF_SLO + kTile64;
 constexpr uint32_t kSmemBytes = kSmallBytes + 1024 + kTileBytes;  // + worst-case alignment
 static_assert(2 * (kSmemBytes + 1024) <= 228 * 1024, "two CTAs per SM");
 constexpr uint32_t kTmemCols = 256;
-
-// Index of element (r, c) of a 64x64 fp32 scratch matrix: 4-float groups of a
-// row are permuted by XOR with (r % 16), so row-wise float4 access and
-// column-wise scalar access both spread over the banks.
-__device__ __forceinline__ int mt_idx(int r, int c) {
-    return r * 64 + ((((c >> 2) ^ (r & 15)) << 2) | (c & 3));
-}
 
 struct InputMaps {
     CUtensorMap m[6];  // r, w, k, v, a, b
@@ -171,127 +174,6 @@ __device__ __forceinline__ void load_row32(const uint8_t *tile, int row, int col
     }
 }
 
-__device__ __forceinline__ uint32_t to_tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
-}
-
-// d += a (16x8, tf32) * b (8x8, tf32), float accumulators; warp-wide.
-__device__ __forceinline__ void mma_tf32_16x8x8(float (&d)[4], uint32_t a0, uint32_t a1,
-                                                uint32_t a2, uint32_t a3, uint32_t b0,
-                                                uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// acc[n] (16 x 8 tile n of a 16x16 block) += A[ar.., ac..] (16x16) * B[br.., bc..]
-// (16x16) for the n-tiles nt0 .. nt0+ntc-1, on swizzled fp32 scratch; warp-wide.
-// Fragments: A (g, t), (g+8, t), (g, t+4), (g+8, t+4); B (t, g), (t+4, g);
-// accumulator (g, 2t), (g, 2t+1), (g+8, 2t), (g+8, 2t+1), g = lane/4, t = lane%4.
-__device__ __forceinline__ void block_mma(const float *A, int ar, int ac, const float *B, int br,
-                                          int bc, int nt0, int ntc, float (&acc)[2][4],
-                                          int lane) {
-    const int g = lane >> 2, t = lane & 3;
-#pragma unroll
-    for (int kk = 0; kk < 16; kk += 8) {
-        const uint32_t a0 = to_tf32(A[mt_idx(ar + g, ac + kk + t)]);
-        const uint32_t a1 = to_tf32(A[mt_idx(ar + g + 8, ac + kk + t)]);
-        const uint32_t a2 = to_tf32(A[mt_idx(ar + g, ac + kk + t + 4)]);
-        const uint32_t a3 = to_tf32(A[mt_idx(ar + g + 8, ac + kk + t + 4)]);
-#pragma unroll
-        for (int n = 0; n < 2; ++n) {
-            if (n < ntc) {
-                const int col = bc + 8 * (nt0 + n) + g;
-                const uint32_t b0 = to_tf32(B[mt_idx(br + kk + t, col)]);
-                const uint32_t b1 = to_tf32(B[mt_idx(br + kk + t + 4, col)]);
-                mma_tf32_16x8x8(acc[n], a0, a1, a2, a3, b0, b1);
-            }
-        }
-    }
-}
-
-__device__ __forceinline__ void block_store(float *C, int cr, int cc, int nt0, int ntc,
-                                            const float (&acc)[2][4], int lane) {
-    const int g = lane >> 2, t = lane & 3;
-#pragma unroll
-    for (int n = 0; n < 2; ++n) {
-        if (n < ntc) {
-            const int col = cc + 8 * (nt0 + n) + 2 * t;
-            *reinterpret_cast<float2 *>(C + mt_idx(cr + g, col)) = make_float2(acc[n][0], acc[n][1]);
-            *reinterpret_cast<float2 *>(C + mt_idx(cr + g + 8, col)) = make_float2(acc[n][2], acc[n][3]);
-        }
-    }
-}
-
-// T = (I - M)^-1 for the strictly upper triangular 64x64 M in MT (fp32),
-// result in TT (upper triangle and 16x16 diagonal blocks), blocked by 16:
-// diagonal blocks by substitution in float32, then T_pq = T_pp sum_{p<u<=q}
-// M_pu T_uq level by level (q - p = 1, 2, 3) with warp-level tf32 MMAs (the
-// blocks are 16x16; T is rounded to bf16 afterwards).  The lower 16x16
-// blocks of MT hold the sums.  All 128 threads take part; ends synchronised.
-__device__ __forceinline__ void invert_unit_upper(float *MT, float *TT, int tid) {
-    if (tid < 64) {
-        const int p = tid >> 4, c = tid & 15;
-        const int o = 16 * p;
-        float x[16];
-#pragma unroll
-        for (int r = 0; r < 16; ++r) x[r] = (r == c) ? 1.f : 0.f;
-#pragma unroll
-        for (int r = 14; r >= 0; --r) {
-            if (r < c) {
-                float acc = 0.f;
-#pragma unroll
-                for (int u = r + 1; u < 16; ++u) acc = fmaf(MT[mt_idx(o + r, o + u)], x[u], acc);
-                x[r] = acc;
-            }
-        }
-#pragma unroll
-        for (int r = 0; r < 16; ++r) TT[mt_idx(o + r, o + c)] = x[r];
-    }
-    __syncthreads();
-    const int warp = tid >> 5, lane = tid & 31;
-    // q - p = 1: blocks (0,1), (1,2), (2,3), one warp each
-    if (warp < 3) {
-        const int p = warp, q = warp + 1;
-        float acc[2][4] = {};
-        block_mma(MT, 16 * p, 16 * q, TT, 16 * q, 16 * q, 0, 2, acc, lane);
-        block_store(MT, 16 * q, 16 * p, 0, 2, acc, lane);
-        __syncwarp();
-        float tq[2][4] = {};
-        block_mma(TT, 16 * p, 16 * p, MT, 16 * q, 16 * p, 0, 2, tq, lane);
-        block_store(TT, 16 * p, 16 * q, 0, 2, tq, lane);
-    }
-    __syncthreads();
-    {  // q - p = 2: blocks (0,2), (1,3), one 8-column half per warp
-        const int p = warp >> 1, q = p + 2, nt = warp & 1;
-        float acc[2][4] = {};
-        block_mma(MT, 16 * p, 16 * (p + 1), TT, 16 * (p + 1), 16 * q, nt, 1, acc, lane);
-        block_mma(MT, 16 * p, 16 * q, TT, 16 * q, 16 * q, nt, 1, acc, lane);
-        block_store(MT, 16 * q, 16 * p, nt, 1, acc, lane);
-        __syncwarp();
-        float tq[2][4] = {};
-        block_mma(TT, 16 * p, 16 * p, MT, 16 * q, 16 * p, nt, 1, tq, lane);
-        block_store(TT, 16 * p, 16 * q, nt, 1, tq, lane);
-    }
-    __syncthreads();
-    if (warp < 2) {  // q - p = 3: block (0,3), one half per warp
-        const int nt = warp;
-        float acc[2][4] = {};
-#pragma unroll
-        for (int u = 1; u <= 3; ++u) block_mma(MT, 0, 16 * u, TT, 16 * u, 48, nt, 1, acc, lane);
-        block_store(MT, 48, 0, nt, 1, acc, lane);
-        __syncwarp();
-        float tq[2][4] = {};
-        block_mma(TT, 0, 0, MT, 48, 0, nt, 1, tq, lane);
-        block_store(TT, 0, 48, nt, 1, tq, lane);
-    }
-    __syncthreads();
-}
-
 // All threads wait on the barrier; returns false (uniformly) if any gave up.
 __device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, volatile int *flag) {
     if (!mbar_wait_bounded(bar, parity, kWaitCycles)) *flag = 1;
@@ -329,8 +211,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     volatile int *flag = reinterpret_cast<volatile int *>(small + SOFF_FLAG);
     float *tot = reinterpret_cast<float *>(small + SOFF_TOT);
     float *gam = reinterpret_cast<float *>(small + SOFF_GAM);
-    float *MT = reinterpret_cast<float *>(base + OFF_MT);
-    float *TT = reinterpret_cast<float *>(base + OFF_TT);
 
     if (warp == 0) tmem_alloc(smem_addr(holder), kTmemCols);
     if (tid == 0) {
@@ -344,10 +224,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     float *S = p.lv.states + static_cast<size_t>(slot) * p.lv.slot_stride + p.lv.layer_off +
                static_cast<size_t>(h) * kHeadFloats;
     {  // start state -> bf16 hi/lo operand tiles (rows i, K = j)
-        const int i = tid >> 1, c0 = 32 * (tid & 1);
-        float hi[32], lo[32];
+        const int i = tid >> 2, c0 = 16 * (tid & 3);
+        float hi[16], lo[16];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
+        for (int q = 0; q < 4; ++q) {
             float4 x = *reinterpret_cast<const float4 *>(S + i * kHeadSize + c0 + 4 * q);
             float xs[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
@@ -356,14 +236,16 @@ __global__ void __launch_bounds__(kThreads, 2)
                 lo[4 * q + e] = xs[e] - hi[4 * q + e];
             }
         }
-        store_row32(base + OFF_SHI, i, c0, hi);
-        store_row32(base + OFF_SLO, i, c0, lo);
+        store_row16(base + OFF_SHI, i, c0, hi);
+        store_row16(base + OFF_SLO, i, c0, lo);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *holder;
-    const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const int row = 32 * (warp & 3) + lane;  // tensor-memory lane (accumulator row) of this thread
+    const int cpart = 32 * (warp >> 2);      // this thread's 32-column part of each 64-column group
 
     // inputs as bf16 pairs: token t (absolute), channels 2*lane, 2*lane+1
     const uint32_t *gR = static_cast<const uint32_t *>(p.in.r);
@@ -384,28 +266,40 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int tc0 = t0 + c * kL;
         const int Lc = min(kL, t1 - tc0);
         const bool last = (c + 1 == n_chunks);
+
         // ---------------------------------------------------------- E phase
         {
-            const int tb = 16 * warp;  // this warp's 16 tokens; lane: channels 2l, 2l+1
+            const int tb = 8 * warp;  // this warp's 8 tokens; lane: channels 2l, 2l+1
             const int ch = 2 * lane;
-            float s0 = 0.f, s1 = 0.f;  // pass 1: this warp's log2-decay totals
+            uint32_t gw[8], ga[8], gb[8], gk[8], gr[8], gv[8];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const uint32_t wv = (tb + i < Lc) ? __ldg(gW + goff(tc0 + tb + i)) : 0x3F803F80u;
-                s0 += lg2_approx(bf16_lo(wv));
-                s1 += lg2_approx(bf16_hi(wv));
+            for (int i = 0; i < 8; ++i) {
+                const bool valid = tb + i < Lc;
+                const size_t o = goff(tc0 + tb + i);
+                gw[i] = valid ? __ldg(gW + o) : 0x3F803F80u;  // 1.0, 1.0
+                ga[i] = valid ? __ldg(gA + o) : 0u;
+                gb[i] = valid ? __ldg(gB + o) : 0u;
+                gk[i] = valid ? __ldg(gK + o) : 0u;
+                gr[i] = valid ? __ldg(gR + o) : 0u;
+                gv[i] = valid ? __ldg(gV + o) : 0u;
+            }
+            float s0 = 0.f, s1 = 0.f;  // this warp's log2-decay totals
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                s0 += lg2_approx(bf16_lo(gw[i]));
+                s1 += lg2_approx(bf16_hi(gw[i]));
             }
             tot[warp * 64 + ch] = s0;
             tot[warp * 64 + ch + 1] = s1;
             __syncthreads();
-            float G0 = 0.f, G1 = 0.f;  // running G (inclusive prefix) of channels ch, ch+1
-            for (int w2 = 0; w2 < warp; ++w2) {
-                G0 += tot[w2 * 64 + ch];
-                G1 += tot[w2 * 64 + ch + 1];
+            float G0 = 0.f, G1 = 0.f, Gm0 = 0.f, Gm1 = 0.f, G630 = 0.f, G631 = 0.f;
+#pragma unroll
+            for (int w2 = 0; w2 < 8; ++w2) {
+                const float x0 = tot[w2 * 64 + ch], x1 = tot[w2 * 64 + ch + 1];
+                if (w2 < warp) { G0 += x0; G1 += x1; }
+                if (w2 < 4) { Gm0 += x0; Gm1 += x1; }
+                G630 += x0; G631 += x1;
             }
-            const float Gm0 = tot[ch] + tot[64 + ch], Gm1 = tot[ch + 1] + tot[64 + ch + 1];
-            const float G630 = Gm0 + tot[128 + ch] + tot[192 + ch];
-            const float G631 = Gm1 + tot[128 + ch + 1] + tot[192 + ch + 1];
             if (warp == 0) {
                 gam[ch] = ex2_approx(G630);
                 gam[ch + 1] = ex2_approx(G631);
@@ -415,71 +309,55 @@ __global__ void __launch_bounds__(kThreads, 2)
             const float EL0 = ex2_approx(G630 - Gm0), EL1 = ex2_approx(G631 - Gm1);
             float ep0 = ex2_approx(G0 - Gm0), ep1 = ex2_approx(G1 - Gm1);  // e_prev
             float dp0 = ex2_approx(G0), dp1 = ex2_approx(G1);              // d_prev
-            // swizzled byte offset of (row tb + i, column ch) = rowbase + row part + xo[i & 7]
+            // swizzled byte offset of (row tb + i, column ch)
             const uint32_t xl = static_cast<uint32_t>(lane) >> 2;
+            const uint32_t rowbase = 1024u * warp + 4u * (lane & 3);
             uint8_t *g1a = base + OFF_G1A, *g1b = base + OFF_G1B, *r0t = base + OFF_R0;
-#pragma unroll 1
-            for (int half = 0; half < 2; ++half) {
-                const int tb8 = tb + 8 * half;
-                const uint32_t rowbase = 1024u * (tb8 >> 3) + 4u * (lane & 3);
-                uint32_t ga[8], gb[8], gk[8], gr[8], gv[8], gw[8];
+            uint32_t cb[4][2][4];  // channel-major operands [Bhat, Khat, A0, V][channel][pair]
+            float prv[4][2];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const bool valid = tb8 + i < Lc;
-                    const size_t o = goff(tc0 + tb8 + i);
-                    gw[i] = valid ? __ldg(gW + o) : 0x3F803F80u;
-                    ga[i] = valid ? __ldg(gA + o) : 0u;
-                    gb[i] = valid ? __ldg(gB + o) : 0u;
-                    gk[i] = valid ? __ldg(gK + o) : 0u;
-                    gr[i] = valid ? __ldg(gR + o) : 0u;
-                    gv[i] = valid ? __ldg(gV + o) : 0u;
-                }
-                uint32_t cb[4][2][4];  // channel-major operands [Bhat, Khat, A0, V][channel][pair]
-                float prv[4][2];
-#pragma unroll
-                for (int ii = 0; ii < 8; ++ii) {
-                    G0 += lg2_approx(bf16_lo(gw[ii]));
-                    G1 += lg2_approx(bf16_hi(gw[ii]));
-                    if (tb8 + ii < Lc &&
-                        !(fabsf(G0 - Gm0) <= kMaxLog2Range && fabsf(G1 - Gm1) <= kMaxLog2Range))
-                        range_bad = true;
-                    const float ec0 = ex2_approx(G0 - Gm0), ec1 = ex2_approx(G1 - Gm1);
-                    const float iv0 = ex2_approx(Gm0 - G0), iv1 = ex2_approx(Gm1 - G1);
-                    const float dc0 = ex2_approx(G0), dc1 = ex2_approx(G1);
-                    const float dl0 = EL0 * iv0, dl1 = EL1 * iv1;
-                    const float ax = bf16_lo(ga[ii]), ay = bf16_hi(ga[ii]);
-                    const float bx = bf16_lo(gb[ii]), by = bf16_hi(gb[ii]);
-                    const float kx = bf16_lo(gk[ii]), ky = bf16_hi(gk[ii]);
-                    const float rx = bf16_lo(gr[ii]), ry = bf16_hi(gr[ii]);
-                    const float vx = bf16_lo(gv[ii]), vy = bf16_hi(gv[ii]);
-                    const uint32_t off = rowbase + ii * 128 + ((xl ^ ii) << 4);
-                    *reinterpret_cast<uint32_t *>(g1a + off) = pack_bf16(bx * iv0, by * iv1);
-                    *reinterpret_cast<uint32_t *>(g1a + 8192 + off) = pack_bf16(kx * iv0, ky * iv1);
-                    *reinterpret_cast<uint32_t *>(g1b + off) = pack_bf16(ax * ep0, ay * ep1);
-                    *reinterpret_cast<uint32_t *>(g1b + 8192 + off) = pack_bf16(rx * ec0, ry * ec1);
-                    *reinterpret_cast<uint32_t *>(r0t + off) = pack_bf16(rx * dc0, ry * dc1);
-                    const float cv[4][2] = {{bx * dl0, by * dl1}, {kx * dl0, ky * dl1},
-                                            {ax * dp0, ay * dp1}, {vx, vy}};
-#pragma unroll
-                    for (int o = 0; o < 4; ++o)
-#pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            if ((ii & 1) == 0)
-                                prv[o][e] = cv[o][e];
-                            else
-                                cb[o][e][ii >> 1] = pack_bf16(prv[o][e], cv[o][e]);
-                        }
-                    ep0 = ec0; ep1 = ec1;
-                    dp0 = dc0; dp1 = dc1;
-                }
-                uint8_t *dst[4] = {base + OFF_G2A, base + OFF_KHT, base + OFF_G34B, base + OFF_V};
+            for (int ii = 0; ii < 8; ++ii) {
+                G0 += lg2_approx(bf16_lo(gw[ii]));
+                G1 += lg2_approx(bf16_hi(gw[ii]));
+                if (tb + ii < Lc &&
+                    !(fabsf(G0 - Gm0) <= kMaxLog2Range && fabsf(G1 - Gm1) <= kMaxLog2Range))
+                    range_bad = true;
+                const float ec0 = ex2_approx(G0 - Gm0), ec1 = ex2_approx(G1 - Gm1);
+                const float iv0 = ex2_approx(Gm0 - G0), iv1 = ex2_approx(Gm1 - G1);
+                const float dc0 = ex2_approx(G0), dc1 = ex2_approx(G1);
+                const float dl0 = EL0 * iv0, dl1 = EL1 * iv1;
+                const float ax = bf16_lo(ga[ii]), ay = bf16_hi(ga[ii]);
+                const float bx = bf16_lo(gb[ii]), by = bf16_hi(gb[ii]);
+                const float kx = bf16_lo(gk[ii]), ky = bf16_hi(gk[ii]);
+                const float rx = bf16_lo(gr[ii]), ry = bf16_hi(gr[ii]);
+                const float vx = bf16_lo(gv[ii]), vy = bf16_hi(gv[ii]);
+                const uint32_t off = rowbase + ii * 128 + ((xl ^ ii) << 4);
+                *reinterpret_cast<uint32_t *>(g1a + off) = pack_bf16(bx * iv0, by * iv1);
+                *reinterpret_cast<uint32_t *>(g1a + 8192 + off) = pack_bf16(kx * iv0, ky * iv1);
+                *reinterpret_cast<uint32_t *>(g1b + off) = pack_bf16(ax * ep0, ay * ep1);
+                *reinterpret_cast<uint32_t *>(g1b + 8192 + off) = pack_bf16(rx * ec0, ry * ec1);
+                *reinterpret_cast<uint32_t *>(r0t + off) = pack_bf16(rx * dc0, ry * dc1);
+                const float cv[4][2] = {{bx * dl0, by * dl1}, {kx * dl0, ky * dl1},
+                                        {ax * dp0, ay * dp1}, {vx, vy}};
 #pragma unroll
                 for (int o = 0; o < 4; ++o)
 #pragma unroll
-                    for (int e = 0; e < 2; ++e)  // 8 tokens of channel-major row ch + e
-                        *reinterpret_cast<uint4 *>(dst[o] + sw128_off(ch + e, tb8)) =
-                            make_uint4(cb[o][e][0], cb[o][e][1], cb[o][e][2], cb[o][e][3]);
+                    for (int e = 0; e < 2; ++e) {
+                        if ((ii & 1) == 0)
+                            prv[o][e] = cv[o][e];
+                        else
+                            cb[o][e][ii >> 1] = pack_bf16(prv[o][e], cv[o][e]);
+                    }
+                ep0 = ec0; ep1 = ec1;
+                dp0 = dc0; dp1 = dc1;
             }
+            uint8_t *dst[4] = {base + OFF_G2A, base + OFF_KHT, base + OFF_G34B, base + OFF_V};
+#pragma unroll
+            for (int o = 0; o < 4; ++o)
+#pragma unroll
+                for (int e = 0; e < 2; ++e)  // 8 tokens of channel-major row ch + e
+                    *reinterpret_cast<uint4 *>(dst[o] + sw128_off(ch + e, tb)) =
+                        make_uint4(cb[o][e][0], cb[o][e][1], cb[o][e][2], cb[o][e][3]);
         }
         fence_proxy_async_smem();
         __syncthreads();
@@ -500,39 +378,43 @@ __global__ void __launch_bounds__(kThreads, 2)
         tc_fence_after();
         {
             float v[16];
-            const int row = 32 * warp + lane;  // TMEM lane
-            if (warp < 2) {  // Mab row s: keep t > s, float32 for the inverse
-                const int s = row;
+            if (row < 64) {  // Mab row s: diagonal block (fp32) | off-diagonal U (bf16)
+                const int s = row, ps = s >> 4;
+                float *md = reinterpret_cast<float *>(base + OFF_MD);
 #pragma unroll 1
-                for (int g = 0; g < 4; ++g) {
-                    tmem_ld16(tmem + lane_base + 16 * g, v);
+                for (int g = 0; g < 2; ++g) {
+                    const int c00 = cpart + 16 * g;
+                    tmem_ld16(tmem + lane_base + c00, v);
                     tmem_ld_wait();
+                    const int pc = c00 >> 4;
+                    if (pc == ps) {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int t = 16 * g + 4 * q;
-                        float4 x = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-                        x.x = (t + 0 > s) ? x.x : 0.f; x.y = (t + 1 > s) ? x.y : 0.f;
-                        x.z = (t + 2 > s) ? x.z : 0.f; x.w = (t + 3 > s) ? x.w : 0.f;
-                        *reinterpret_cast<float4 *>(MT + mt_idx(s, t)) = x;
+                        for (int q = 0; q < 16; ++q) md[s * 16 + q] = (c00 + q > s) ? v[q] : 0.f;
+                    }
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) v[q] = (pc > ps) ? v[q] : 0.f;
+                    store_row16(base + OFF_UT, s, c00, v);
+                    if (pc != ps) {  // Tdiag is zero off its diagonal blocks
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) v[q] = 0.f;
+                        store_row16(base + OFF_TD, s, c00, v);
                     }
                 }
             } else {  // Mak row s' (keep s > s'), and Qb^T row t' (keep s <= t')
                 const int s = row - 64;
 #pragma unroll 1
-                for (int g = 0; g < 4; ++g) {
-                    tmem_ld16(tmem + lane_base + 16 * g, v);
+                for (int g = 0; g < 2; ++g) {
+                    const int c00 = cpart + 16 * g;
+                    tmem_ld16(tmem + lane_base + c00, v);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) v[q] = (16 * g + q > s) ? v[q] : 0.f;
-                    store_row16(base + OFF_G34B, 64 + s, 16 * g, v);
-                }
-#pragma unroll 1
-                for (int g = 0; g < 4; ++g) {
-                    tmem_ld16(tmem + lane_base + 128 + 16 * g, v);
+                    for (int q = 0; q < 16; ++q) v[q] = (c00 + q > s) ? v[q] : 0.f;
+                    store_row16(base + OFF_G34B, 64 + s, c00, v);
+                    tmem_ld16(tmem + lane_base + 128 + c00, v);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) v[q] = (16 * g + q <= s) ? v[q] : 0.f;
-                    store_row16(base + OFF_G2A, 64 + s, 16 * g, v);
+                    for (int q = 0; q < 16; ++q) v[q] = (c00 + q <= s) ? v[q] : 0.f;
+                    store_row16(base + OFF_G2A, 64 + s, c00, v);
                 }
             }
         }
@@ -540,21 +422,72 @@ __global__ void __launch_bounds__(kThreads, 2)
         __syncthreads();
 
         // ------------------------------------------------ T = (I - Mab)^-1
-        invert_unit_upper(MT, TT, tid);
-        {  // T (fp32, TT) -> bf16 operand over the dead MT region
-            const int s = tid >> 1, c0 = 32 * (tid & 1);
-            float x[32];
+        if (tid < 64) {  // Tdiag: column c of the 16x16 block p, by substitution in fp32
+            const int pb = tid >> 4, c = tid & 15;
+            const float *md = reinterpret_cast<const float *>(base + OFF_MD) + (16 * pb) * 16;
+            float x[16];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const float4 y = *reinterpret_cast<const float4 *>(TT + mt_idx(s, c0 + 4 * q));
-                x[4 * q] = y.x; x[4 * q + 1] = y.y; x[4 * q + 2] = y.z; x[4 * q + 3] = y.w;
+            for (int r = 0; r < 16; ++r) x[r] = (r == c) ? 1.f : 0.f;
+#pragma unroll
+            for (int r = 14; r >= 0; --r) {
+                float mrow[16];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float4 y = *reinterpret_cast<const float4 *>(md + r * 16 + 4 * q);
+                    mrow[4 * q] = y.x; mrow[4 * q + 1] = y.y; mrow[4 * q + 2] = y.z; mrow[4 * q + 3] = y.w;
+                }
+                float acc = 0.f;
+#pragma unroll
+                for (int u = r + 1; u < 16; ++u) acc = fmaf(mrow[u], x[u], acc);
+                if (r < c) x[r] = acc;
             }
 #pragma unroll
-            for (int q = 0; q < 32; ++q) x[q] = (c0 + q >= s) ? x[q] : 0.f;
-            store_row32(base + OFF_G2B, s, c0, x);
+            for (int r = 0; r < 16; ++r)
+                *reinterpret_cast<__nv_bfloat16 *>(base + OFF_TD + sw128_off(16 * pb + r, 16 * pb + c)) =
+                    __float2bfloat16_rn(x[r]);
         }
         fence_proxy_async_smem();
         __syncthreads();
+        // N = Tdiag U, then W <- Tdiag + N W three times (W0 = Tdiag): W3 = T
+#pragma unroll 1
+        for (int k = 0; k < 4; ++k) {
+            if (tid == 0) {
+                tc_fence_after();
+                if (k == 0)
+                    umma_128xNx64_bmn(tmem + 0, smem_addr(base + OFF_TD), smem_addr(base + OFF_UT), 64, false);
+                else
+                    umma_128xNx64_bmn(tmem + 0, smem_addr(base + OFF_NT),
+                                      smem_addr(base + (k == 1 ? OFF_TD : OFF_WT)), 64, false);
+                umma_commit(bar_mma);
+            }
+            if (!wait_all(bar_mma, ph_mma, flag)) break;
+            ph_mma ^= 1;
+            tc_fence_after();
+            if (row < 64) {
+                const int s = row, ps = s >> 4;
+                float v[16], add[16];
+#pragma unroll 1
+                for (int g = 0; g < 2; ++g) {
+                    const int c00 = cpart + 16 * g;
+                    tmem_ld16(tmem + lane_base + c00, v);
+                    tmem_ld_wait();
+                    if (k == 0) {
+                        store_row16(base + OFF_NT, s, c00, v);
+                    } else {
+                        if ((c00 >> 4) == ps) {
+                            load_row16(base + OFF_TD, s, c00, add);
+#pragma unroll
+                            for (int q = 0; q < 16; ++q) v[q] += add[q];
+                        }
+                        store_row16(base + OFF_WT, s, c00, v);
+                    }
+                }
+            }
+            tc_fence_before();
+            fence_proxy_async_smem();
+            __syncthreads();
+        }
+        if (*flag) break;
 
         // ------------------------------------------------------------- G2
         if (tid == 0) {
@@ -566,12 +499,13 @@ __global__ void __launch_bounds__(kThreads, 2)
         ph_mma ^= 1;
         tc_fence_after();
         {
-            float v0[32], v1[32];
-            tmem_ld32(tmem + lane_base + 0, v0);
-            tmem_ld32(tmem + lane_base + 32, v1);
-            tmem_ld_wait();
-            store_row32(base + OFF_OPZ, 32 * warp + lane, 0, v0);
-            store_row32(base + OFF_OPZ, 32 * warp + lane, 32, v1);
+            float v[16];
+#pragma unroll 1
+            for (int g = 0; g < 2; ++g) {
+                tmem_ld16(tmem + lane_base + cpart + 16 * g, v);
+                tmem_ld_wait();
+                store_row16(base + OFF_OPZ, row, cpart + 16 * g, v);
+            }
         }
         tc_fence_before();
         fence_proxy_async_smem();
@@ -588,45 +522,41 @@ __global__ void __launch_bounds__(kThreads, 2)
         tc_fence_after();
         {
             float v[16], add[16];
-            if (warp < 2) {  // row j: Phi^T = Phi'^T + diag(gamma); Y_B^T = Y'^T + Khat^T
-                const int j = 32 * warp + lane;
+            if (row < 64) {  // row j: Phi^T = Phi'^T + diag(gamma); Y_B^T = Y'^T + Khat^T
+                const int j = row;
                 const float gj = gam[j];
 #pragma unroll 1
-                for (int g = 0; g < 4; ++g) {
-                    tmem_ld16(tmem + lane_base + 16 * g, v);
+                for (int g = 0; g < 2; ++g) {
+                    const int c00 = cpart + 16 * g;
+                    tmem_ld16(tmem + lane_base + c00, v);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) v[q] += (16 * g + q == j) ? gj : 0.f;
-                    store_row16(base + OFF_OPA2, 64 + j, 16 * g, v);
-                }
-#pragma unroll 1
-                for (int g = 0; g < 4; ++g) {
-                    tmem_ld16(tmem + lane_base + 64 + 16 * g, v);
-                    load_row16(base + OFF_KHT, j, 16 * g, add);
+                    for (int q = 0; q < 16; ++q) v[q] += (c00 + q == j) ? gj : 0.f;
+                    store_row16(base + OFF_OPA2, 64 + j, c00, v);
+                    tmem_ld16(tmem + lane_base + 64 + c00, v);
+                    load_row16(base + OFF_KHT, j, c00, add);
                     tmem_ld_wait();
 #pragma unroll
                     for (int q = 0; q < 16; ++q) v[q] += add[q];
-                    store_row16(base + OFF_OPY, 64 + j, 16 * g, v);
+                    store_row16(base + OFF_OPY, 64 + j, c00, v);
                 }
             } else {  // row t': R'^T = R''^T + R0; Y_Q^T = Y'^T + Qk^T (causal: s <= t')
-                const int tq = 32 * warp + lane - 64;
+                const int tq = row - 64;
 #pragma unroll 1
-                for (int g = 0; g < 4; ++g) {
-                    tmem_ld16(tmem + lane_base + 16 * g, v);
-                    load_row16(base + OFF_R0, tq, 16 * g, add);
+                for (int g = 0; g < 2; ++g) {
+                    const int c00 = cpart + 16 * g;
+                    tmem_ld16(tmem + lane_base + c00, v);
+                    load_row16(base + OFF_R0, tq, c00, add);
                     tmem_ld_wait();
 #pragma unroll
                     for (int q = 0; q < 16; ++q) v[q] += add[q];
-                    store_row16(base + OFF_OPA2, tq, 16 * g, v);
-                }
-#pragma unroll 1
-                for (int g = 0; g < 4; ++g) {
-                    tmem_ld16(tmem + lane_base + 64 + 16 * g, v);
-                    tmem_ld16(tmem + lane_base + 192 + 16 * g, add);
+                    store_row16(base + OFF_OPA2, tq, c00, v);
+                    tmem_ld16(tmem + lane_base + 64 + c00, v);
+                    tmem_ld16(tmem + lane_base + 192 + c00, add);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) v[q] += (16 * g + q <= tq) ? add[q] : 0.f;
-                    store_row16(base + OFF_OPY, tq, 16 * g, v);
+                    for (int q = 0; q < 16; ++q) v[q] += (c00 + q <= tq) ? add[q] : 0.f;
+                    store_row16(base + OFF_OPY, tq, c00, v);
                 }
             }
         }
@@ -645,13 +575,13 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (!wait_all(bar_mma, ph_mma, flag)) break;
         ph_mma ^= 1;
         tc_fence_after();
-        if (warp < 2) {  // O row t' -> o[tc0 + t'][h][:]
-            const int tq = 32 * warp + lane;
-            float *dst = p.in.o + (static_cast<size_t>(tc0 + tq) * H + h) * kHeadSize;
+        if (row < 64) {  // O row t' -> o[tc0 + t'][h][cpart ..]
+            const int tq = row;
+            float *dst = p.in.o + (static_cast<size_t>(tc0 + tq) * H + h) * kHeadSize + cpart;
 #pragma unroll 1
-            for (int g = 0; g < 4; ++g) {
+            for (int g = 0; g < 2; ++g) {
                 float v[16];
-                tmem_ld16(tmem + lane_base + 128 + 16 * g, v);
+                tmem_ld16(tmem + lane_base + 128 + cpart + 16 * g, v);
                 tmem_ld_wait();
                 if (tq < Lc) {
 #pragma unroll
@@ -660,17 +590,17 @@ __global__ void __launch_bounds__(kThreads, 2)
                             make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
                 }
             }
-        } else {  // S_L column j (rows i) -> next chunk's hi/lo operand; last chunk -> slot
-            const int j = 32 * warp + lane - 64;
+        } else {  // S_L column j, rows i in this thread's part -> next chunk's hi/lo; last -> slot
+            const int j = row - 64;
             uint8_t *shi = base + OFF_SHI, *slo = base + OFF_SLO;
 #pragma unroll 1
-            for (int g = 0; g < 4; ++g) {
+            for (int g = 0; g < 2; ++g) {
                 float v[16];
-                tmem_ld16(tmem + lane_base + 128 + 16 * g, v);
+                tmem_ld16(tmem + lane_base + 128 + cpart + 16 * g, v);
                 tmem_ld_wait();
 #pragma unroll
                 for (int q = 0; q < 16; ++q) {
-                    const int i = 16 * g + q;
+                    const int i = cpart + 16 * g + q;
                     const __nv_bfloat16 hb = __float2bfloat16_rn(v[q]);
                     const float lo = v[q] - __bfloat162float(hb);
                     *reinterpret_cast<__nv_bfloat16 *>(shi + sw128_off(i, j)) = hb;

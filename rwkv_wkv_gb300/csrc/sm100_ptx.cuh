@@ -158,11 +158,26 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
     return d;
 }
 
+// Descriptor for an MN-major operand with the 128-byte swizzle: each 128-byte
+// row holds 64 consecutive M (or N) elements of one K index, 8-row atoms of
+// 1024 bytes stacked along K (stride byte offset 1024); atoms along M/N are
+// `mn_stride` bytes apart (leading byte offset).
+__device__ __forceinline__ uint64_t desc_sw128_mn(uint32_t saddr, uint32_t mn_stride) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((mn_stride >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(2) << 61;
+    return d;
+}
+
 // Instruction descriptor, kind::f16: bf16 A and B (format 1 in bits 7-9 and
 // 10-12), f32 accumulator (format 1 in bits 4-5), both operands K-major
 // (bits 15, 16 clear), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, uint32_t b_mn = 0) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn << 16) | ((N >> 3) << 17) |
+           ((M >> 4) << 24);
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T for one K=16 slice; issued by one thread.
@@ -194,6 +209,18 @@ __device__ __forceinline__ void umma_128xNx64(uint32_t d_tmem, uint32_t a_saddr,
     for (int k = 0; k < 4; ++k) {
         umma_bf16(d_tmem, desc_sw128(a_saddr + 32 * k), desc_sw128(b_saddr + 32 * k), idesc,
                   (accumulate || k > 0) ? 1u : 0u);
+    }
+}
+
+// As above with B stored MN-major (rows of 64 N-elements per K index, N <= 64):
+// the K=16 slices advance 2048 bytes (two 8-row atoms) through B.
+__device__ __forceinline__ void umma_128xNx64_bmn(uint32_t d_tmem, uint32_t a_saddr,
+                                                  uint32_t b_saddr, uint32_t N, bool accumulate) {
+    const uint32_t idesc = idesc_bf16_f32(128, N, 1);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        umma_bf16(d_tmem, desc_sw128(a_saddr + 32 * k), desc_sw128_mn(b_saddr + 2048 * k, 8192),
+                  idesc, (accumulate || k > 0) ? 1u : 0u);
     }
 }
 
