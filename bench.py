@@ -80,6 +80,37 @@ def load_peaks():
         return dict(FALLBACK_PEAKS)
 
 
+KERNEL_SOURCES = {
+    "prefill": ("prefill_chunk_kernel.mixed_prefill_64seq.md",
+                ["prefill_chunk.cu", "sm100_ptx.cuh", "device_common.cuh", "wkv7_internal.h"]),
+    "decode": ("decode_kernel.decode_12L_12H_256of1024.md",
+               ["decode.cu", "device_common.cuh", "wkv7_internal.h"]),
+}
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if that summary
+    was taken on this workload's launch shape and the kernel's sources are
+    unchanged since; else None."""
+    import hashlib
+    if kernel not in KERNEL_SOURCES or workload != "mixed" or kernel != "prefill":
+        return None
+    fname, sources = KERNEL_SOURCES[kernel]
+    try:
+        text = open(os.path.join(ROOT, "profiles", fname)).read()
+        m = hashlib.sha256()
+        for f in sources:
+            with open(os.path.join(ROOT, "rwkv_wkv_gb300", "csrc", f), "rb") as fh:
+                m.update(fh.read())
+    except OSError:
+        return None
+    fields = dict(line.strip().split(": ", 1) for line in text.splitlines()
+                  if line.strip().startswith(("dram_bytes_per_launch:", "source_sha256:")))
+    if fields.get("source_sha256") != m.hexdigest()[:16]:
+        return None
+    return int(fields["dram_bytes_per_launch"])
+
+
 def aggregate(elapsed_s: float, units: float, world: int, device=None):
     """Whole-job figures over ranks: max of the elapsed times, sum of the units."""
     if world <= 1:
@@ -558,7 +589,7 @@ def run_ours(args):
                 "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
                 "peak_source": peaks["source"] + " (hbm copy)",
                 "bytes_per_launch": wk.phase_bytes[dom], "ms_per_launch": round(dom_ms, 4),
-                "traffic": None}
+                "traffic": profiled_traffic(dom, args.workload)}
     phases = {}
     for n in wk.phases:
         ms = phase_ms.get(n)
