@@ -21,10 +21,10 @@
 // of shared memory and 256 tensor-memory columns each), so one CTA's MMA
 // waits and load latencies are covered by the other's CUDA-core phases.
 // Per chunk:
-//   E   bf16 inputs read from global memory (the chunk's six boxes were
-//       prefetched into L2 by TMA one chunk earlier) -> log2-decay prefix
-//       sums (one warp per 8 tokens, two channels per lane) -> scaled bf16
-//       operands in 128-byte swizzled K-major tiles.
+//   E   bf16 inputs, TMA-loaded into shared memory during the previous
+//       chunk's last MMA (and prefetched into L2 a chunk before that) ->
+//       log2-decay prefix sums (one warp per 8 tokens, two channels per lane)
+//       -> scaled bf16 operands in 128-byte swizzled K-major tiles.
 // Tensor-memory readbacks give warps w and w+4 the same 32 lanes (rows) and
 // split the columns between them.  Decays inside the Gram products are taken
 //       relative to the chunk midpoint (token 31), so no factor exceeds
@@ -34,12 +34,15 @@
 //   T   (I - Mab)^-1: with Mab = D + U (D its 16x16 diagonal blocks),
 //       T = (I + N + N^2 + N^3) Tdiag, Tdiag = (I - D)^-1 (float32 substitution
 //       on the CUDA cores, four 16x16 blocks), N = Tdiag U nilpotent of
-//       index 4; N and the three Horner steps W <- Tdiag + N W are UMMAs
-//       (M=128 with the upper 64 rows unused, B read MN-major)
+//       index 4; N, then [N Tdiag | N^2] in one N=128 UMMA, then
+//       T = W1 + N^2 W1 with W1 = Tdiag + N Tdiag (M=128 with the upper 64
+//       rows unused, B read MN-major)
 //   G2  [Bhat^T; Qb^T] x T^T -> Z^T                  (M=128, N=64)
 //   G34 Z^T x [A0^T; Mak]^T -> Phi'^T, R''^T, Y'^T   (M=128, N=128)
 //   G5  [Y_Q^T; Y_B^T] x V -> O0^T, Psi^T; then += [R'^T; Phi^T] x S0^T with
-//       S0 split into bf16 hi + lo (two MMAs)        (M=128, N=64)
+//       S0 split into bf16 hi + lo (two MMAs, B = S0^T rows read MN-major,
+//       so the accumulator's S_L^T rows are written back as they come)
+//                                                    (M=128, N=64)
 // Accumulators live in tensor memory (256 columns); the float32 state leaves
 // the accumulator each chunk, is written back as the next chunk's bf16 hi/lo
 // operand pair and, after the last chunk, to the slot in float32.
@@ -63,15 +66,15 @@ constexpr float kMaxLog2Range = 120.0f;           // |G - Gm| limit (float expon
 
 // Shared-memory map.  Small items first (from the raw base), then the tiles
 // from the next 1024-byte boundary.  Region R1 is reused through the chunk:
-// G1A | G1B (E -> G1)  ->  TD | UT | NT | WT (the inverse; NT first holds the
-// fp32 diagonal blocks of Mab, WT ends as T for G2)  ->  OPZ (-> G34)  ->
-// OPY | OPA2 (-> G5).
+// G1A | G1B (E -> G1)  ->  TD | UT (later N^2) | NT | WT (the inverse; NT first
+// holds the fp32 diagonal blocks of Mab, WT ends as T for G2)  ->  OPZ (-> G34)
+// ->  OPY | OPA2 (-> G5).
 constexpr uint32_t kTile64 = 8192;    // 64 rows x 128 B (bf16, K = 64)
 constexpr uint32_t kTile128 = 16384;  // 128 rows
 constexpr uint32_t SOFF_TOT = 0;                    // per-warp log2-decay totals [8][64] fp32
 constexpr uint32_t SOFF_GAM = SOFF_TOT + 8 * 64 * 4;  // D(0,L] per channel [64]
-constexpr uint32_t SOFF_BAR = SOFF_GAM + 64 * 4;    // one mbarrier (8 B)
-constexpr uint32_t SOFF_HOLD = SOFF_BAR + 8;        // tensor-memory base
+constexpr uint32_t SOFF_BAR = SOFF_GAM + 64 * 4;    // mbarriers: MMA completion, input TMA
+constexpr uint32_t SOFF_HOLD = SOFF_BAR + 16;       // tensor-memory base
 constexpr uint32_t SOFF_FLAG = SOFF_HOLD + 4;       // abort flag
 constexpr uint32_t kSmallBytes = SOFF_FLAG + 4;
 constexpr uint32_t OFF_R1 = 0;                      // tile offsets from the aligned base
@@ -81,7 +84,8 @@ constexpr uint32_t OFF_TD = OFF_R1;                 // Tdiag rows (bf16, zero of
 constexpr uint32_t OFF_UT = OFF_R1 + kTile64;       // U = Mab off the diagonal blocks, rows
 constexpr uint32_t OFF_NT = OFF_R1 + 2 * kTile64;   // N = Tdiag U rows
 constexpr uint32_t OFF_MD = OFF_NT;                 // fp32 [64][16]: diagonal blocks of Mab
-constexpr uint32_t OFF_WT = OFF_R1 + 3 * kTile64;   // Horner iterate W, finally T (rows s, K = t)
+constexpr uint32_t OFF_WT = OFF_R1 + 3 * kTile64;   // W1, finally T (rows s, K = t)
+constexpr uint32_t OFF_N2 = OFF_UT;                 // N^2 rows (over U, dead after the first UMMA)
 constexpr uint32_t OFF_G2B = OFF_WT;
 constexpr uint32_t OFF_OPZ = OFF_R1;
 constexpr uint32_t OFF_OPY = OFF_R1;
@@ -91,9 +95,17 @@ constexpr uint32_t OFF_G34B = OFF_G2A + kTile128;    // [A0^T; Mak]
 constexpr uint32_t OFF_V = OFF_G34B + kTile128;      // V^T (rows i, K = s)
 constexpr uint32_t OFF_KHT = OFF_V + kTile64;        // Khat^T (rows j, K = s)
 constexpr uint32_t OFF_R0 = OFF_KHT + kTile64;       // R0 (rows t, K = j)
-constexpr uint32_t OFF_SHI = OFF_R0 + kTile64;       // S0 hi (rows i, K = j)
-constexpr uint32_t OFF_SLO = OFF_SHI + kTile64;      // S0 lo
+constexpr uint32_t OFF_SHI = OFF_R0 + kTile64;       // S0^T hi (rows j, 64 values i; MN-major B)
+constexpr uint32_t OFF_SLO = OFF_SHI + kTile64;      // S0^T lo
 constexpr uint32_t kTileBytes = OFF_SLO + kTile64;
+// Staging of the next chunk's six input boxes ([64 tokens][64 channels] bf16,
+// 8 KB each), loaded by TMA into tiles that are dead from the end of the G34
+// readback until E has read its inputs (E reads them all before its first
+// barrier and writes these tiles only after it).
+__host__ __device__ constexpr uint32_t stage_off(int x) {  // r, w, k, v, a, b
+    return x == 0 ? OFF_G2A : x == 1 ? OFF_G2A + kTile64 : x == 2 ? OFF_G34B
+         : x == 3 ? OFF_G34B + kTile64 : x == 4 ? OFF_KHT : OFF_R0;
+}
 constexpr uint32_t kSmemBytes = kSmallBytes + 1024 + kTileBytes;  // + worst-case alignment
 static_assert(2 * (kSmemBytes + 1024) <= 228 * 1024, "two CTAs per SM");
 constexpr uint32_t kTmemCols = 256;
@@ -174,11 +186,12 @@ __device__ __forceinline__ void load_row32(const uint8_t *tile, int row, int col
     }
 }
 
-// All threads wait on the barrier; returns false (uniformly) if any gave up.
-__device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, volatile int *flag) {
+// Every thread waits on the MMA barrier itself.  A thread that gives up sets
+// the CTA's abort flag; the flag is read (uniformly) after the phase's closing
+// barrier, so a timed-out phase runs to that barrier on garbage and then the
+// CTA leaves.
+__device__ __forceinline__ void mma_wait(uint32_t bar, uint32_t parity, volatile int *flag) {
     if (!mbar_wait_bounded(bar, parity, kWaitCycles)) *flag = 1;
-    __syncthreads();
-    return *flag == 0;
 }
 
 __global__ void __launch_bounds__(kThreads, 2)
@@ -213,31 +226,34 @@ __global__ void __launch_bounds__(kThreads, 2)
     float *gam = reinterpret_cast<float *>(small + SOFF_GAM);
 
     if (warp == 0) tmem_alloc(smem_addr(holder), kTmemCols);
+    const uint32_t bar_tma = bar_mma + 8;
     if (tid == 0) {
         mbar_init(bar_mma, 1);
+        mbar_init(bar_tma, 1);
         fence_mbar_init();
         *flag = 0;
 #pragma unroll
         for (int x = 0; x < 6; ++x) prefetch_tensormap(&maps.m[x]);
+        mbar_arrive_expect_tx(bar_tma, 6 * kTile64);  // chunk 0's inputs
+#pragma unroll
+        for (int x = 0; x < 6; ++x)
+            tma_load_3d(smem_addr(base + stage_off(x)), &maps.m[x], 0, h, t0, bar_tma);
     }
 
     float *S = p.lv.states + static_cast<size_t>(slot) * p.lv.slot_stride + p.lv.layer_off +
                static_cast<size_t>(h) * kHeadFloats;
-    {  // start state -> bf16 hi/lo operand tiles (rows i, K = j)
-        const int i = tid >> 2, c0 = 16 * (tid & 3);
-        float hi[16], lo[16];
+    {  // start state -> bf16 hi/lo tiles of S^T (rows j = key, 64 value entries i per row):
+       // the MN-major B operand of the state product
+        const int j = tid & 63, i0 = 16 * (tid >> 6);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            float4 x = *reinterpret_cast<const float4 *>(S + i * kHeadSize + c0 + 4 * q);
-            float xs[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                hi[4 * q + e] = __bfloat162float(__float2bfloat16_rn(xs[e]));
-                lo[4 * q + e] = xs[e] - hi[4 * q + e];
-            }
+        for (int q = 0; q < 16; ++q) {
+            const int i = i0 + q;
+            const float x = S[i * kHeadSize + j];
+            const __nv_bfloat16 hb = __float2bfloat16_rn(x);
+            *reinterpret_cast<__nv_bfloat16 *>(base + OFF_SHI + sw128_off(j, i)) = hb;
+            *reinterpret_cast<__nv_bfloat16 *>(base + OFF_SLO + sw128_off(j, i)) =
+                __float2bfloat16_rn(x - __bfloat162float(hb));
         }
-        store_row16(base + OFF_SHI, i, c0, hi);
-        store_row16(base + OFF_SLO, i, c0, lo);
     }
     tc_fence_before();
     __syncthreads();
@@ -247,19 +263,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int row = 32 * (warp & 3) + lane;  // tensor-memory lane (accumulator row) of this thread
     const int cpart = 32 * (warp >> 2);      // this thread's 32-column part of each 64-column group
 
-    // inputs as bf16 pairs: token t (absolute), channels 2*lane, 2*lane+1
-    const uint32_t *gR = static_cast<const uint32_t *>(p.in.r);
-    const uint32_t *gW = static_cast<const uint32_t *>(p.in.w);
-    const uint32_t *gK = static_cast<const uint32_t *>(p.in.k);
-    const uint32_t *gV = static_cast<const uint32_t *>(p.in.v);
-    const uint32_t *gA = static_cast<const uint32_t *>(p.in.a);
-    const uint32_t *gB = static_cast<const uint32_t *>(p.in.b);
-    auto goff = [&](int t) -> size_t {
-        return (static_cast<size_t>(t) * H + h) * (kHeadSize / 2) + lane;
-    };
-
     const int n_chunks = (len + kL - 1) / kL;
-    uint32_t ph_mma = 0;
+    uint32_t ph_mma = 0, ph_tma = 0;
     bool range_bad = false;
 
     for (int c = 0; c < n_chunks; ++c) {
@@ -272,16 +277,23 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int tb = 8 * warp;  // this warp's 8 tokens; lane: channels 2l, 2l+1
             const int ch = 2 * lane;
             uint32_t gw[8], ga[8], gb[8], gk[8], gr[8], gv[8];
+            mma_wait(bar_tma, ph_tma, flag);
+            ph_tma ^= 1;
+            {
+                auto st = [&](int x, int t) -> uint32_t {
+                    return *reinterpret_cast<const uint32_t *>(base + stage_off(x) + t * 128 + 4 * lane);
+                };
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const bool valid = tb + i < Lc;
-                const size_t o = goff(tc0 + tb + i);
-                gw[i] = valid ? __ldg(gW + o) : 0x3F803F80u;  // 1.0, 1.0
-                ga[i] = valid ? __ldg(gA + o) : 0u;
-                gb[i] = valid ? __ldg(gB + o) : 0u;
-                gk[i] = valid ? __ldg(gK + o) : 0u;
-                gr[i] = valid ? __ldg(gR + o) : 0u;
-                gv[i] = valid ? __ldg(gV + o) : 0u;
+                for (int i = 0; i < 8; ++i) {
+                    const int t = tb + i;
+                    const bool valid = t < Lc;
+                    gr[i] = valid ? st(0, t) : 0u;
+                    gw[i] = valid ? st(1, t) : 0x3F803F80u;  // 1.0, 1.0
+                    gk[i] = valid ? st(2, t) : 0u;
+                    gv[i] = valid ? st(3, t) : 0u;
+                    ga[i] = valid ? st(4, t) : 0u;
+                    gb[i] = valid ? st(5, t) : 0u;
+                }
             }
             float s0 = 0.f, s1 = 0.f;  // this warp's log2-decay totals
 #pragma unroll
@@ -373,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 for (int x = 0; x < 6; ++x) tma_prefetch_l2_3d(&maps.m[x], 0, h, tc0 + kL);
             }
         }
-        if (!wait_all(bar_mma, ph_mma, flag)) break;
+        mma_wait(bar_mma, ph_mma, flag);
         ph_mma ^= 1;
         tc_fence_after();
         {
@@ -420,6 +432,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         tc_fence_before();
         __syncthreads();
+        if (*flag) break;
 
         // ------------------------------------------------ T = (I - Mab)^-1
         if (tid < 64) {  // Tdiag: column c of the 16x16 block p, by substitution in fp32
@@ -448,19 +461,22 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         fence_proxy_async_smem();
         __syncthreads();
-        // N = Tdiag U, then W <- Tdiag + N W three times (W0 = Tdiag): W3 = T
+        // N = Tdiag U;  [N Tdiag | N^2] in one N=128 UMMA (B = [TD | NT] MN-major);
+        // W1 = Tdiag + N Tdiag;  T = W1 + N^2 W1 = (I + N + N^2 + N^3) Tdiag.
 #pragma unroll 1
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < 3; ++k) {
             if (tid == 0) {
                 tc_fence_after();
                 if (k == 0)
                     umma_128xNx64_bmn(tmem + 0, smem_addr(base + OFF_TD), smem_addr(base + OFF_UT), 64, false);
+                else if (k == 1)
+                    umma_128xNx64_bmn(tmem + 0, smem_addr(base + OFF_NT), smem_addr(base + OFF_TD), 128,
+                                      false, OFF_NT - OFF_TD);
                 else
-                    umma_128xNx64_bmn(tmem + 0, smem_addr(base + OFF_NT),
-                                      smem_addr(base + (k == 1 ? OFF_TD : OFF_WT)), 64, false);
+                    umma_128xNx64_bmn(tmem + 0, smem_addr(base + OFF_N2), smem_addr(base + OFF_WT), 64, false);
                 umma_commit(bar_mma);
             }
-            if (!wait_all(bar_mma, ph_mma, flag)) break;
+            mma_wait(bar_mma, ph_mma, flag);
             ph_mma ^= 1;
             tc_fence_after();
             if (row < 64) {
@@ -470,15 +486,22 @@ __global__ void __launch_bounds__(kThreads, 2)
                 for (int g = 0; g < 2; ++g) {
                     const int c00 = cpart + 16 * g;
                     tmem_ld16(tmem + lane_base + c00, v);
+                    if (k == 1) tmem_ld16(tmem + lane_base + 64 + c00, add);
                     tmem_ld_wait();
-                    if (k == 0) {
+                    if (k == 0) {  // N
                         store_row16(base + OFF_NT, s, c00, v);
-                    } else {
+                    } else if (k == 1) {  // W1 = Tdiag + N Tdiag ; N^2
+                        store_row16(base + OFF_N2, s, c00, add);
                         if ((c00 >> 4) == ps) {
                             load_row16(base + OFF_TD, s, c00, add);
 #pragma unroll
                             for (int q = 0; q < 16; ++q) v[q] += add[q];
                         }
+                        store_row16(base + OFF_WT, s, c00, v);
+                    } else {  // T = W1 + N^2 W1
+                        load_row16(base + OFF_WT, s, c00, add);
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) v[q] += add[q];
                         store_row16(base + OFF_WT, s, c00, v);
                     }
                 }
@@ -486,6 +509,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             tc_fence_before();
             fence_proxy_async_smem();
             __syncthreads();
+            if (*flag) break;
         }
         if (*flag) break;
 
@@ -495,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             umma_128xNx64(tmem + 0, smem_addr(base + OFF_G2A), smem_addr(base + OFF_G2B), 64, false);
             umma_commit(bar_mma);
         }
-        if (!wait_all(bar_mma, ph_mma, flag)) break;
+        mma_wait(bar_mma, ph_mma, flag);
         ph_mma ^= 1;
         tc_fence_after();
         {
@@ -510,6 +534,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         tc_fence_before();
         fence_proxy_async_smem();
         __syncthreads();
+        if (*flag) break;
 
         // ------------------------------------------------------------ G34
         if (tid == 0) {
@@ -517,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             umma_128xNx64(tmem + 0, smem_addr(base + OFF_OPZ), smem_addr(base + OFF_G34B), 128, false);
             umma_commit(bar_mma);
         }
-        if (!wait_all(bar_mma, ph_mma, flag)) break;
+        mma_wait(bar_mma, ph_mma, flag);
         ph_mma ^= 1;
         tc_fence_after();
         {
@@ -563,16 +588,23 @@ __global__ void __launch_bounds__(kThreads, 2)
         tc_fence_before();
         fence_proxy_async_smem();
         __syncthreads();
+        if (*flag) break;
 
         // ---------------------------------- G5 and the state product S0 [R'|Phi]
         if (tid == 0) {
+            if (!last) {  // the staging tiles are dead now: fetch the next chunk's inputs
+                mbar_arrive_expect_tx(bar_tma, 6 * kTile64);
+#pragma unroll
+                for (int x = 0; x < 6; ++x)
+                    tma_load_3d(smem_addr(base + stage_off(x)), &maps.m[x], 0, h, tc0 + kL, bar_tma);
+            }
             tc_fence_after();
             umma_128xNx64(tmem + 128, smem_addr(base + OFF_OPY), smem_addr(base + OFF_V), 64, false);
-            umma_128xNx64(tmem + 128, smem_addr(base + OFF_OPA2), smem_addr(base + OFF_SHI), 64, true);
-            umma_128xNx64(tmem + 128, smem_addr(base + OFF_OPA2), smem_addr(base + OFF_SLO), 64, true);
+            umma_128xNx64_bmn(tmem + 128, smem_addr(base + OFF_OPA2), smem_addr(base + OFF_SHI), 64, true);
+            umma_128xNx64_bmn(tmem + 128, smem_addr(base + OFF_OPA2), smem_addr(base + OFF_SLO), 64, true);
             umma_commit(bar_mma);
         }
-        if (!wait_all(bar_mma, ph_mma, flag)) break;
+        mma_wait(bar_mma, ph_mma, flag);
         ph_mma ^= 1;
         tc_fence_after();
         if (row < 64) {  // O row t' -> o[tc0 + t'][h][cpart ..]
@@ -590,33 +622,37 @@ __global__ void __launch_bounds__(kThreads, 2)
                             make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
                 }
             }
-        } else {  // S_L column j, rows i in this thread's part -> next chunk's hi/lo; last -> slot
+        } else {  // S_L^T row j (values i of this thread's part) -> next chunk's hi/lo; last -> slot
             const int j = row - 64;
-            uint8_t *shi = base + OFF_SHI, *slo = base + OFF_SLO;
 #pragma unroll 1
             for (int g = 0; g < 2; ++g) {
-                float v[16];
-                tmem_ld16(tmem + lane_base + 128 + cpart + 16 * g, v);
+                const int i0 = cpart + 16 * g;
+                float v[16], hi[16], lo[16];
+                tmem_ld16(tmem + lane_base + 128 + i0, v);
                 tmem_ld_wait();
 #pragma unroll
                 for (int q = 0; q < 16; ++q) {
-                    const int i = cpart + 16 * g + q;
-                    const __nv_bfloat16 hb = __float2bfloat16_rn(v[q]);
-                    const float lo = v[q] - __bfloat162float(hb);
-                    *reinterpret_cast<__nv_bfloat16 *>(shi + sw128_off(i, j)) = hb;
-                    *reinterpret_cast<__nv_bfloat16 *>(slo + sw128_off(i, j)) = __float2bfloat16_rn(lo);
-                    if (last) S[i * kHeadSize + j] = v[q];
+                    hi[q] = __bfloat162float(__float2bfloat16_rn(v[q]));
+                    lo[q] = v[q] - hi[q];
+                }
+                store_row16(base + OFF_SHI, j, i0, hi);
+                store_row16(base + OFF_SLO, j, i0, lo);
+                if (last) {
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) S[(i0 + q) * kHeadSize + j] = v[q];
                 }
             }
         }
         tc_fence_before();
         fence_proxy_async_smem();
         __syncthreads();
+        if (*flag) break;
     }
 
     if (*flag) {  // a wait gave up: give in-flight MMAs a last chance, then leave
         if (tid == 0) flag_status(p.lv.status, WKV7_DEV_WAIT_TIMEOUT);
         mbar_wait_bounded(bar_mma, ph_mma, kWaitCycles);
+        mbar_wait_bounded(bar_tma, ph_tma, kWaitCycles);
     }
     if (range_bad) flag_status(p.lv.status, WKV7_DEV_DECAY_RANGE);
     tc_fence_before();

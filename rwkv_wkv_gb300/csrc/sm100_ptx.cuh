@@ -212,15 +212,18 @@ __device__ __forceinline__ void umma_128xNx64(uint32_t d_tmem, uint32_t a_saddr,
     }
 }
 
-// As above with B stored MN-major (rows of 64 N-elements per K index, N <= 64):
-// the K=16 slices advance 2048 bytes (two 8-row atoms) through B.
+// As above with B stored MN-major: rows of 64 N-elements per K index, 64-wide
+// N atoms `b_atom_stride` bytes apart (N = 128 uses two); the K=16 slices
+// advance 2048 bytes (two 8-row atoms) through B.
 __device__ __forceinline__ void umma_128xNx64_bmn(uint32_t d_tmem, uint32_t a_saddr,
-                                                  uint32_t b_saddr, uint32_t N, bool accumulate) {
+                                                  uint32_t b_saddr, uint32_t N, bool accumulate,
+                                                  uint32_t b_atom_stride = 8192) {
     const uint32_t idesc = idesc_bf16_f32(128, N, 1);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        umma_bf16(d_tmem, desc_sw128(a_saddr + 32 * k), desc_sw128_mn(b_saddr + 2048 * k, 8192),
-                  idesc, (accumulate || k > 0) ? 1u : 0u);
+        umma_bf16(d_tmem, desc_sw128(a_saddr + 32 * k),
+                  desc_sw128_mn(b_saddr + 2048 * k, b_atom_stride), idesc,
+                  (accumulate || k > 0) ? 1u : 0u);
     }
 }
 
