@@ -245,10 +245,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     {  // start state -> bf16 hi/lo tiles of S^T (rows j = key, 64 value entries i per row):
        // the MN-major B operand of the state product
         const int j = tid & 63, i0 = 16 * (tid >> 6);
+        float xs[16];  // all loads issued before any shared-memory store
+#pragma unroll
+        for (int q = 0; q < 16; ++q) xs[q] = __ldcg(S + (i0 + q) * kHeadSize + j);
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
             const int i = i0 + q;
-            const float x = S[i * kHeadSize + j];
+            const float x = xs[q];
             const __nv_bfloat16 hb = __float2bfloat16_rn(x);
             *reinterpret_cast<__nv_bfloat16 *>(base + OFF_SHI + sw128_off(j, i)) = hb;
             *reinterpret_cast<__nv_bfloat16 *>(base + OFF_SLO + sw128_off(j, i)) =
