@@ -595,17 +595,17 @@ __global__ void __launch_bounds__(kThreads, 2)
 
         // ---------------------------------- G5 and the state product S0 [R'|Phi]
         if (tid == 0) {
+            tc_fence_after();
+            umma_128xNx64(tmem + 128, smem_addr(base + OFF_OPY), smem_addr(base + OFF_V), 64, false);
+            umma_128xNx64_bmn(tmem + 128, smem_addr(base + OFF_OPA2), smem_addr(base + OFF_SHI), 64, true);
+            umma_128xNx64_bmn(tmem + 128, smem_addr(base + OFF_OPA2), smem_addr(base + OFF_SLO), 64, true);
+            umma_commit(bar_mma);
             if (!last) {  // the staging tiles are dead now: fetch the next chunk's inputs
                 mbar_arrive_expect_tx(bar_tma, 6 * kTile64);
 #pragma unroll
                 for (int x = 0; x < 6; ++x)
                     tma_load_3d(smem_addr(base + stage_off(x)), &maps.m[x], 0, h, tc0 + kL, bar_tma);
             }
-            tc_fence_after();
-            umma_128xNx64(tmem + 128, smem_addr(base + OFF_OPY), smem_addr(base + OFF_V), 64, false);
-            umma_128xNx64_bmn(tmem + 128, smem_addr(base + OFF_OPA2), smem_addr(base + OFF_SHI), 64, true);
-            umma_128xNx64_bmn(tmem + 128, smem_addr(base + OFF_OPA2), smem_addr(base + OFF_SLO), 64, true);
-            umma_commit(bar_mma);
         }
         mma_wait(bar_mma, ph_mma, flag);
         ph_mma ^= 1;
