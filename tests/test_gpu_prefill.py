@@ -147,3 +147,58 @@ def test_chunked_and_sequential_agree():
             outs.append((o, pool.states[:, 0].cpu().numpy()))
     assert rel(outs[0][0], outs[1][0]) < PREFILL_TOL
     assert rel(outs[0][1], outs[1][1]) < PREFILL_TOL
+
+
+def test_decay_beyond_the_chunk_factorisation_is_flagged():
+    """A channel whose decay over half a chunk exceeds 2^120 (w = 2^-8 for 40
+    tokens) makes the chunked path flag WKV7_DEV_DECAY_RANGE; the float32
+    token-by-token path takes the same inputs and still matches the oracle."""
+    from rwkv_wkv_gb300 import DEV_DECAY_RANGE
+    H, N, T = 2, 64, 40
+    ins = wl.token_inputs(31, "decay", T, H, N, dtype="bf16")
+    ins["w"] = ins["w"].copy()
+    ins["w"][:, 1, 5] = 2.0 ** -8
+    cu = wl.cu_seqlens([T])
+    with Pool(1, H, 2) as pool:
+        pool.create(1)
+        pool.prefill(0, i32([0]), i32(cu), *dev_inputs(ins, "bf16"), max_seqlen=T)
+        assert pool.device_status() == DEV_DECAY_RANGE
+        pool.states.zero_()
+        o_seq, code = _run(pool, [0], cu, ins, sequential=True)
+        assert code == 0
+        S_seq = pool.states[0, 0].cpu().numpy()
+    o_ref, S_ref = oracle.prefill(np.zeros((1, H, N, N)), cu, *host_inputs(ins))
+    assert rel(o_seq, o_ref) < SEQ_PREFILL_TOL
+    assert rel(S_seq, S_ref[0]) < SEQ_PREFILL_TOL
+
+
+@pytest.mark.parametrize("sequential", [False, True])
+def test_all_sequences_empty(sequential):
+    H, N = 2, 64
+    ins = wl.token_inputs(2, "empty", 1, H, N, dtype="bf16")
+    with Pool(1, H, 4) as pool:
+        pool.states.fill_(0.25)
+        dev = [x[:0] for x in dev_inputs(ins, "bf16")]
+        o = pool.prefill(0, i32([1, 3]), i32([0, 0, 0]), *dev, max_seqlen=0,
+                         sequential=sequential)
+        assert o.shape == (0, H, N)
+        assert pool.device_status() == 0
+        assert bool((pool.states == 0.25).all())
+
+
+def test_chunked_prefill_is_deterministic():
+    """Same inputs and start states -> the same bits (no atomics, fixed order)."""
+    H, N = 4, 64
+    lengths = [777, 64, 1, 130]
+    cu = wl.cu_seqlens(lengths)
+    ins = wl.token_inputs(12, "det", int(cu[-1]), H, N, dtype="bf16")
+    S0 = torch.from_numpy(wl.slot_states(12, "state", range(4), 1, H, N)[:, 0]).cuda()
+    runs = []
+    with Pool(1, H, 4) as pool:
+        for _ in range(2):
+            pool.states[:, 0] = S0
+            o, code = _run(pool, [2, 0, 3, 1], cu, ins, sequential=False)
+            assert code == 0
+            runs.append((o, pool.states.cpu().numpy()))
+    np.testing.assert_array_equal(runs[0][0], runs[1][0])
+    np.testing.assert_array_equal(runs[0][1], runs[1][1])
