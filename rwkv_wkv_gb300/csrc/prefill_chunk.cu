@@ -31,12 +31,11 @@
 //       2^(half-chunk decay); factors that meet S0 are relative to the start.
 //   G1  [Bbar;Kbar] x Am^T  -> Mab, Mak rows        (M=128, N=64,  K=64)
 //   G1' [Am;Rm] x [Bbar;Kbar]^T -> Qb^T, Qk^T rows  (M=128, N=128, K=64)
-//   T   (I - Mab)^-1: with Mab = D + U (D its 16x16 diagonal blocks),
-//       T = (I + N + N^2 + N^3) Tdiag, Tdiag = (I - D)^-1 (float32 substitution
-//       on the CUDA cores, four 16x16 blocks), N = Tdiag U nilpotent of
-//       index 4; N, then [N Tdiag | N^2] in one N=128 UMMA, then
-//       T = W1 + N^2 W1 with W1 = Tdiag + N Tdiag (M=128 with the upper 64
-//       rows unused, B read MN-major)
+//   T   (I - Mab)^-1 in fp32 on the CUDA cores, by 16x16 blocks: the four
+//       diagonal blocks T_ii = (I - M_ii)^-1 by back substitution (two warps,
+//       while the other warps read the rest of G1 back), then N_ij = T_ii M_ij
+//       and the off-diagonal blocks one block diagonal at a time,
+//       T_ij = sum_{i<k<=j} N_ik T_kj; T goes to shared memory in bf16
 //   G2  [Bhat^T; Qb^T] x T^T -> Z^T                  (M=128, N=64)
 //   G34 Z^T x [A0^T; Mak]^T -> Phi'^T, R''^T, Y'^T   (M=128, N=128)
 //   G5  [Y_Q^T; Y_B^T] x V -> O0^T, Psi^T; then += [R'^T; Phi^T] x S0^T with
@@ -66,9 +65,8 @@ constexpr float kMaxLog2Range = 120.0f;           // |G - Gm| limit (float expon
 
 // Shared-memory map.  Small items first (from the raw base), then the tiles
 // from the next 1024-byte boundary.  Region R1 is reused through the chunk:
-// G1A | G1B (E -> G1)  ->  TD | UT (later N^2) | NT | WT (the inverse; NT first
-// holds the fp32 diagonal blocks of Mab, WT ends as T for G2)  ->  OPZ (-> G34)
-// ->  OPY | OPA2 (-> G5).
+// G1A | G1B (E -> G1)  ->  fp32 blocks of the inverse | WT (T in bf16 for G2)
+// ->  OPZ (-> G34)  ->  OPY | OPA2 (-> G5).
 constexpr uint32_t kTile64 = 8192;    // 64 rows x 128 B (bf16, K = 64)
 constexpr uint32_t kTile128 = 16384;  // 128 rows
 constexpr uint32_t SOFF_TOT = 0;                    // per-warp log2-decay totals [8][64] fp32
@@ -80,12 +78,13 @@ constexpr uint32_t kSmallBytes = SOFF_FLAG + 4;
 constexpr uint32_t OFF_R1 = 0;                      // tile offsets from the aligned base
 constexpr uint32_t OFF_G1A = OFF_R1;
 constexpr uint32_t OFF_G1B = OFF_R1 + kTile128;
-constexpr uint32_t OFF_TD = OFF_R1;                 // Tdiag rows (bf16, zero off the 16x16 blocks)
-constexpr uint32_t OFF_UT = OFF_R1 + kTile64;       // U = Mab off the diagonal blocks, rows
-constexpr uint32_t OFF_NT = OFF_R1 + 2 * kTile64;   // N = Tdiag U rows
-constexpr uint32_t OFF_MD = OFF_NT;                 // fp32 [64][16]: diagonal blocks of Mab
-constexpr uint32_t OFF_WT = OFF_R1 + 3 * kTile64;   // W1, finally T (rows s, K = t)
-constexpr uint32_t OFF_N2 = OFF_UT;                 // N^2 rows (over U, dead after the first UMMA)
+// fp32 16x16 blocks of the inverse, 80-byte rows (conflict-free float4 rows):
+// slots 0-3 M_ii then T_ii, 4-9 M_ij (i < j), 10-15 N_ij = T_ii M_ij, 16-18 T_12, T_23, T_13
+constexpr int kSlotRow = 20;                          // floats per block row
+constexpr uint32_t kSlotBytes = 16 * kSlotRow * 4;
+constexpr int kSlotM = 4, kSlotN = 10, kSlotT = 16;
+constexpr uint32_t OFF_WT = OFF_R1 + 3 * kTile64;   // T in bf16 (rows s, K = t)
+static_assert(19 * kSlotBytes <= OFF_WT - OFF_R1, "inverse blocks overlap T");
 constexpr uint32_t OFF_G2B = OFF_WT;
 constexpr uint32_t OFF_OPZ = OFF_R1;
 constexpr uint32_t OFF_OPY = OFF_R1;
@@ -106,6 +105,8 @@ __host__ __device__ constexpr uint32_t stage_off(int x) {  // r, w, k, v, a, b
     return x == 0 ? OFF_G2A : x == 1 ? OFF_G2A + kTile64 : x == 2 ? OFF_G34B
          : x == 3 ? OFF_G34B + kTile64 : x == 4 ? OFF_KHT : OFF_R0;
 }
+// Index of the strictly-upper 16x16 block (i, j), i < j < 4, in 0..5.
+__device__ __forceinline__ int up_idx(int i, int j) { return i * (7 - i) / 2 + (j - i - 1); }
 constexpr uint32_t kSmemBytes = kSmallBytes + 1024 + kTileBytes;  // + worst-case alignment
 static_assert(2 * (kSmemBytes + 1024) <= 228 * 1024, "two CTAs per SM");
 constexpr uint32_t kTmemCols = 256;
@@ -130,23 +131,6 @@ __device__ __forceinline__ float lg2_approx(float x) {
     float y;
     asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
-}
-
-__device__ __forceinline__ float bf16_to_f(uint16_t u) {
-    return __uint_as_float(static_cast<uint32_t>(u) << 16);
-}
-
-// Write 32 floats as bf16 into columns col0..col0+31 of `row` of a swizzled tile.
-__device__ __forceinline__ void store_row32(uint8_t *tile, int row, int col0, const float *v) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        uint4 u;
-        u.x = pack_bf16(v[8 * q + 0], v[8 * q + 1]);
-        u.y = pack_bf16(v[8 * q + 2], v[8 * q + 3]);
-        u.z = pack_bf16(v[8 * q + 4], v[8 * q + 5]);
-        u.w = pack_bf16(v[8 * q + 6], v[8 * q + 7]);
-        *reinterpret_cast<uint4 *>(tile + sw128_off(row, col0 + 8 * q)) = u;
-    }
 }
 
 // Write 16 floats as bf16 into columns col0..col0+15 of `row` of a swizzled tile.
@@ -174,16 +158,74 @@ __device__ __forceinline__ void load_row16(const uint8_t *tile, int row, int col
     }
 }
 
-// Read 32 bf16 of `row` (columns col0..) of a swizzled tile as floats.
-__device__ __forceinline__ void load_row32(const uint8_t *tile, int row, int col0, float *v) {
+// Longest-first order of the sequences (by chunk count, capped at 255; ties in
+// index order), so that the CTAs of the longest sequences start first and the
+// ragged tail of the grid is short.  The grid is (head, rank) with the rank
+// split over y and z.
+// Every CTA derives the same order from cu_seqlens; `work` is 1.1 KB of shared
+// memory.  Returns the sequence of the given rank.
+constexpr int kMaxRankedSeqs = 4096;
+constexpr unsigned kGridY = 65535;
+
+__device__ __forceinline__ int chunk_key(const int *cu, int q) {
+    const int n = (__ldg(cu + q + 1) - __ldg(cu + q) + kL - 1) / kL;
+    return 255 - min(max(n, 0), 255);  // bin 0 holds the longest sequences
+}
+
+// Exclusive prefix sum over the CTA of one value per thread; `sums` holds 8 ints.
+__device__ __forceinline__ int cta_exclusive_scan(int x, int *sums, int &total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int y = x;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        uint4 u = *reinterpret_cast<const uint4 *>(tile + sw128_off(row, col0 + 8 * q));
-        v[8 * q + 0] = bf16_lo(u.x); v[8 * q + 1] = bf16_hi(u.x);
-        v[8 * q + 2] = bf16_lo(u.y); v[8 * q + 3] = bf16_hi(u.y);
-        v[8 * q + 4] = bf16_lo(u.z); v[8 * q + 5] = bf16_hi(u.z);
-        v[8 * q + 6] = bf16_lo(u.w); v[8 * q + 7] = bf16_hi(u.w);
+    for (int d = 1; d < 32; d <<= 1) {
+        const int z = __shfl_up_sync(0xffffffffu, y, d);
+        if (lane >= d) y += z;
     }
+    if (lane == 31) sums[warp] = y;
+    __syncthreads();
+    int before = 0;
+    total = 0;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) {
+        const int t = sums[w];
+        before += (w < warp) ? t : 0;
+        total += t;
+    }
+    __syncthreads();  // sums may be reused
+    return before + y - x;
+}
+
+__device__ __noinline__ int seq_of_rank(const int *cu, int n, int rank, int *work) {
+    if (n == 1) return 0;
+    int *hist = work, *sums = work + 256, *found = work + 264;
+    const int tid = threadIdx.x;
+    hist[tid] = 0;
+    __syncthreads();
+    for (int q = tid; q < n; q += kThreads) atomicAdd(&hist[chunk_key(cu, q)], 1);
+    __syncthreads();
+    int total;
+    const int cnt = hist[tid];
+    const int start = cta_exclusive_scan(cnt, sums, total);
+    if (start <= rank && rank < start + cnt) { found[0] = tid; found[1] = rank - start; }
+    __syncthreads();
+    const int bin = found[0], want = found[1];
+    const int per = (n + kThreads - 1) / kThreads;
+    const int q0 = min(n, tid * per), q1 = min(n, q0 + per);
+    int mine = 0;
+    for (int q = q0; q < q1; ++q) mine += chunk_key(cu, q) == bin;
+    const int before = cta_exclusive_scan(mine, sums, total);
+    if (before <= want && want < before + mine) {
+        int k = before;
+        for (int q = q0; q < q1; ++q)
+            if (chunk_key(cu, q) == bin) {
+                if (k == want) found[2] = q;
+                ++k;
+            }
+    }
+    __syncthreads();
+    const int seq = found[2];
+    __syncthreads();  // the work area is reused by the caller
+    return seq;
 }
 
 // Every thread waits on the MMA barrier itself.  A thread that gives up sets
@@ -197,10 +239,14 @@ __device__ __forceinline__ void mma_wait(uint32_t bar, uint32_t parity, volatile
 __global__ void __launch_bounds__(kThreads, 2)
     prefill_chunk_kernel(const PrefillArgs p, const __grid_constant__ InputMaps maps) {
     extern __shared__ uint8_t smem_raw[];
-    const int seq = blockIdx.x;
-    const int h = blockIdx.y;
     const int H = p.lv.n_heads;
+    const int h = blockIdx.x;
+    const int rank = static_cast<int>(blockIdx.z * kGridY + blockIdx.y);
+    if (rank >= p.n_seqs) return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int seq = p.n_seqs <= kMaxRankedSeqs
+                        ? seq_of_rank(p.cu_seqlens, p.n_seqs, rank, reinterpret_cast<int *>(smem_raw))
+                        : rank;
 
     const int slot = __ldg(p.slot_ids + seq);
     const int t0 = __ldg(p.cu_seqlens + seq);
@@ -224,6 +270,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     volatile int *flag = reinterpret_cast<volatile int *>(small + SOFF_FLAG);
     float *tot = reinterpret_cast<float *>(small + SOFF_TOT);
     float *gam = reinterpret_cast<float *>(small + SOFF_GAM);
+    auto blk = [base](int b) { return reinterpret_cast<float *>(base + OFF_R1 + b * kSlotBytes); };
 
     if (warp == 0) tmem_alloc(smem_addr(holder), kTmemCols);
     const uint32_t bar_tma = bar_mma + 8;
@@ -322,8 +369,11 @@ __global__ void __launch_bounds__(kThreads, 2)
             if (!(fabsf(G0 - Gm0) <= kMaxLog2Range && fabsf(G1 - Gm1) <= kMaxLog2Range))
                 range_bad = true;  // G[tb-1] (G[-1] = 0 for the first warp)
             const float EL0 = ex2_approx(G630 - Gm0), EL1 = ex2_approx(G631 - Gm1);
+            // 2^Gm is a normal float whenever the range check passes (|Gm| <= 120), so
+            // the decays from the chunk start are 2^(G - Gm) * 2^Gm.
+            const float eGm0 = ex2_approx(Gm0), eGm1 = ex2_approx(Gm1);
             float ep0 = ex2_approx(G0 - Gm0), ep1 = ex2_approx(G1 - Gm1);  // e_prev
-            float dp0 = ex2_approx(G0), dp1 = ex2_approx(G1);              // d_prev
+            float dp0 = ep0 * eGm0, dp1 = ep1 * eGm1;                      // d_prev
             // swizzled byte offset of (row tb + i, column ch)
             const uint32_t xl = static_cast<uint32_t>(lane) >> 2;
             const uint32_t rowbase = 1024u * warp + 4u * (lane & 3);
@@ -339,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     range_bad = true;
                 const float ec0 = ex2_approx(G0 - Gm0), ec1 = ex2_approx(G1 - Gm1);
                 const float iv0 = ex2_approx(Gm0 - G0), iv1 = ex2_approx(Gm1 - G1);
-                const float dc0 = ex2_approx(G0), dc1 = ex2_approx(G1);
+                const float dc0 = ec0 * eGm0, dc1 = ec1 * eGm1;
                 const float dl0 = EL0 * iv0, dl1 = EL1 * iv1;
                 const float ax = bf16_lo(ga[ii]), ay = bf16_hi(ga[ii]);
                 const float bx = bf16_lo(gb[ii]), by = bf16_hi(gb[ii]);
@@ -393,27 +443,62 @@ __global__ void __launch_bounds__(kThreads, 2)
         tc_fence_after();
         {
             float v[16];
-            if (row < 64) {  // Mab row s: diagonal block (fp32) | off-diagonal U (bf16)
-                const int s = row, ps = s >> 4;
-                float *md = reinterpret_cast<float *>(base + OFF_MD);
+            if (row < 64) {  // Mab row s -> fp32 block slots (strictly upper part only)
+                const int s = row, ps = s >> 4, r = s & 15;
 #pragma unroll 1
                 for (int g = 0; g < 2; ++g) {
                     const int c00 = cpart + 16 * g;
+                    const int pc = c00 >> 4;
                     tmem_ld16(tmem + lane_base + c00, v);
                     tmem_ld_wait();
-                    const int pc = c00 >> 4;
-                    if (pc == ps) {
+                    if (pc >= ps) {
 #pragma unroll
-                        for (int q = 0; q < 16; ++q) md[s * 16 + q] = (c00 + q > s) ? v[q] : 0.f;
+                        for (int q = 0; q < 16; ++q) v[q] = (c00 + q > s) ? v[q] : 0.f;
+                        float *dst = blk(pc == ps ? ps : kSlotM + up_idx(ps, pc)) + r * kSlotRow;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            reinterpret_cast<float4 *>(dst)[q] =
+                                make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
                     }
+                }
+                bar_sync_named(1, 128);  // warps 0, 1, 4, 5: Mab is in shared memory
+                if (warp < 2) {
+                    // T_pp = (I - M_pp)^-1 for the 16x16 diagonal block p, column c, by
+                    // back substitution in fp32: x_r = sum_{u > r} M_pp[r][u] x_u (r < c).
+                    const int pb = tid >> 4, c = tid & 15;
+                    float *md = blk(pb);
+                    float x[16];
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) v[q] = (pc > ps) ? v[q] : 0.f;
-                    store_row16(base + OFF_UT, s, c00, v);
-                    if (pc != ps) {  // Tdiag is zero off its diagonal blocks
+                    for (int rr = 0; rr < 16; ++rr) x[rr] = (rr == c) ? 1.f : 0.f;
 #pragma unroll
-                        for (int q = 0; q < 16; ++q) v[q] = 0.f;
-                        store_row16(base + OFF_TD, s, c00, v);
+                    for (int rr = 14; rr >= 0; --rr) {
+                        float mrow[16];
+#pragma unroll
+                        for (int q = (rr + 1) >> 2; q < 4; ++q) {
+                            const float4 y = reinterpret_cast<const float4 *>(md + rr * kSlotRow)[q];
+                            mrow[4 * q] = y.x; mrow[4 * q + 1] = y.y;
+                            mrow[4 * q + 2] = y.z; mrow[4 * q + 3] = y.w;
+                        }
+                        float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+                        for (int u = rr + 1; u < 16; ++u) {
+                            if (u & 1) acc1 = fmaf(mrow[u], x[u], acc1);
+                            else acc0 = fmaf(mrow[u], x[u], acc0);
+                        }
+                        if (rr < c) x[rr] = acc0 + acc1;
                     }
+                    __syncwarp();  // this warp's two blocks are read; overwrite M_pp with T_pp
+#pragma unroll
+                    for (int rr = 0; rr < 16; ++rr) {
+                        md[rr * kSlotRow + c] = x[rr];
+                        *reinterpret_cast<__nv_bfloat16 *>(base + OFF_WT + sw128_off(16 * pb + rr, 16 * pb + c)) =
+                            __float2bfloat16_rn(x[rr]);
+                    }
+                } else {  // warps 4, 5: T is zero below its diagonal blocks
+                    const int s2 = tid - 128;
+                    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                    for (int q = 0; q < 2 * (s2 >> 4); ++q)
+                        *reinterpret_cast<uint4 *>(base + OFF_WT + sw128_off(s2, 8 * q)) = z;
                 }
             } else {  // Mak row s' (keep s > s'), and Qb^T row t' (keep s <= t')
                 const int s = row - 64;
@@ -438,83 +523,115 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (*flag) break;
 
         // ------------------------------------------------ T = (I - Mab)^-1
-        if (tid < 64) {  // Tdiag: column c of the 16x16 block p, by substitution in fp32
-            const int pb = tid >> 4, c = tid & 15;
-            const float *md = reinterpret_cast<const float *>(base + OFF_MD) + (16 * pb) * 16;
-            float x[16];
+        // Off-diagonal 16x16 blocks by diagonals of the block triangle, fp32 on the
+        // CUDA cores: with N_ij = T_ii M_ij (i < j),  T_ij = sum_{i<k<=j} N_ik T_kj.
+        if (tid < 192) {  // N_ij: row r, 8 columns
+            const int r = tid & 15, k = tid >> 4;  // k: 0-5 row block 0, 6-9 block 1, 10-11 block 2
+            const int i = k < 6 ? 0 : (k < 10 ? 1 : 2);
+            const int kk = k - (i == 0 ? 0 : (i == 1 ? 6 : 10));
+            const int j = i + 1 + (kk >> 1), c0 = 8 * (kk & 1);
+            const float *trow = blk(i) + r * kSlotRow;
+            const float *m = blk(kSlotM + up_idx(i, j)) + c0;
+            float t[16], acc[8];
 #pragma unroll
-            for (int r = 0; r < 16; ++r) x[r] = (r == c) ? 1.f : 0.f;
-#pragma unroll
-            for (int r = 14; r >= 0; --r) {
-                float mrow[16];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float4 y = *reinterpret_cast<const float4 *>(md + r * 16 + 4 * q);
-                    mrow[4 * q] = y.x; mrow[4 * q + 1] = y.y; mrow[4 * q + 2] = y.z; mrow[4 * q + 3] = y.w;
-                }
-                float acc = 0.f;
-#pragma unroll
-                for (int u = r + 1; u < 16; ++u) acc = fmaf(mrow[u], x[u], acc);
-                if (r < c) x[r] = acc;
+            for (int q = 0; q < 4; ++q) {
+                const float4 y = reinterpret_cast<const float4 *>(trow)[q];
+                t[4 * q] = y.x; t[4 * q + 1] = y.y; t[4 * q + 2] = y.z; t[4 * q + 3] = y.w;
             }
 #pragma unroll
-            for (int r = 0; r < 16; ++r)
-                *reinterpret_cast<__nv_bfloat16 *>(base + OFF_TD + sw128_off(16 * pb + r, 16 * pb + c)) =
-                    __float2bfloat16_rn(x[r]);
+            for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const float4 m0 = reinterpret_cast<const float4 *>(m + u * kSlotRow)[0];
+                const float4 m1 = reinterpret_cast<const float4 *>(m + u * kSlotRow)[1];
+                acc[0] = fmaf(t[u], m0.x, acc[0]); acc[1] = fmaf(t[u], m0.y, acc[1]);
+                acc[2] = fmaf(t[u], m0.z, acc[2]); acc[3] = fmaf(t[u], m0.w, acc[3]);
+                acc[4] = fmaf(t[u], m1.x, acc[4]); acc[5] = fmaf(t[u], m1.y, acc[5]);
+                acc[6] = fmaf(t[u], m1.z, acc[6]); acc[7] = fmaf(t[u], m1.w, acc[7]);
+            }
+            float *dst = blk(kSlotN + up_idx(i, j)) + r * kSlotRow + c0;
+            reinterpret_cast<float4 *>(dst)[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            reinterpret_cast<float4 *>(dst)[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        }
+        __syncthreads();
+        if (tid < 192) {  // first diagonal: T_i,i+1 = N_i,i+1 T_i+1,i+1; row r, 4 columns
+            const int r = tid & 15, k = tid >> 4, i = k >> 2, c0 = 4 * (k & 3);
+            const float *nrow = blk(kSlotN + up_idx(i, i + 1)) + r * kSlotRow;
+            const float *tb = blk(i + 1) + c0;
+            float nv[16], acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 y = reinterpret_cast<const float4 *>(nrow)[q];
+                nv[4 * q] = y.x; nv[4 * q + 1] = y.y; nv[4 * q + 2] = y.z; nv[4 * q + 3] = y.w;
+            }
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const float4 y = *reinterpret_cast<const float4 *>(tb + u * kSlotRow);
+                acc[0] = fmaf(nv[u], y.x, acc[0]); acc[1] = fmaf(nv[u], y.y, acc[1]);
+                acc[2] = fmaf(nv[u], y.z, acc[2]); acc[3] = fmaf(nv[u], y.w, acc[3]);
+            }
+            if (i > 0)  // T_12, T_23 are read again by the next diagonals
+                *reinterpret_cast<float4 *>(blk(kSlotT + i - 1) + r * kSlotRow + c0) =
+                    make_float4(acc[0], acc[1], acc[2], acc[3]);
+            *reinterpret_cast<uint2 *>(base + OFF_WT + sw128_off(16 * i + r, 16 * (i + 1) + c0)) =
+                make_uint2(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]));
+        }
+        __syncthreads();
+        {  // second diagonal: T_02 = N_01 T_12 + N_02 T_22,  T_13 = N_12 T_23 + N_13 T_33
+            const int r = tid & 15, k = tid >> 4, b = k >> 3, c0 = 2 * (k & 7);
+            const float *na = blk(kSlotN + (b == 0 ? up_idx(0, 1) : up_idx(1, 2))) + r * kSlotRow;
+            const float *nb = blk(kSlotN + (b == 0 ? up_idx(0, 2) : up_idx(1, 3))) + r * kSlotRow;
+            const float *ta = blk(kSlotT + (b == 0 ? 0 : 1)) + c0;
+            const float *tb = blk(b == 0 ? 2 : 3) + c0;
+            float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 ya = reinterpret_cast<const float4 *>(na)[q];
+                const float4 yb = reinterpret_cast<const float4 *>(nb)[q];
+                const float av[4] = {ya.x, ya.y, ya.z, ya.w}, bv[4] = {yb.x, yb.y, yb.z, yb.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int u = 4 * q + e;
+                    const float2 xa = *reinterpret_cast<const float2 *>(ta + u * kSlotRow);
+                    const float2 xb = *reinterpret_cast<const float2 *>(tb + u * kSlotRow);
+                    acc0 = fmaf(av[e], xa.x, acc0); acc1 = fmaf(av[e], xa.y, acc1);
+                    acc2 = fmaf(bv[e], xb.x, acc2); acc3 = fmaf(bv[e], xb.y, acc3);
+                }
+            }
+            acc0 += acc2; acc1 += acc3;
+            if (b == 1)
+                *reinterpret_cast<float2 *>(blk(kSlotT + 2) + r * kSlotRow + c0) = make_float2(acc0, acc1);
+            *reinterpret_cast<uint32_t *>(base + OFF_WT + sw128_off(16 * b + r, 16 * (b + 2) + c0)) =
+                pack_bf16(acc0, acc1);
+        }
+        __syncthreads();
+        {  // third diagonal: T_03 = N_01 T_13 + N_02 T_23 + N_03 T_33; row r, column c
+            const int r = tid & 15, c = tid >> 4;
+            const float *n1 = blk(kSlotN + up_idx(0, 1)) + r * kSlotRow;
+            const float *n2 = blk(kSlotN + up_idx(0, 2)) + r * kSlotRow;
+            const float *n3 = blk(kSlotN + up_idx(0, 3)) + r * kSlotRow;
+            const float *t1 = blk(kSlotT + 2) + c, *t2 = blk(kSlotT + 1) + c, *t3 = blk(3) + c;
+            float a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 y1 = reinterpret_cast<const float4 *>(n1)[q];
+                const float4 y2 = reinterpret_cast<const float4 *>(n2)[q];
+                const float4 y3 = reinterpret_cast<const float4 *>(n3)[q];
+                const float v1[4] = {y1.x, y1.y, y1.z, y1.w}, v2[4] = {y2.x, y2.y, y2.z, y2.w},
+                            v3[4] = {y3.x, y3.y, y3.z, y3.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int u = 4 * q + e;
+                    a1 = fmaf(v1[e], t1[u * kSlotRow], a1);
+                    a2 = fmaf(v2[e], t2[u * kSlotRow], a2);
+                    a3 = fmaf(v3[e], t3[u * kSlotRow], a3);
+                }
+            }
+            *reinterpret_cast<__nv_bfloat16 *>(base + OFF_WT + sw128_off(r, 48 + c)) =
+                __float2bfloat16_rn(a1 + a2 + a3);
         }
         fence_proxy_async_smem();
         __syncthreads();
-        // N = Tdiag U;  [N Tdiag | N^2] in one N=128 UMMA (B = [TD | NT] MN-major);
-        // W1 = Tdiag + N Tdiag;  T = W1 + N^2 W1 = (I + N + N^2 + N^3) Tdiag.
-#pragma unroll 1
-        for (int k = 0; k < 3; ++k) {
-            if (tid == 0) {
-                tc_fence_after();
-                if (k == 0)
-                    umma_128xNx64_bmn(tmem + 0, smem_addr(base + OFF_TD), smem_addr(base + OFF_UT), 64, false);
-                else if (k == 1)
-                    umma_128xNx64_bmn(tmem + 0, smem_addr(base + OFF_NT), smem_addr(base + OFF_TD), 128,
-                                      false, OFF_NT - OFF_TD);
-                else
-                    umma_128xNx64_bmn(tmem + 0, smem_addr(base + OFF_N2), smem_addr(base + OFF_WT), 64, false);
-                umma_commit(bar_mma);
-            }
-            mma_wait(bar_mma, ph_mma, flag);
-            ph_mma ^= 1;
-            tc_fence_after();
-            if (row < 64) {
-                const int s = row, ps = s >> 4;
-                float v[16], add[16];
-#pragma unroll 1
-                for (int g = 0; g < 2; ++g) {
-                    const int c00 = cpart + 16 * g;
-                    tmem_ld16(tmem + lane_base + c00, v);
-                    if (k == 1) tmem_ld16(tmem + lane_base + 64 + c00, add);
-                    tmem_ld_wait();
-                    if (k == 0) {  // N
-                        store_row16(base + OFF_NT, s, c00, v);
-                    } else if (k == 1) {  // W1 = Tdiag + N Tdiag ; N^2
-                        store_row16(base + OFF_N2, s, c00, add);
-                        if ((c00 >> 4) == ps) {
-                            load_row16(base + OFF_TD, s, c00, add);
-#pragma unroll
-                            for (int q = 0; q < 16; ++q) v[q] += add[q];
-                        }
-                        store_row16(base + OFF_WT, s, c00, v);
-                    } else {  // T = W1 + N^2 W1
-                        load_row16(base + OFF_WT, s, c00, add);
-#pragma unroll
-                        for (int q = 0; q < 16; ++q) v[q] += add[q];
-                        store_row16(base + OFF_WT, s, c00, v);
-                    }
-                }
-            }
-            tc_fence_before();
-            fence_proxy_async_smem();
-            __syncthreads();
-            if (*flag) break;
-        }
-        if (*flag) break;
 
         // ------------------------------------------------------------- G2
         if (tid == 0) {
@@ -707,7 +824,7 @@ cudaError_t launch_prefill_chunked(const PrefillArgs &a, cudaStream_t s, int *la
     if (a.n_seqs <= 0) return cudaSuccess;
     if (a.total_tokens == 0)  // only empty sequences: nothing to load, only metadata to check
         return launch_prefill_sequential(a, s, launches);
-    if (a.lv.n_heads > 65535) return cudaErrorInvalidValue;
+    if (a.lv.n_heads > 0x7fffffff / 2) return cudaErrorInvalidValue;
     InputMaps maps;
     const void *src[6] = {a.in.r, a.in.w, a.in.k, a.in.v, a.in.a, a.in.b};
     for (int x = 0; x < 6; ++x)
@@ -716,7 +833,8 @@ cudaError_t launch_prefill_chunked(const PrefillArgs &a, cudaStream_t s, int *la
     cudaError_t e = cudaFuncSetAttribute(prefill_chunk_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    dim3 grid(static_cast<unsigned>(a.n_seqs), static_cast<unsigned>(a.lv.n_heads));
+    const unsigned ny = static_cast<unsigned>(a.n_seqs) < kGridY ? static_cast<unsigned>(a.n_seqs) : kGridY;
+    const dim3 grid(static_cast<unsigned>(a.lv.n_heads), ny, (static_cast<unsigned>(a.n_seqs) + kGridY - 1) / kGridY);
     prefill_chunk_kernel<<<grid, kThreads, kSmemBytes, s>>>(a, maps);
     ++*launches;
     return cudaGetLastError();
