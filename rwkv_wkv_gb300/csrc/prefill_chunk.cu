@@ -34,8 +34,8 @@
 //   T   (I - Mab)^-1 in fp32 on the CUDA cores, by 16x16 blocks: the four
 //       diagonal blocks T_ii = (I - M_ii)^-1 by back substitution (two warps,
 //       while the other warps read the rest of G1 back), then N_ij = T_ii M_ij
-//       and the off-diagonal blocks one block diagonal at a time,
-//       T_ij = sum_{i<k<=j} N_ik T_kj; T goes to shared memory in bf16
+//       and the off-diagonal blocks from products of pairs of those blocks
+//       (three barrier steps); T goes to shared memory in bf16
 //   G2  [Bhat^T; Qb^T] x T^T -> Z^T                  (M=128, N=64)
 //   G34 Z^T x [A0^T; Mak]^T -> Phi'^T, R''^T, Y'^T   (M=128, N=128)
 //   G5  [Y_Q^T; Y_B^T] x V -> O0^T, Psi^T; then += [R'^T; Phi^T] x S0^T with
@@ -79,12 +79,14 @@ constexpr uint32_t OFF_R1 = 0;                      // tile offsets from the ali
 constexpr uint32_t OFF_G1A = OFF_R1;
 constexpr uint32_t OFF_G1B = OFF_R1 + kTile128;
 // fp32 16x16 blocks of the inverse, 80-byte rows (conflict-free float4 rows):
-// slots 0-3 M_ii then T_ii, 4-9 M_ij (i < j), 10-15 N_ij = T_ii M_ij, 16-18 T_12, T_23, T_13
+// slots 0-3 M_ii then T_ii, 4-9 M_ij (i < j; later T_23, R_02, R_03, R_13),
+// 10-15 N_ij = T_ii M_ij
 constexpr int kSlotRow = 20;                          // floats per block row
 constexpr uint32_t kSlotBytes = 16 * kSlotRow * 4;
-constexpr int kSlotM = 4, kSlotN = 10, kSlotT = 16;
+constexpr int kSlotM = 4, kSlotN = 10;
+constexpr int kSlotT23 = 0, kSlotR02 = 1, kSlotR03 = 2, kSlotR13 = 3;  // from kSlotM, after N
 constexpr uint32_t OFF_WT = OFF_R1 + 3 * kTile64;   // T in bf16 (rows s, K = t)
-static_assert(19 * kSlotBytes <= OFF_WT - OFF_R1, "inverse blocks overlap T");
+static_assert(16 * kSlotBytes <= OFF_WT - OFF_R1, "inverse blocks overlap T");
 constexpr uint32_t OFF_G2B = OFF_WT;
 constexpr uint32_t OFF_OPZ = OFF_R1;
 constexpr uint32_t OFF_OPY = OFF_R1;
@@ -378,15 +380,15 @@ __global__ void __launch_bounds__(kThreads, 2)
             const uint32_t xl = static_cast<uint32_t>(lane) >> 2;
             const uint32_t rowbase = 1024u * warp + 4u * (lane & 3);
             uint8_t *g1a = base + OFF_G1A, *g1b = base + OFF_G1B, *r0t = base + OFF_R0;
+            float dmax = 0.f;  // max |G - Gm| over this warp's tokens
             uint32_t cb[4][2][4];  // channel-major operands [Bhat, Khat, A0, V][channel][pair]
             float prv[4][2];
 #pragma unroll
             for (int ii = 0; ii < 8; ++ii) {
                 G0 += lg2_approx(bf16_lo(gw[ii]));
                 G1 += lg2_approx(bf16_hi(gw[ii]));
-                if (tb + ii < Lc &&
-                    !(fabsf(G0 - Gm0) <= kMaxLog2Range && fabsf(G1 - Gm1) <= kMaxLog2Range))
-                    range_bad = true;
+                // padding tokens have w = 1 and leave G unchanged
+                dmax = fmaxf(dmax, fmaxf(fabsf(G0 - Gm0), fabsf(G1 - Gm1)));
                 const float ec0 = ex2_approx(G0 - Gm0), ec1 = ex2_approx(G1 - Gm1);
                 const float iv0 = ex2_approx(Gm0 - G0), iv1 = ex2_approx(Gm1 - G1);
                 const float dc0 = ec0 * eGm0, dc1 = ec1 * eGm1;
@@ -416,6 +418,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 ep0 = ec0; ep1 = ec1;
                 dp0 = dc0; dp1 = dc1;
             }
+            if (!(dmax <= kMaxLog2Range) || G0 != G0 || G1 != G1) range_bad = true;  // NaN too
             uint8_t *dst[4] = {base + OFF_G2A, base + OFF_KHT, base + OFF_G34B, base + OFF_V};
 #pragma unroll
             for (int o = 0; o < 4; ++o)
@@ -442,57 +445,88 @@ __global__ void __launch_bounds__(kThreads, 2)
         ph_mma ^= 1;
         tc_fence_after();
         {
-            float v[16];
+            float v[32];
             if (row < 64) {  // Mab row s -> fp32 block slots (strictly upper part only)
                 const int s = row, ps = s >> 4, r = s & 15;
-#pragma unroll 1
+                tmem_ld32(tmem + lane_base + cpart, v);
+                tmem_ld_wait();
+#pragma unroll
                 for (int g = 0; g < 2; ++g) {
                     const int c00 = cpart + 16 * g;
                     const int pc = c00 >> 4;
-                    tmem_ld16(tmem + lane_base + c00, v);
-                    tmem_ld_wait();
                     if (pc >= ps) {
-#pragma unroll
-                        for (int q = 0; q < 16; ++q) v[q] = (c00 + q > s) ? v[q] : 0.f;
                         float *dst = blk(pc == ps ? ps : kSlotM + up_idx(ps, pc)) + r * kSlotRow;
 #pragma unroll
-                        for (int q = 0; q < 4; ++q)
+                        for (int q = 0; q < 4; ++q) {
+                            const int c = c00 + 4 * q;
+                            const float *x = v + 16 * g + 4 * q;
                             reinterpret_cast<float4 *>(dst)[q] =
-                                make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                                make_float4(c > s ? x[0] : 0.f, c + 1 > s ? x[1] : 0.f,
+                                            c + 2 > s ? x[2] : 0.f, c + 3 > s ? x[3] : 0.f);
+                        }
                     }
                 }
                 bar_sync_named(1, 128);  // warps 0, 1, 4, 5: Mab is in shared memory
                 if (warp < 2) {
-                    // T_pp = (I - M_pp)^-1 for the 16x16 diagonal block p, column c, by
-                    // back substitution in fp32: x_r = sum_{u > r} M_pp[r][u] x_u (r < c).
-                    const int pb = tid >> 4, c = tid & 15;
+                    // T_pp = (I - M_pp)^-1 for the 16x16 diagonal block p, column c, in fp32.
+                    // With M_pp = [A B; 0 C] (8x8 blocks), T_pp = [A' A'BC'; 0 C'],
+                    // A' = (I - A)^-1 and C' = (I - C)^-1 by back substitution
+                    // (x_r = sum_{u > r} M[r][u] x_u above the diagonal), then A'(B C').
+                    const int pb = tid >> 4, c = tid & 15, cl = c & 7;
+                    const bool right = c >= 8;  // column of C' (rows 8-15) and of A'BC'
+                    const int o = right ? 8 : 0;
                     float *md = blk(pb);
-                    float x[16];
+                    float x[8];
 #pragma unroll
-                    for (int rr = 0; rr < 16; ++rr) x[rr] = (rr == c) ? 1.f : 0.f;
+                    for (int rr = 0; rr < 8; ++rr) x[rr] = (rr == cl) ? 1.f : 0.f;
 #pragma unroll
-                    for (int rr = 14; rr >= 0; --rr) {
-                        float mrow[16];
+                    for (int rr = 6; rr >= 0; --rr) {
+                        const float4 y0 = reinterpret_cast<const float4 *>(md + (o + rr) * kSlotRow + o)[0];
+                        const float4 y1 = reinterpret_cast<const float4 *>(md + (o + rr) * kSlotRow + o)[1];
+                        const float mrow[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+                        float acc = 0.f;
 #pragma unroll
-                        for (int q = (rr + 1) >> 2; q < 4; ++q) {
-                            const float4 y = reinterpret_cast<const float4 *>(md + rr * kSlotRow)[q];
-                            mrow[4 * q] = y.x; mrow[4 * q + 1] = y.y;
-                            mrow[4 * q + 2] = y.z; mrow[4 * q + 3] = y.w;
-                        }
-                        float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
-                        for (int u = rr + 1; u < 16; ++u) {
-                            if (u & 1) acc1 = fmaf(mrow[u], x[u], acc1);
-                            else acc0 = fmaf(mrow[u], x[u], acc0);
-                        }
-                        if (rr < c) x[rr] = acc0 + acc1;
+                        for (int u = rr + 1; u < 8; ++u) acc = fmaf(mrow[u], x[u], acc);
+                        if (rr < cl) x[rr] = acc;
                     }
-                    __syncwarp();  // this warp's two blocks are read; overwrite M_pp with T_pp
+                    float y[8];  // right: y = B x
 #pragma unroll
-                    for (int rr = 0; rr < 16; ++rr) {
-                        md[rr * kSlotRow + c] = x[rr];
+                    for (int rr = 0; rr < 8; ++rr) y[rr] = 0.f;
+                    if (right) {
+#pragma unroll
+                        for (int rr = 0; rr < 8; ++rr) {
+                            const float4 b0 = reinterpret_cast<const float4 *>(md + rr * kSlotRow + 8)[0];
+                            const float4 b1 = reinterpret_cast<const float4 *>(md + rr * kSlotRow + 8)[1];
+                            y[rr] = b0.x * x[0] + b0.y * x[1] + b0.z * x[2] + b0.w * x[3] +
+                                    b1.x * x[4] + b1.y * x[5] + b1.z * x[6] + b1.w * x[7];
+                        }
+                    }
+                    __syncwarp();  // A, B, C of this warp's two blocks are read
+                    if (!right) {
+#pragma unroll
+                        for (int rr = 0; rr < 8; ++rr) md[rr * kSlotRow + c] = x[rr];  // A'
+                    }
+                    __syncwarp();
+                    float z[8];  // right: A' y (A' is upper triangular)
+                    if (right) {
+#pragma unroll
+                        for (int rr = 0; rr < 8; ++rr) {
+                            const float4 a0 = reinterpret_cast<const float4 *>(md + rr * kSlotRow)[0];
+                            const float4 a1 = reinterpret_cast<const float4 *>(md + rr * kSlotRow)[1];
+                            z[rr] = a0.x * y[0] + a0.y * y[1] + a0.z * y[2] + a0.w * y[3] +
+                                    a1.x * y[4] + a1.y * y[5] + a1.z * y[6] + a1.w * y[7];
+                        }
+                    }
+                    __syncwarp();  // A' is read
+#pragma unroll
+                    for (int rr = 0; rr < 8; ++rr) {
+                        const float top = right ? z[rr] : x[rr], bot = right ? x[rr] : 0.f;
+                        md[rr * kSlotRow + c] = top;
+                        md[(8 + rr) * kSlotRow + c] = bot;
                         *reinterpret_cast<__nv_bfloat16 *>(base + OFF_WT + sw128_off(16 * pb + rr, 16 * pb + c)) =
-                            __float2bfloat16_rn(x[rr]);
+                            __float2bfloat16_rn(top);
+                        *reinterpret_cast<__nv_bfloat16 *>(base + OFF_WT + sw128_off(16 * pb + 8 + rr, 16 * pb + c)) =
+                            __float2bfloat16_rn(bot);
                     }
                 } else {  // warps 4, 5: T is zero below its diagonal blocks
                     const int s2 = tid - 128;
@@ -502,20 +536,19 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
             } else {  // Mak row s' (keep s > s'), and Qb^T row t' (keep s <= t')
                 const int s = row - 64;
-#pragma unroll 1
-                for (int g = 0; g < 2; ++g) {
-                    const int c00 = cpart + 16 * g;
-                    tmem_ld16(tmem + lane_base + c00, v);
-                    tmem_ld_wait();
+                float qb[32];
+                tmem_ld32(tmem + lane_base + cpart, v);
+                tmem_ld32(tmem + lane_base + 128 + cpart, qb);
+                tmem_ld_wait();
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) v[q] = (c00 + q > s) ? v[q] : 0.f;
-                    store_row16(base + OFF_G34B, 64 + s, c00, v);
-                    tmem_ld16(tmem + lane_base + 128 + c00, v);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int q = 0; q < 16; ++q) v[q] = (c00 + q <= s) ? v[q] : 0.f;
-                    store_row16(base + OFF_G2A, 64 + s, c00, v);
+                for (int q = 0; q < 32; ++q) {
+                    v[q] = (cpart + q > s) ? v[q] : 0.f;
+                    qb[q] = (cpart + q <= s) ? qb[q] : 0.f;
                 }
+                store_row16(base + OFF_G34B, 64 + s, cpart, v);
+                store_row16(base + OFF_G34B, 64 + s, cpart + 16, v + 16);
+                store_row16(base + OFF_G2A, 64 + s, cpart, qb);
+                store_row16(base + OFF_G2A, 64 + s, cpart + 16, qb + 16);
             }
         }
         tc_fence_before();
@@ -523,8 +556,12 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (*flag) break;
 
         // ------------------------------------------------ T = (I - Mab)^-1
-        // Off-diagonal 16x16 blocks by diagonals of the block triangle, fp32 on the
-        // CUDA cores: with N_ij = T_ii M_ij (i < j),  T_ij = sum_{i<k<=j} N_ik T_kj.
+        // Off-diagonal 16x16 blocks in fp32 on the CUDA cores.  With N_ij = T_ii M_ij
+        // (i < j), T_ij = sum_{i<k<=j} N_ik T_kj; grouping the products in pairs,
+        //   T_i,i+1 = N_i,i+1 T_i+1,i+1,  T_02 = R_02 T_22,  T_13 = R_13 T_33,
+        //   T_03 = R_02 T_23 + R_03 T_33,
+        // R_02 = N_02 + N_01 N_12, R_03 = N_03 + N_01 N_13, R_13 = N_13 + N_12 N_23:
+        // three steps after the diagonal blocks.
         if (tid < 192) {  // N_ij: row r, 8 columns
             const int r = tid & 15, k = tid >> 4;  // k: 0-5 row block 0, 6-9 block 1, 10-11 block 2
             const int i = k < 6 ? 0 : (k < 10 ? 1 : 2);
@@ -554,81 +591,94 @@ __global__ void __launch_bounds__(kThreads, 2)
             reinterpret_cast<float4 *>(dst)[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
         }
         __syncthreads();
-        if (tid < 192) {  // first diagonal: T_i,i+1 = N_i,i+1 T_i+1,i+1; row r, 4 columns
-            const int r = tid & 15, k = tid >> 4, i = k >> 2, c0 = 4 * (k & 3);
-            const float *nrow = blk(kSlotN + up_idx(i, i + 1)) + r * kSlotRow;
-            const float *tb = blk(i + 1) + c0;
-            float nv[16], acc[4] = {0.f, 0.f, 0.f, 0.f};
+        if (tid < 192) {
+            // Pair products (one per warp), row r, 8 columns:
+            //   T_01 = N_01 T_11, T_12 = N_12 T_22, T_23 = N_23 T_33,
+            //   R_02 = N_02 + N_01 N_12, R_03 = N_03 + N_01 N_13, R_13 = N_13 + N_12 N_23
+            const int pw = tid >> 5, r = tid & 15, c0 = 8 * ((tid >> 4) & 1);
+            const int ia = pw == 0 ? kSlotN + up_idx(0, 1) : pw == 1 ? kSlotN + up_idx(1, 2)
+                         : pw == 2 ? kSlotN + up_idx(2, 3) : pw == 5 ? kSlotN + up_idx(1, 2)
+                                                                    : kSlotN + up_idx(0, 1);
+            const int ib = pw == 0 ? 1 : pw == 1 ? 2 : pw == 2 ? 3 : pw == 3 ? kSlotN + up_idx(1, 2)
+                         : pw == 4 ? kSlotN + up_idx(1, 3) : kSlotN + up_idx(2, 3);
+            const float *arow = blk(ia) + r * kSlotRow;
+            const float *bcol = blk(ib) + c0;
+            float av[16], acc[8];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const float4 y = reinterpret_cast<const float4 *>(nrow)[q];
-                nv[4 * q] = y.x; nv[4 * q + 1] = y.y; nv[4 * q + 2] = y.z; nv[4 * q + 3] = y.w;
+                const float4 y = reinterpret_cast<const float4 *>(arow)[q];
+                av[4 * q] = y.x; av[4 * q + 1] = y.y; av[4 * q + 2] = y.z; av[4 * q + 3] = y.w;
+            }
+            if (pw >= 3) {  // R_0j / R_13 start from N_02, N_03, N_13
+                const int ic = kSlotN + (pw == 3 ? up_idx(0, 2) : pw == 4 ? up_idx(0, 3) : up_idx(1, 3));
+                const float4 y0 = reinterpret_cast<const float4 *>(blk(ic) + r * kSlotRow + c0)[0];
+                const float4 y1 = reinterpret_cast<const float4 *>(blk(ic) + r * kSlotRow + c0)[1];
+                acc[0] = y0.x; acc[1] = y0.y; acc[2] = y0.z; acc[3] = y0.w;
+                acc[4] = y1.x; acc[5] = y1.y; acc[6] = y1.z; acc[7] = y1.w;
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[e] = 0.f;
             }
 #pragma unroll
             for (int u = 0; u < 16; ++u) {
-                const float4 y = *reinterpret_cast<const float4 *>(tb + u * kSlotRow);
-                acc[0] = fmaf(nv[u], y.x, acc[0]); acc[1] = fmaf(nv[u], y.y, acc[1]);
-                acc[2] = fmaf(nv[u], y.z, acc[2]); acc[3] = fmaf(nv[u], y.w, acc[3]);
+                const float4 m0 = reinterpret_cast<const float4 *>(bcol + u * kSlotRow)[0];
+                const float4 m1 = reinterpret_cast<const float4 *>(bcol + u * kSlotRow)[1];
+                acc[0] = fmaf(av[u], m0.x, acc[0]); acc[1] = fmaf(av[u], m0.y, acc[1]);
+                acc[2] = fmaf(av[u], m0.z, acc[2]); acc[3] = fmaf(av[u], m0.w, acc[3]);
+                acc[4] = fmaf(av[u], m1.x, acc[4]); acc[5] = fmaf(av[u], m1.y, acc[5]);
+                acc[6] = fmaf(av[u], m1.z, acc[6]); acc[7] = fmaf(av[u], m1.w, acc[7]);
             }
-            if (i > 0)  // T_12, T_23 are read again by the next diagonals
-                *reinterpret_cast<float4 *>(blk(kSlotT + i - 1) + r * kSlotRow + c0) =
-                    make_float4(acc[0], acc[1], acc[2], acc[3]);
-            *reinterpret_cast<uint2 *>(base + OFF_WT + sw128_off(16 * i + r, 16 * (i + 1) + c0)) =
+            if (pw >= 2) {  // kept in fp32 for the last step (over the dead M_ij blocks)
+                float *dst = blk(kSlotM + pw - 2) + r * kSlotRow + c0;
+                reinterpret_cast<float4 *>(dst)[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                reinterpret_cast<float4 *>(dst)[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+            }
+            if (pw < 3)  // T_i,i+1 -> bf16 T
+                *reinterpret_cast<uint4 *>(base + OFF_WT + sw128_off(16 * pw + r, 16 * (pw + 1) + c0)) =
+                    make_uint4(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]),
+                               pack_bf16(acc[4], acc[5]), pack_bf16(acc[6], acc[7]));
+        }
+        __syncthreads();
+        if (tid < 128) {  // T_02 = R_02 T_22, T_13 = R_13 T_33: row r, 4 columns
+            const int r = tid & 15, b = tid >> 6, c0 = 4 * ((tid >> 4) & 3);
+            const float *arow = blk(kSlotM + (b == 0 ? kSlotR02 : kSlotR13)) + r * kSlotRow;
+            const float *bcol = blk(2 + b) + c0;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 y = reinterpret_cast<const float4 *>(arow)[q];
+                const float yv[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float4 x = *reinterpret_cast<const float4 *>(bcol + (4 * q + e) * kSlotRow);
+                    acc[0] = fmaf(yv[e], x.x, acc[0]); acc[1] = fmaf(yv[e], x.y, acc[1]);
+                    acc[2] = fmaf(yv[e], x.z, acc[2]); acc[3] = fmaf(yv[e], x.w, acc[3]);
+                }
+            }
+            *reinterpret_cast<uint2 *>(base + OFF_WT + sw128_off(16 * b + r, 16 * (b + 2) + c0)) =
                 make_uint2(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]));
-        }
-        __syncthreads();
-        {  // second diagonal: T_02 = N_01 T_12 + N_02 T_22,  T_13 = N_12 T_23 + N_13 T_33
-            const int r = tid & 15, k = tid >> 4, b = k >> 3, c0 = 2 * (k & 7);
-            const float *na = blk(kSlotN + (b == 0 ? up_idx(0, 1) : up_idx(1, 2))) + r * kSlotRow;
-            const float *nb = blk(kSlotN + (b == 0 ? up_idx(0, 2) : up_idx(1, 3))) + r * kSlotRow;
-            const float *ta = blk(kSlotT + (b == 0 ? 0 : 1)) + c0;
-            const float *tb = blk(b == 0 ? 2 : 3) + c0;
-            float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+        } else {  // T_03 = R_02 T_23 + R_03 T_33: row r, 2 columns
+            const int r = tid & 15, c0 = 2 * ((tid - 128) >> 4);
+            const float *a1 = blk(kSlotM + kSlotR02) + r * kSlotRow;
+            const float *a2 = blk(kSlotM + kSlotR03) + r * kSlotRow;
+            const float *b1 = blk(kSlotM + kSlotT23) + c0;
+            const float *b2 = blk(3) + c0;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const float4 ya = reinterpret_cast<const float4 *>(na)[q];
-                const float4 yb = reinterpret_cast<const float4 *>(nb)[q];
-                const float av[4] = {ya.x, ya.y, ya.z, ya.w}, bv[4] = {yb.x, yb.y, yb.z, yb.w};
+                const float4 y1 = reinterpret_cast<const float4 *>(a1)[q];
+                const float4 y2 = reinterpret_cast<const float4 *>(a2)[q];
+                const float v1[4] = {y1.x, y1.y, y1.z, y1.w}, v2[4] = {y2.x, y2.y, y2.z, y2.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const int u = 4 * q + e;
-                    const float2 xa = *reinterpret_cast<const float2 *>(ta + u * kSlotRow);
-                    const float2 xb = *reinterpret_cast<const float2 *>(tb + u * kSlotRow);
-                    acc0 = fmaf(av[e], xa.x, acc0); acc1 = fmaf(av[e], xa.y, acc1);
-                    acc2 = fmaf(bv[e], xb.x, acc2); acc3 = fmaf(bv[e], xb.y, acc3);
+                    const float2 x1 = *reinterpret_cast<const float2 *>(b1 + (4 * q + e) * kSlotRow);
+                    const float2 x2 = *reinterpret_cast<const float2 *>(b2 + (4 * q + e) * kSlotRow);
+                    acc[0] = fmaf(v1[e], x1.x, acc[0]); acc[1] = fmaf(v1[e], x1.y, acc[1]);
+                    acc[2] = fmaf(v2[e], x2.x, acc[2]); acc[3] = fmaf(v2[e], x2.y, acc[3]);
                 }
             }
-            acc0 += acc2; acc1 += acc3;
-            if (b == 1)
-                *reinterpret_cast<float2 *>(blk(kSlotT + 2) + r * kSlotRow + c0) = make_float2(acc0, acc1);
-            *reinterpret_cast<uint32_t *>(base + OFF_WT + sw128_off(16 * b + r, 16 * (b + 2) + c0)) =
-                pack_bf16(acc0, acc1);
-        }
-        __syncthreads();
-        {  // third diagonal: T_03 = N_01 T_13 + N_02 T_23 + N_03 T_33; row r, column c
-            const int r = tid & 15, c = tid >> 4;
-            const float *n1 = blk(kSlotN + up_idx(0, 1)) + r * kSlotRow;
-            const float *n2 = blk(kSlotN + up_idx(0, 2)) + r * kSlotRow;
-            const float *n3 = blk(kSlotN + up_idx(0, 3)) + r * kSlotRow;
-            const float *t1 = blk(kSlotT + 2) + c, *t2 = blk(kSlotT + 1) + c, *t3 = blk(3) + c;
-            float a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float4 y1 = reinterpret_cast<const float4 *>(n1)[q];
-                const float4 y2 = reinterpret_cast<const float4 *>(n2)[q];
-                const float4 y3 = reinterpret_cast<const float4 *>(n3)[q];
-                const float v1[4] = {y1.x, y1.y, y1.z, y1.w}, v2[4] = {y2.x, y2.y, y2.z, y2.w},
-                            v3[4] = {y3.x, y3.y, y3.z, y3.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int u = 4 * q + e;
-                    a1 = fmaf(v1[e], t1[u * kSlotRow], a1);
-                    a2 = fmaf(v2[e], t2[u * kSlotRow], a2);
-                    a3 = fmaf(v3[e], t3[u * kSlotRow], a3);
-                }
-            }
-            *reinterpret_cast<__nv_bfloat16 *>(base + OFF_WT + sw128_off(r, 48 + c)) =
-                __float2bfloat16_rn(a1 + a2 + a3);
+            *reinterpret_cast<uint32_t *>(base + OFF_WT + sw128_off(r, 48 + c0)) =
+                pack_bf16(acc[0] + acc[2], acc[1] + acc[3]);
         }
         fence_proxy_async_smem();
         __syncthreads();
@@ -643,13 +693,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         ph_mma ^= 1;
         tc_fence_after();
         {
-            float v[16];
-#pragma unroll 1
-            for (int g = 0; g < 2; ++g) {
-                tmem_ld16(tmem + lane_base + cpart + 16 * g, v);
-                tmem_ld_wait();
-                store_row16(base + OFF_OPZ, row, cpart + 16 * g, v);
-            }
+            float v[32];
+            tmem_ld32(tmem + lane_base + cpart, v);
+            tmem_ld_wait();
+            store_row16(base + OFF_OPZ, row, cpart, v);
+            store_row16(base + OFF_OPZ, row, cpart + 16, v + 16);
         }
         tc_fence_before();
         fence_proxy_async_smem();
@@ -666,43 +714,44 @@ __global__ void __launch_bounds__(kThreads, 2)
         ph_mma ^= 1;
         tc_fence_after();
         {
-            float v[16], add[16];
+            float v[32], y[32];
             if (row < 64) {  // row j: Phi^T = Phi'^T + diag(gamma); Y_B^T = Y'^T + Khat^T
                 const int j = row;
                 const float gj = gam[j];
-#pragma unroll 1
+                tmem_ld32(tmem + lane_base + cpart, v);
+                tmem_ld32(tmem + lane_base + 64 + cpart, y);
+                tmem_ld_wait();
+#pragma unroll
+                for (int q = 0; q < 32; ++q) v[q] += (cpart + q == j) ? gj : 0.f;
+                store_row16(base + OFF_OPA2, 64 + j, cpart, v);
+                store_row16(base + OFF_OPA2, 64 + j, cpart + 16, v + 16);
+#pragma unroll
                 for (int g = 0; g < 2; ++g) {
-                    const int c00 = cpart + 16 * g;
-                    tmem_ld16(tmem + lane_base + c00, v);
-                    tmem_ld_wait();
+                    float add[16];
+                    load_row16(base + OFF_KHT, j, cpart + 16 * g, add);
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) v[q] += (c00 + q == j) ? gj : 0.f;
-                    store_row16(base + OFF_OPA2, 64 + j, c00, v);
-                    tmem_ld16(tmem + lane_base + 64 + c00, v);
-                    load_row16(base + OFF_KHT, j, c00, add);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int q = 0; q < 16; ++q) v[q] += add[q];
-                    store_row16(base + OFF_OPY, 64 + j, c00, v);
+                    for (int q = 0; q < 16; ++q) y[16 * g + q] += add[q];
+                    store_row16(base + OFF_OPY, 64 + j, cpart + 16 * g, y + 16 * g);
                 }
             } else {  // row t': R'^T = R''^T + R0; Y_Q^T = Y'^T + Qk^T (causal: s <= t')
                 const int tq = row - 64;
-#pragma unroll 1
+                tmem_ld32(tmem + lane_base + cpart, v);
+                tmem_ld32(tmem + lane_base + 64 + cpart, y);
+                tmem_ld_wait();
+#pragma unroll
                 for (int g = 0; g < 2; ++g) {
-                    const int c00 = cpart + 16 * g;
-                    tmem_ld16(tmem + lane_base + c00, v);
-                    load_row16(base + OFF_R0, tq, c00, add);
-                    tmem_ld_wait();
+                    float add[16];
+                    load_row16(base + OFF_R0, tq, cpart + 16 * g, add);
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) v[q] += add[q];
-                    store_row16(base + OFF_OPA2, tq, c00, v);
-                    tmem_ld16(tmem + lane_base + 64 + c00, v);
-                    tmem_ld16(tmem + lane_base + 192 + c00, add);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int q = 0; q < 16; ++q) v[q] += (c00 + q <= tq) ? add[q] : 0.f;
-                    store_row16(base + OFF_OPY, tq, c00, v);
+                    for (int q = 0; q < 16; ++q) v[16 * g + q] += add[q];
+                    store_row16(base + OFF_OPA2, tq, cpart + 16 * g, v + 16 * g);
                 }
+                tmem_ld32(tmem + lane_base + 192 + cpart, v);  // Qk^T
+                tmem_ld_wait();
+#pragma unroll
+                for (int q = 0; q < 32; ++q) y[q] += (cpart + q <= tq) ? v[q] : 0.f;
+                store_row16(base + OFF_OPY, tq, cpart, y);
+                store_row16(base + OFF_OPY, tq, cpart + 16, y + 16);
             }
         }
         tc_fence_before();
@@ -730,37 +779,37 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (row < 64) {  // O row t' -> o[tc0 + t'][h][cpart ..]
             const int tq = row;
             float *dst = p.in.o + (static_cast<size_t>(tc0 + tq) * H + h) * kHeadSize + cpart;
-#pragma unroll 1
-            for (int g = 0; g < 2; ++g) {
-                float v[16];
-                tmem_ld16(tmem + lane_base + 128 + cpart + 16 * g, v);
-                tmem_ld_wait();
-                if (tq < Lc) {
+            float v[32];
+            tmem_ld32(tmem + lane_base + 128 + cpart, v);
+            tmem_ld_wait();
+            if (tq < Lc) {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        reinterpret_cast<float4 *>(dst + 16 * g)[q] =
-                            make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-                }
+                for (int q = 0; q < 8; ++q)
+                    reinterpret_cast<float4 *>(dst)[q] =
+                        make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
             }
         } else {  // S_L^T row j (values i of this thread's part) -> next chunk's hi/lo; last -> slot
             const int j = row - 64;
-#pragma unroll 1
-            for (int g = 0; g < 2; ++g) {
-                const int i0 = cpart + 16 * g;
-                float v[16], hi[16], lo[16];
-                tmem_ld16(tmem + lane_base + 128 + i0, v);
-                tmem_ld_wait();
+            float v[32];
+            tmem_ld32(tmem + lane_base + 128 + cpart, v);
+            tmem_ld_wait();
 #pragma unroll
-                for (int q = 0; q < 16; ++q) {
-                    hi[q] = __bfloat162float(__float2bfloat16_rn(v[q]));
-                    lo[q] = v[q] - hi[q];
-                }
-                store_row16(base + OFF_SHI, j, i0, hi);
-                store_row16(base + OFF_SLO, j, i0, lo);
-                if (last) {
+            for (int q8 = 0; q8 < 4; ++q8) {  // 8 values: bf16 hi and the bf16 of the remainder
+                uint32_t hw[4], lw[4];
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) S[(i0 + q) * kHeadSize + j] = v[q];
+                for (int e = 0; e < 4; ++e) {
+                    const float x0 = v[8 * q8 + 2 * e], x1 = v[8 * q8 + 2 * e + 1];
+                    hw[e] = pack_bf16(x0, x1);
+                    lw[e] = pack_bf16(x0 - bf16_lo(hw[e]), x1 - bf16_hi(hw[e]));
                 }
+                const uint32_t off = sw128_off(j, cpart + 8 * q8);
+                *reinterpret_cast<uint4 *>(base + OFF_SHI + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4 *>(base + OFF_SLO + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            }
+            if (last) {
+                float *sp = S + cpart * kHeadSize + j;  // column j of S, rows cpart..
+#pragma unroll
+                for (int q = 0; q < 32; ++q) sp[q * kHeadSize] = v[q];
             }
         }
         tc_fence_before();
