@@ -265,8 +265,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (len == 0) return;
 
     uint8_t *small = smem_raw;
-    uint8_t *base = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw + kSmallBytes) + 1023) & ~static_cast<uintptr_t>(1023));
+    // Tiles from the next 1024-byte boundary; offsetting smem_raw (rather than
+    // rounding an integer address) keeps the pointers in the shared address space,
+    // so every tile access compiles to a shared-memory instruction.
+    uint8_t *base = smem_raw + kSmallBytes + ((1024u - ((smem_addr(smem_raw) + kSmallBytes) & 1023u)) & 1023u);
     const uint32_t bar_mma = smem_addr(small + SOFF_BAR);
     uint32_t *holder = reinterpret_cast<uint32_t *>(small + SOFF_HOLD);
     volatile int *flag = reinterpret_cast<volatile int *>(small + SOFF_FLAG);
