@@ -112,6 +112,9 @@ __device__ __forceinline__ int up_idx(int i, int j) { return i * (7 - i) / 2 + (
 constexpr uint32_t kSmemBytes = kSmallBytes + 1024 + kTileBytes;  // + worst-case alignment
 static_assert(2 * (kSmemBytes + 1024) <= 228 * 1024, "two CTAs per SM");
 constexpr uint32_t kTmemCols = 256;
+// Tensor-memory columns: G1 0-63, G1' 128-255 (Q_k^T at 192-255 until the G34 readback),
+// G2 0-63, G34 0-127, G5 64-127 (its readback overlaps the next chunk's G1).
+constexpr uint32_t kColG5 = 64;
 
 struct InputMaps {
     CUtensorMap m[6];  // r, w, k, v, a, b
@@ -320,6 +323,48 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int n_chunks = (len + kL - 1) / kL;
     uint32_t ph_mma = 0, ph_tma = 0;
     bool range_bad = false;
+    int prev_tc0 = 0, prev_Lc = 0;  // chunk whose state product awaits its readback
+
+    // Readback of the state product [O^T; S_L^T] (tensor-memory columns kColG5..+63):
+    // O rows to the output, S_L^T rows to the bf16 hi/lo operand tiles of the next
+    // chunk, and after the last chunk the float32 state to the slot.
+    auto readback_state_product = [&](int otc0, int oLc, bool final) {
+        float v[32];
+        tmem_ld32(tmem + lane_base + kColG5 + cpart, v);
+        tmem_ld_wait();
+        if (row < 64) {  // O row t' -> o[otc0 + t'][h][cpart ..]
+            const int tq = row;
+            float *dst = p.in.o + (static_cast<size_t>(otc0 + tq) * H + h) * kHeadSize + cpart;
+            if (tq < oLc) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    reinterpret_cast<float4 *>(dst)[q] =
+                        make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            }
+        } else {  // S_L^T row j (values i of this thread's part)
+            const int j = row - 64;
+            if (final) {
+                float *sp = S + cpart * kHeadSize + j;  // column j of S, rows cpart..
+#pragma unroll
+                for (int q = 0; q < 32; ++q) sp[q * kHeadSize] = v[q];
+            } else {
+#pragma unroll
+                for (int q8 = 0; q8 < 4; ++q8) {  // 8 values: bf16 hi and the bf16 of the remainder
+                    uint32_t hw[4], lw[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float x0 = v[8 * q8 + 2 * e], x1 = v[8 * q8 + 2 * e + 1];
+                        hw[e] = pack_bf16(x0, x1);
+                        lw[e] = pack_bf16(x0 - bf16_lo(hw[e]), x1 - bf16_hi(hw[e]));
+                    }
+                    const uint32_t off = sw128_off(j, cpart + 8 * q8);
+                    *reinterpret_cast<uint4 *>(base + OFF_SHI + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                    *reinterpret_cast<uint4 *>(base + OFF_SLO + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                }
+                fence_proxy_async_smem();  // the hi/lo tiles feed the next state product
+            }
+        }
+    };
 
     for (int c = 0; c < n_chunks; ++c) {
         const int tc0 = t0 + c * kL;
@@ -442,6 +487,10 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                 for (int x = 0; x < 6; ++x) tma_prefetch_l2_3d(&maps.m[x], 0, h, tc0 + kL);
             }
+        }
+        if (c > 0) {  // the previous chunk's state product, read back while G1 runs
+            tc_fence_after();
+            readback_state_product(prev_tc0, prev_Lc, false);
         }
         mma_wait(bar_mma, ph_mma, flag);
         ph_mma ^= 1;
@@ -764,9 +813,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         // ---------------------------------- G5 and the state product S0 [R'|Phi]
         if (tid == 0) {
             tc_fence_after();
-            umma_128xNx64(tmem + 128, smem_addr(base + OFF_OPY), smem_addr(base + OFF_V), 64, false);
-            umma_128xNx64_bmn(tmem + 128, smem_addr(base + OFF_OPA2), smem_addr(base + OFF_SHI), 64, true);
-            umma_128xNx64_bmn(tmem + 128, smem_addr(base + OFF_OPA2), smem_addr(base + OFF_SLO), 64, true);
+            umma_128xNx64(tmem + kColG5, smem_addr(base + OFF_OPY), smem_addr(base + OFF_V), 64, false);
+            umma_128xNx64_bmn(tmem + kColG5, smem_addr(base + OFF_OPA2), smem_addr(base + OFF_SHI), 64, true);
+            umma_128xNx64_bmn(tmem + kColG5, smem_addr(base + OFF_OPA2), smem_addr(base + OFF_SLO), 64, true);
             umma_commit(bar_mma);
             if (!last) {  // the staging tiles are dead now: fetch the next chunk's inputs
                 mbar_arrive_expect_tx(bar_tma, 6 * kTile64);
@@ -778,46 +827,15 @@ __global__ void __launch_bounds__(kThreads, 2)
         mma_wait(bar_mma, ph_mma, flag);
         ph_mma ^= 1;
         tc_fence_after();
-        if (row < 64) {  // O row t' -> o[tc0 + t'][h][cpart ..]
-            const int tq = row;
-            float *dst = p.in.o + (static_cast<size_t>(tc0 + tq) * H + h) * kHeadSize + cpart;
-            float v[32];
-            tmem_ld32(tmem + lane_base + 128 + cpart, v);
-            tmem_ld_wait();
-            if (tq < Lc) {
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    reinterpret_cast<float4 *>(dst)[q] =
-                        make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-            }
-        } else {  // S_L^T row j (values i of this thread's part) -> next chunk's hi/lo; last -> slot
-            const int j = row - 64;
-            float v[32];
-            tmem_ld32(tmem + lane_base + 128 + cpart, v);
-            tmem_ld_wait();
-#pragma unroll
-            for (int q8 = 0; q8 < 4; ++q8) {  // 8 values: bf16 hi and the bf16 of the remainder
-                uint32_t hw[4], lw[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float x0 = v[8 * q8 + 2 * e], x1 = v[8 * q8 + 2 * e + 1];
-                    hw[e] = pack_bf16(x0, x1);
-                    lw[e] = pack_bf16(x0 - bf16_lo(hw[e]), x1 - bf16_hi(hw[e]));
-                }
-                const uint32_t off = sw128_off(j, cpart + 8 * q8);
-                *reinterpret_cast<uint4 *>(base + OFF_SHI + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                *reinterpret_cast<uint4 *>(base + OFF_SLO + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-            }
-            if (last) {
-                float *sp = S + cpart * kHeadSize + j;  // column j of S, rows cpart..
-#pragma unroll
-                for (int q = 0; q < 32; ++q) sp[q * kHeadSize] = v[q];
-            }
-        }
-        tc_fence_before();
-        fence_proxy_async_smem();
-        __syncthreads();
-        if (*flag) break;
+        prev_tc0 = tc0;
+        prev_Lc = Lc;
+        // The readback of this product waits for the next chunk's first MMA (or the loop end);
+        // R1 and the staging tiles are free for the next chunk's elementwise phase now.
+    }
+    __syncthreads();  // every thread sees the same abort flag
+    if (!*flag) {
+        tc_fence_after();
+        readback_state_product(prev_tc0, prev_Lc, true);
     }
 
     if (*flag) {  // a wait gave up: give in-flight MMAs a last chance, then leave
