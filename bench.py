@@ -58,6 +58,8 @@ def parse_args(argv=None):
     p.add_argument("--graph", action="store_true", help="replay each step as a CUDA graph")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--checkpoints", action="store_true",
+                   help="prefill workload: also keep the state at every 64-token boundary")
     return p.parse_args(argv)
 
 
@@ -401,14 +403,20 @@ class Sweep(Workload):
 class Prefill(Workload):
     name = wl.PREFILL_8x4096.name
 
-    def __init__(self, torch, device):
+    def __init__(self, torch, device, checkpoints=False):
         from rwkv_wkv_gb300 import Pool
         W = wl.PREFILL_8x4096
         self.torch, self.W = torch, W
         self.H, self.N = W.H, W.N
         self.S, self.T = 8, 4096
         self.total = self.S * self.T
-        self.pool = Pool(1, W.H, W.n_slots, device=device)
+        self.checkpoints = checkpoints
+        n_ck = self.S * (self.T // 64) if checkpoints else 0
+        self.pool = Pool(1, W.H, W.n_slots, n_snapshots=n_ck, device=device)
+        self.ck = None
+        if checkpoints:  # the state after every 64th token of every sequence
+            i32 = lambda x: torch.as_tensor(np.asarray(x, dtype=np.int32), device=device)  # noqa: E731
+            self.ck = (i32(np.arange(self.S + 1) * (self.T // 64)), i32(np.arange(n_ck)))
         self.pool.alloc(W.n_slots)
         self.pool.free(list(range(W.n_slots))[::-1])
         self.ids = torch.arange(self.S, dtype=torch.int32, device=device)
@@ -418,7 +426,8 @@ class Prefill(Workload):
         self.phases = ["create", "prefill"]
         self.phase_bytes = {"create": self.S * self.pool.slot_bytes,
                             "prefill": self.total * W.H * (W.N * 2 * 6 + W.N * 4)
-                            + self.S * W.H * 2 * HEAD_BYTES_STATE}
+                            + self.S * W.H * 2 * HEAD_BYTES_STATE
+                            + n_ck * W.H * HEAD_BYTES_STATE}
         self.tokens_per_step = self.total
         self.dominant = "prefill"
         self.launches_per_step = 2
@@ -428,17 +437,25 @@ class Prefill(Workload):
         rec("start")
         created = self.pool.create(self.S)
         rec("create")
-        self.pool.prefill(0, self.ids, self.cu, *self.ins, o=self.o, max_seqlen=self.T)
+        if self.ck is None:
+            self.pool.prefill(0, self.ids, self.cu, *self.ins, o=self.o, max_seqlen=self.T)
+        else:
+            self.pool.prefill(0, self.ids, self.cu, *self.ins, o=self.o, max_seqlen=self.T,
+                              cu_ckpt=self.ck[0], ckpt_ids=self.ck[1])
         rec("prefill")
         self.pool.free(created[::-1])
 
     def host_io(self):
-        return [self.ids, self.cu] + list(self.ins), [self.o]
+        meta = [self.ids, self.cu] + (list(self.ck) if self.ck is not None else [])
+        return meta + list(self.ins), [self.o]
 
     def config(self):
-        return {"workload": self.W.description, "layers": 1, "heads": self.H,
+        return {"workload": self.W.description
+                + (" + state checkpoint every 64 tokens" if self.checkpoints else ""),
+                "layers": 1, "heads": self.H,
                 "head_size": self.N, "prefill_seqs": self.S, "prefill_tokens": self.total,
-                "chunk": 64, "state_dtype": "f32", "input_dtype": "bf16", "output_dtype": "f32"}
+                "chunk": 64, "state_dtype": "f32", "input_dtype": "bf16", "output_dtype": "f32",
+                "checkpoints": self.S * (self.T // 64) if self.checkpoints else 0}
 
     def oracle_sample(self, frac_target):
         return _head_sample(self.H, frac_target, 0, np.array([self.T] * self.S),
@@ -451,7 +468,7 @@ def make_workload(args, torch, device):
     if args.workload == "decode12":
         return Decode12(torch, device)
     if args.workload == "prefill":
-        return Prefill(torch, device)
+        return Prefill(torch, device, checkpoints=args.checkpoints)
     return Sweep(torch, device, args.batch)
 
 

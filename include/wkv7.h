@@ -193,6 +193,30 @@ wkv7_status wkv7_decode_step(wkv7_pool *pool, int32_t layer, const int32_t *slot
                              const void *k, const void *v, const void *a, const void *b,
                              float *o, cudaStream_t stream);
 
+/* decode_multi: n_tokens (K >= 1) consecutive tokens for each of n slots at
+ * one layer, the verify pass of speculative decoding on state slots (the
+ * rvLLM README, "Speculative decoding (GPU, shipped)": K drafted tokens are
+ * checked by one pass over K+1 tokens; with a recurrent state the pass must
+ * also leave a state at every token so that the slot can be rolled back to
+ * the last accepted one, the fork/restore verbs of "wkvm: state-slot
+ * inference for RWKV, GDN and Mamba hybrids").  Inputs x[b][k][h][:] and
+ * o[b][k][h][:] are [n][K][n_heads][64]; row b's state at
+ * (slot_ids_dev[b], layer) takes the K steps in order, held on chip between
+ * them (read once, written once), and o gets every token's readout.  With
+ * step_snap_ids_dev ([n][K] device ids, or NULL for none) the state after
+ * token k of row b is also written to this layer's slice of snapshot
+ * step_snap_ids_dev[b*K + k]; restoring that snapshot rolls the slot back to
+ * just after token k.  K == 1 without snapshots equals wkv7_decode_step bit
+ * for bit.  Errors: INVALID_ARG (including n > n_slots, K < 1, snapshots
+ * asked of a pool without a snapshot store), UNSUPPORTED, CUDA.  Device:
+ * WKV7_DEV_BAD_SLOT for an out-of-range slot id (that row is untouched) or
+ * snapshot id (that snapshot is not written). */
+wkv7_status wkv7_decode_multi(wkv7_pool *pool, int32_t layer, const int32_t *slot_ids_dev,
+                              int32_t n, int32_t n_tokens, wkv7_dtype in_dtype, const void *r,
+                              const void *w, const void *k, const void *v, const void *a,
+                              const void *b, float *o, const int32_t *step_snap_ids_dev,
+                              cudaStream_t stream);
+
 /* prefill: n_seqs sequences packed back to back (RWKV-X Architecture, "What
  * Was Stripped": the batch forward is the prefill path).  Sequence s holds
  * tokens cu_seqlens_dev[s] .. cu_seqlens_dev[s+1]-1 of the packed inputs
@@ -224,6 +248,34 @@ wkv7_status wkv7_prefill_sequential(wkv7_pool *pool, int32_t layer,
                                     wkv7_dtype in_dtype, const void *r, const void *w,
                                     const void *k, const void *v, const void *a,
                                     const void *b, float *o, cudaStream_t stream);
+
+/* prefill_checkpointed: wkv7_prefill (sequential == 0) or
+ * wkv7_prefill_sequential (sequential != 0) that also keeps the state at
+ * every 64-token boundary of each sequence (xLLM, "Virtual Memory for KV
+ * Cache and Model Weights", prefix caching: chunked prefill publishes whole
+ * blocks only, and a hybrid model's linear-attention part can resume a
+ * cached prefix only from a stored state).  Sequence s (length len_s) owns the ids
+ * ckpt_snap_ids_dev[cu_ckpt_dev[s] .. cu_ckpt_dev[s+1]-1], which must number
+ * len_s / 64 (rounded down); the m-th (m = 1, 2, ...) receives, in this
+ * layer's slice of that snapshot, the float32 state after the sequence's
+ * token 64*m, exactly as the next chunk starts from it, so restoring it and
+ * prefilling the rest of the sequence reproduces the uninterrupted run's
+ * later outputs and final state bit for bit on either path.  When a
+ * length is a multiple of 64 the last checkpoint equals the final state.
+ * cu_ckpt_dev ([n_seqs+1]) and ckpt_snap_ids_dev are caller-owned device
+ * arrays.  Errors: those of the chosen path, and INVALID_ARG when either array
+ * is missing or the pool has no snapshot store.  Device: WKV7_DEV_BAD_SEQLENS
+ * for a count that does not match (that sequence is skipped),
+ * WKV7_DEV_BAD_SLOT for an out-of-range snapshot id (that checkpoint is not
+ * written). */
+wkv7_status wkv7_prefill_checkpointed(wkv7_pool *pool, int32_t layer, const int32_t *slot_ids_dev,
+                                      const int32_t *cu_seqlens_dev, int32_t n_seqs,
+                                      int32_t total_tokens, int32_t max_seqlen,
+                                      wkv7_dtype in_dtype, const void *r, const void *w,
+                                      const void *k, const void *v, const void *a,
+                                      const void *b, float *o, const int32_t *cu_ckpt_dev,
+                                      const int32_t *ckpt_snap_ids_dev, int32_t sequential,
+                                      cudaStream_t stream);
 
 /* ------------------------------------------------------------- status ---- */
 

@@ -178,6 +178,61 @@ def prefill(states, cu_seqlens, r, w, k, v, a, b, n_threads: int = 1):
     return o.reshape(Ttot, H, N), S.reshape(nS, H, N, N)
 
 
+def prefill_checkpoints(states, cu_seqlens, r, w, k, v, a, b, n_threads: int = 1,
+                        every: int = 64):
+    """Ragged prefill that also returns the state after every `every`-th token.
+
+    The sequential recurrence is run segment by segment (segment m of sequence
+    s covers its tokens every*m .. every*(m+1)-1) with the state carried from
+    one segment to the next, so each recorded state is the recurrence's state
+    after that token (the stored linear-state checkpoint of a chunked prefill:
+    xLLM, "Virtual Memory for KV Cache and Model Weights", prefix caching).
+    Returns (o [Ttot, H, N], final states [S, H, N, N], checkpoints) where
+    checkpoints[s] is a list of len_s // every arrays [H, N, N].
+    """
+    st = _f64(states)
+    nS, H, N, _ = st.shape
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    lens = np.diff(cu)
+    S = st.reshape(nS * H, N, N).copy()
+    Ttot = np.asarray(r).shape[0]
+    o = np.zeros(Ttot * H * N)
+    ckpts = [[] for _ in range(nS)]
+    n_seg = int((lens.max() + every - 1) // every) if nS else 0
+    for m in range(n_seg):
+        base = np.empty(nS * H, dtype=np.int64)
+        T = np.empty(nS * H, dtype=np.int32)
+        for s_ in range(nS):
+            t_seg = int(max(0, min(every, lens[s_] - every * m)))
+            for h in range(H):
+                base[s_ * H + h] = (cu[s_] + every * m) * H * N + h * N
+                T[s_ * H + h] = t_seg
+        o_seg, S = run_units(S, base, T, H * N, (r, w, k, v, a, b), n_threads)
+        o += o_seg  # each token is written by exactly one segment
+        for s_ in range(nS):
+            if lens[s_] >= every * (m + 1):
+                ckpts[s_].append(S.reshape(nS, H, N, N)[s_].copy())
+    return o.reshape(Ttot, H, N), S.reshape(nS, H, N, N), ckpts
+
+
+def decode_multi(states, r, w, k, v, a, b, n_threads: int = 1):
+    """K consecutive tokens on each of B rows (the verify pass of speculative
+    decoding: rvLLM README, "Speculative decoding").
+
+    states: [B, H, N, N]; inputs [B, K, H, N].  Returns (o [B, K, H, N], final
+    states [B, H, N, N], per-token states [B, K, H, N, N]) in float64, where
+    per-token state k is the state right after token k.
+    """
+    st = _f64(states)
+    B, H, N, _ = st.shape
+    K = np.asarray(r).shape[1]
+    flat = [_f64(x).reshape(B * K, H, N) for x in (r, w, k, v, a, b)]
+    cu = np.arange(B + 1, dtype=np.int64) * K
+    o, S, ck = prefill_checkpoints(st, cu, *flat, n_threads=n_threads, every=1)
+    per_tok = np.stack([np.stack(c) for c in ck]) if B and K else np.zeros((B, K, H, N, N))
+    return o.reshape(B, K, H, N), S, per_tok
+
+
 def rel_err(x, ref) -> float:
     """Normwise-max relative error: max|x - ref| / max|ref| (0 when both are 0)."""
     x = np.asarray(x, dtype=np.float64)

@@ -360,12 +360,40 @@ wkv7_status wkv7_decode_step(wkv7_pool *pool, int32_t layer, const int32_t *slot
     return cuda_status("decode_step", e, launches);
 }
 
+wkv7_status wkv7_decode_multi(wkv7_pool *pool, int32_t layer, const int32_t *slot_ids_dev,
+                              int32_t n, int32_t n_tokens, wkv7_dtype in_dtype, const void *r,
+                              const void *w, const void *k, const void *v, const void *a,
+                              const void *b, float *o, const int32_t *step_snap_ids_dev,
+                              cudaStream_t stream) {
+    if (!pool || layer < 0 || layer >= pool->desc.n_layers || n < 0 || n_tokens < 1)
+        return WKV7_ERR_INVALID_ARG;
+    if (!dtype_valid(in_dtype)) return WKV7_ERR_INVALID_ARG;
+    if (n > pool->desc.n_slots) return WKV7_ERR_INVALID_ARG;
+    if (n == 0) return WKV7_OK;
+    if (!slot_ids_dev || !inputs_present(r, w, k, v, a, b, o)) return WKV7_ERR_INVALID_ARG;
+    if (step_snap_ids_dev && pool->desc.n_snapshots == 0) return WKV7_ERR_INVALID_ARG;
+    if (static_cast<long long>(n) * n_tokens > 0x7fffffffLL) return WKV7_ERR_INVALID_ARG;
+    wkv7::DecodeMultiArgs da;
+    da.lv = layer_view(pool, layer);
+    da.slot_ids = slot_ids_dev;
+    da.n = n;
+    da.n_tok = n_tokens;
+    da.in = {r, w, k, v, a, b, in_dtype == WKV7_BF16, o};
+    da.snaps = pool->snaps;
+    da.n_snaps = pool->desc.n_snapshots;
+    da.step_snap_ids = step_snap_ids_dev;
+    int launches = 0;
+    cudaError_t e = wkv7::launch_decode_multi(da, stream, &launches);
+    return cuda_status("decode_multi", e, launches);
+}
+
 static wkv7_status prefill_common(wkv7_pool *pool, int32_t layer, const int32_t *slot_ids_dev,
                                   const int32_t *cu_seqlens_dev, int32_t n_seqs,
                                   int32_t total_tokens, int32_t max_seqlen, wkv7_dtype in_dtype,
                                   const void *r, const void *w, const void *k, const void *v,
                                   const void *a, const void *b, float *o, cudaStream_t stream,
-                                  bool chunked) {
+                                  bool chunked, const int32_t *cu_ckpt_dev = nullptr,
+                                  const int32_t *ckpt_snap_ids_dev = nullptr) {
     if (!pool || layer < 0 || layer >= pool->desc.n_layers) return WKV7_ERR_INVALID_ARG;
     if (n_seqs < 0 || total_tokens < 0 || max_seqlen < 0) return WKV7_ERR_INVALID_ARG;
     if (!dtype_valid(in_dtype)) return WKV7_ERR_INVALID_ARG;
@@ -388,6 +416,7 @@ static wkv7_status prefill_common(wkv7_pool *pool, int32_t layer, const int32_t 
     pa.total_tokens = total_tokens;
     pa.max_seqlen = max_seqlen;
     pa.in = {r, w, k, v, a, b, in_dtype == WKV7_BF16, o};
+    pa.ck = {pool->snaps, pool->desc.n_snapshots, cu_ckpt_dev, ckpt_snap_ids_dev};
     int launches = 0;
     cudaError_t e = chunked ? wkv7::launch_prefill_chunked(pa, stream, &launches)
                             : wkv7::launch_prefill_sequential(pa, stream, &launches);
@@ -411,6 +440,22 @@ wkv7_status wkv7_prefill_sequential(wkv7_pool *pool, int32_t layer, const int32_
                                     float *o, cudaStream_t stream) {
     return prefill_common(pool, layer, slot_ids_dev, cu_seqlens_dev, n_seqs, total_tokens,
                           max_seqlen, in_dtype, r, w, k, v, a, b, o, stream, false);
+}
+
+wkv7_status wkv7_prefill_checkpointed(wkv7_pool *pool, int32_t layer, const int32_t *slot_ids_dev,
+                                      const int32_t *cu_seqlens_dev, int32_t n_seqs,
+                                      int32_t total_tokens, int32_t max_seqlen,
+                                      wkv7_dtype in_dtype, const void *r, const void *w,
+                                      const void *k, const void *v, const void *a, const void *b,
+                                      float *o, const int32_t *cu_ckpt_dev,
+                                      const int32_t *ckpt_snap_ids_dev, int32_t sequential,
+                                      cudaStream_t stream) {
+    if (!pool) return WKV7_ERR_INVALID_ARG;
+    if (n_seqs > 0 && (!cu_ckpt_dev || !ckpt_snap_ids_dev)) return WKV7_ERR_INVALID_ARG;
+    if (n_seqs > 0 && pool->desc.n_snapshots == 0) return WKV7_ERR_INVALID_ARG;  // nowhere to write
+    return prefill_common(pool, layer, slot_ids_dev, cu_seqlens_dev, n_seqs, total_tokens,
+                          max_seqlen, in_dtype, r, w, k, v, a, b, o, stream, sequential == 0,
+                          cu_ckpt_dev, ckpt_snap_ids_dev);
 }
 
 // ----------------------------------------------------------------- status --

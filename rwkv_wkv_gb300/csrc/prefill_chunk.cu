@@ -265,6 +265,14 @@ __global__ void __launch_bounds__(kThreads, 2)
         return;
     }
     const int len = t1 - t0;
+    int ck0 = 0;  // this sequence's first checkpoint id index
+    if (p.ck.cu_ckpt) {
+        ck0 = __ldg(p.ck.cu_ckpt + seq);
+        if (ck0 < 0 || __ldg(p.ck.cu_ckpt + seq + 1) - ck0 != len / kL) {
+            if (tid == 0 && h == 0) flag_status(p.lv.status, WKV7_DEV_BAD_SEQLENS);
+            return;
+        }
+    }
     if (len == 0) return;
 
     uint8_t *small = smem_raw;
@@ -323,12 +331,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int n_chunks = (len + kL - 1) / kL;
     uint32_t ph_mma = 0, ph_tma = 0;
     bool range_bad = false;
-    int prev_tc0 = 0, prev_Lc = 0;  // chunk whose state product awaits its readback
+    int prev_c = 0, prev_tc0 = 0, prev_Lc = 0;  // chunk whose state product awaits its readback
 
     // Readback of the state product [O^T; S_L^T] (tensor-memory columns kColG5..+63):
     // O rows to the output, S_L^T rows to the bf16 hi/lo operand tiles of the next
-    // chunk, and after the last chunk the float32 state to the slot.
-    auto readback_state_product = [&](int otc0, int oLc, bool final) {
+    // chunk, after the last chunk the float32 state to the slot, and after a full
+    // chunk the float32 state to its checkpoint snapshot when checkpoints are asked for.
+    auto readback_state_product = [&](int occ, int otc0, int oLc, bool final) {
         float v[32];
         tmem_ld32(tmem + lane_base + kColG5 + cpart, v);
         tmem_ld_wait();
@@ -343,6 +352,17 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
         } else {  // S_L^T row j (values i of this thread's part)
             const int j = row - 64;
+            if (p.ck.cu_ckpt && oLc == kL) {  // the state at token 64 (occ + 1) of the sequence
+                const int id = __ldg(p.ck.ckpt_ids + ck0 + occ);
+                if (id >= 0 && id < p.ck.n_snaps) {
+                    float *cp = p.ck.snaps + static_cast<size_t>(id) * p.lv.slot_stride + p.lv.layer_off +
+                                static_cast<size_t>(h) * kHeadFloats + cpart * kHeadSize + j;
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) cp[q * kHeadSize] = v[q];
+                } else if (j == 0) {
+                    flag_status(p.lv.status, WKV7_DEV_BAD_SLOT);
+                }
+            }
             if (final) {
                 float *sp = S + cpart * kHeadSize + j;  // column j of S, rows cpart..
 #pragma unroll
@@ -490,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         if (c > 0) {  // the previous chunk's state product, read back while G1 runs
             tc_fence_after();
-            readback_state_product(prev_tc0, prev_Lc, false);
+            readback_state_product(prev_c, prev_tc0, prev_Lc, false);
         }
         mma_wait(bar_mma, ph_mma, flag);
         ph_mma ^= 1;
@@ -827,6 +847,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         mma_wait(bar_mma, ph_mma, flag);
         ph_mma ^= 1;
         tc_fence_after();
+        prev_c = c;
         prev_tc0 = tc0;
         prev_Lc = Lc;
         // The readback of this product waits for the next chunk's first MMA (or the loop end);
@@ -835,7 +856,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     __syncthreads();  // every thread sees the same abort flag
     if (!*flag) {
         tc_fence_after();
-        readback_state_product(prev_tc0, prev_Lc, true);
+        readback_state_product(prev_c, prev_tc0, prev_Lc, true);
     }
 
     if (*flag) {  // a wait gave up: give in-flight MMAs a last chance, then leave

@@ -39,6 +39,14 @@ __global__ void __launch_bounds__(256) prefill_seq_kernel(PrefillArgs p) {
         if (threadIdx.x == 0 && h == 0) flag_status(p.lv.status, WKV7_DEV_BAD_SEQLENS);
         return;
     }
+    int ck0 = 0;  // this sequence's first checkpoint id index
+    if (p.ck.cu_ckpt) {
+        ck0 = __ldg(p.ck.cu_ckpt + seq);
+        if (ck0 < 0 || __ldg(p.ck.cu_ckpt + seq + 1) - ck0 != (t1 - t0) / 64) {
+            if (threadIdx.x == 0 && h == 0) flag_status(p.lv.status, WKV7_DEV_BAD_SEQLENS);
+            return;
+        }
+    }
     float *S = p.lv.states + static_cast<size_t>(slot) * p.lv.slot_stride + p.lv.layer_off +
                static_cast<size_t>(h) * kHeadFloats;
     const int tid = threadIdx.x;
@@ -104,6 +112,20 @@ __global__ void __launch_bounds__(256) prefill_seq_kernel(PrefillArgs p) {
             osum += __shfl_xor_sync(0xffffffffu, osum, 1);
             osum += __shfl_xor_sync(0xffffffffu, osum, 2);
             if (q == 0) p.in.o[(static_cast<size_t>(tb + tau) * H + h) * kHeadSize + i] = osum;
+        }
+        const int done = tb + n_tok - t0;  // tokens of the sequence consumed so far
+        if (p.ck.cu_ckpt && n_tok == kTile && (done & 63) == 0) {  // a 64-token boundary
+            const int id = __ldg(p.ck.ckpt_ids + ck0 + done / 64 - 1);
+            if (id >= 0 && id < p.ck.n_snaps) {
+                float *cp = p.ck.snaps + static_cast<size_t>(id) * p.lv.slot_stride + p.lv.layer_off +
+                            static_cast<size_t>(h) * kHeadFloats + i * kHeadSize + 16 * q;
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+                    reinterpret_cast<float4 *>(cp)[m] =
+                        make_float4(s[4 * m], s[4 * m + 1], s[4 * m + 2], s[4 * m + 3]);
+            } else if (tid == 0) {
+                flag_status(p.lv.status, WKV7_DEV_BAD_SLOT);
+            }
         }
     }
 #pragma unroll

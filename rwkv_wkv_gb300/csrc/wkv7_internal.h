@@ -33,6 +33,30 @@ struct DecodeArgs {
     TokenInputs in;
 };
 
+// K consecutive tokens per slot: inputs and o are [n][K][H][64]; with
+// step_snap_ids ([n][K]) non-null, the state after token k of row b also goes
+// to snapshot step_snap_ids[b*K + k] (this layer's slice).
+struct DecodeMultiArgs {
+    LayerView lv;
+    const int *slot_ids;
+    int n;
+    int n_tok;
+    TokenInputs in;
+    float *snaps;
+    int n_snaps;
+    const int *step_snap_ids;
+};
+
+// Optional states at every 64-token boundary of each sequence: sequence s
+// writes the state after its token 64*m (m = 1 .. len_s / 64) into snapshot
+// ckpt_ids[cu_ckpt[s] + m - 1] (this layer's slice).  cu_ckpt == nullptr: none.
+struct CheckpointArgs {
+    float *snaps;          // snapshot store base (snapshot 0, layer 0, head 0)
+    int n_snaps;
+    const int *cu_ckpt;    // [n_seqs + 1]
+    const int *ckpt_ids;
+};
+
 struct PrefillArgs {
     LayerView lv;
     const int *slot_ids;
@@ -41,6 +65,7 @@ struct PrefillArgs {
     int total_tokens;
     int max_seqlen;
     TokenInputs in;
+    CheckpointArgs ck;
 };
 
 // Whole-slot copies: dst[dst_ids[i]] <- src[src_ids[i]], slot_floats each.
@@ -62,6 +87,7 @@ struct ZeroIds {
 };
 
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s, int *launches);
+cudaError_t launch_decode_multi(const DecodeMultiArgs &a, cudaStream_t s, int *launches);
 cudaError_t launch_prefill_sequential(const PrefillArgs &a, cudaStream_t s, int *launches);
 cudaError_t launch_prefill_chunked(const PrefillArgs &a, cudaStream_t s, int *launches);
 cudaError_t launch_slot_copy(const CopyArgs &a, cudaStream_t s, int *launches);

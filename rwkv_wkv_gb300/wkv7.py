@@ -72,6 +72,10 @@ _SIGS = {
                      + [_VP] * 7 + [_VP]),
     "wkv7_prefill_sequential": (ctypes.c_int, [_P, _I32, _VP, _VP, _I32, _I32, _I32, ctypes.c_int]
                                 + [_VP] * 7 + [_VP]),
+    "wkv7_decode_multi": (ctypes.c_int, [_P, _I32, _VP, _I32, _I32, ctypes.c_int] + [_VP] * 7
+                          + [_VP, _VP]),
+    "wkv7_prefill_checkpointed": (ctypes.c_int, [_P, _I32, _VP, _VP, _I32, _I32, _I32, ctypes.c_int]
+                                  + [_VP] * 7 + [_VP, _VP, _I32, _VP]),
     "wkv7_get_device_status": (ctypes.c_int, [_P, _VP, _I32, _I32P]),
     "wkv7_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "wkv7_last_error": (ctypes.c_char_p, []),
@@ -280,14 +284,58 @@ class Pool:
                                           _stream_handle(stream, self.device)), "decode_step")
         return o
 
+    def decode_multi(self, layer: int, slot_ids: torch.Tensor, r, w, k, v, a, b, o=None,
+                     step_snap_ids: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        """K consecutive tokens per slot: inputs [n, K, n_heads, 64] (one dtype), o the
+        same shape in float32; with step_snap_ids ([n, K] device int32) the state after
+        every token also goes to those snapshot ids (this layer)."""
+        n = slot_ids.numel()
+        if r.dim() != 4 or r.shape[0] != n:
+            raise ValueError("decode_multi inputs must be [n, K, n_heads, 64]")
+        K = int(r.shape[1])
+        dt, ptrs = self._inputs(tuple(x.reshape(n * K, *x.shape[2:]) if x.dim() == 4 and
+                                      tuple(x.shape[:2]) == (n, K) else x
+                                      for x in (r, w, k, v, a, b)), n * K)
+        if o is None:
+            o = torch.empty(n, K, self.n_heads, self.head_size, dtype=torch.float32,
+                            device=self.device)
+        self._out(o.reshape(n * K, *o.shape[2:]) if o.dim() == 4 else o, n * K)
+        snaps = None
+        if step_snap_ids is not None:
+            if step_snap_ids.numel() != n * K:
+                raise ValueError("step_snap_ids must hold n * K ids")
+            snaps = _dev_i32(step_snap_ids, "step_snap_ids", self.device)
+        _check(self._lib.wkv7_decode_multi(self._h, layer, _dev_i32(slot_ids, "slot_ids", self.device),
+                                           n, K, dt, *ptrs, o.data_ptr(), snaps,
+                                           _stream_handle(stream, self.device)), "decode_multi")
+        return o
+
     def prefill(self, layer: int, slot_ids: torch.Tensor, cu_seqlens: torch.Tensor, r, w, k, v,
                 a, b, o=None, max_seqlen: int | None = None, stream=None,
-                sequential: bool = False) -> torch.Tensor:
+                sequential: bool = False, cu_ckpt: torch.Tensor | None = None,
+                ckpt_ids: torch.Tensor | None = None) -> torch.Tensor:
+        """Prefill; with cu_ckpt / ckpt_ids (device int32), also the state at every
+        64-token boundary of each sequence into those snapshot ids (this layer)."""
         total = r.shape[0]
         dt, ptrs = self._inputs((r, w, k, v, a, b), total)
         o = self._out(o, total)
         if cu_seqlens.numel() != slot_ids.numel() + 1:
             raise ValueError("cu_seqlens must have n_seqs + 1 entries")
+        if (cu_ckpt is None) != (ckpt_ids is None):
+            raise ValueError("cu_ckpt and ckpt_ids go together")
+        if cu_ckpt is not None:
+            if cu_ckpt.numel() != slot_ids.numel() + 1:
+                raise ValueError("cu_ckpt must have n_seqs + 1 entries")
+            ids_ptr = _dev_i32(ckpt_ids, "ckpt_ids", self.device) if ckpt_ids.numel() else None
+            if ids_ptr is None:  # no boundary anywhere: any non-null pointer will do
+                ids_ptr = _dev_i32(cu_ckpt, "cu_ckpt", self.device)
+            _check(self._lib.wkv7_prefill_checkpointed(
+                self._h, layer, _dev_i32(slot_ids, "slot_ids", self.device),
+                _dev_i32(cu_seqlens, "cu_seqlens", self.device), slot_ids.numel(), total,
+                total if max_seqlen is None else int(max_seqlen), dt, *ptrs, o.data_ptr(),
+                _dev_i32(cu_ckpt, "cu_ckpt", self.device), ids_ptr, int(bool(sequential)),
+                _stream_handle(stream, self.device)), "prefill_checkpointed")
+            return o
         fn = self._lib.wkv7_prefill_sequential if sequential else self._lib.wkv7_prefill
         _check(fn(self._h, layer, _dev_i32(slot_ids, "slot_ids", self.device),
                   _dev_i32(cu_seqlens, "cu_seqlens", self.device), slot_ids.numel(), total,

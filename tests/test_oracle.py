@@ -239,6 +239,58 @@ def test_batched_units_match_single_head_calls():
             np.testing.assert_array_equal(S[s, h], S1)
 
 
+def test_checkpoints_match_matrix_product_of_the_prefix():
+    """Chunk-boundary checkpoints (xLLM, "Virtual Memory for KV Cache and Model
+    Weights", prefix caching): the state recorded after token every*m of a
+    sequence equals the matrix-product form (an independent closed form) over
+    that prefix, and a sequence whose length is a multiple of the spacing ends
+    on its final state."""
+    rng = np.random.default_rng(17)
+    H, N, every = 2, 4, 8
+    lens = [20, 8, 3, 0, 16]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    Ttot = int(cu[-1])
+    ins = [rng.standard_normal((Ttot, H, N)) * 0.5 for _ in range(6)]
+    ins[1] = rng.uniform(0.3, 1.1, (Ttot, H, N))  # non-contractive steps too
+    S0 = rng.standard_normal((len(lens), H, N, N))
+    o, S, ck = oracle.prefill_checkpoints(S0, cu, *ins, every=every)
+    o_ref, S_ref = oracle.prefill(S0, cu, *ins)
+    np.testing.assert_array_equal(o, o_ref)
+    np.testing.assert_array_equal(S, S_ref)
+    assert [len(c) for c in ck] == [n // every for n in lens]
+    for s_, n in enumerate(lens):
+        for m, c in enumerate(ck[s_]):
+            sl = slice(cu[s_], cu[s_] + every * (m + 1))
+            for h in range(H):
+                _, Sm = oracle.matprod(S0[s_, h], *[x[sl, h] for x in ins])
+                np.testing.assert_allclose(c[h], Sm, rtol=1e-10, atol=1e-10)
+        if n and n % every == 0:
+            np.testing.assert_array_equal(ck[s_][-1], S[s_])
+
+
+def test_multi_token_decode_states_match_matrix_product():
+    """K tokens per row: per-token states equal the matrix-product form over the
+    row's first k+1 tokens, outputs equal K successive single-token steps."""
+    rng = np.random.default_rng(19)
+    B, K, H, N = 3, 5, 2, 4
+    ins = [rng.standard_normal((B, K, H, N)) * 0.5 for _ in range(6)]
+    ins[1] = rng.uniform(0.3, 1.1, (B, K, H, N))
+    S0 = rng.standard_normal((B, H, N, N))
+    o, S, per_tok = oracle.decode_multi(S0, *ins)
+    assert o.shape == (B, K, H, N) and per_tok.shape == (B, K, H, N, N)
+    np.testing.assert_array_equal(per_tok[:, -1], S)
+    cur = S0.copy()
+    for t in range(K):
+        o1, cur = oracle.decode_step(cur, *[x[:, t] for x in ins])
+        np.testing.assert_array_equal(o[:, t], o1)
+        np.testing.assert_array_equal(per_tok[:, t], cur)
+    for bi in range(B):
+        for h in range(H):
+            for t in range(K):
+                _, Sm = oracle.matprod(S0[bi, h], *[x[bi, :t + 1, h] for x in ins])
+                np.testing.assert_allclose(per_tok[bi, t, h], Sm, rtol=1e-10, atol=1e-10)
+
+
 # ---------------------------------------------------------------- the pins bite
 
 def _planted(S0, r, w, k, v, a, b, mistake):
