@@ -52,7 +52,7 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=["mixed", "decode12", "prefill", "sweep"],
+    p.add_argument("--workload", choices=["mixed", "decode12", "prefill", "sweep", "verify"],
                    default="mixed")
     p.add_argument("--batch", type=int, default=4096, help="sweep batch size")
     p.add_argument("--graph", action="store_true", help="replay each step as a CUDA graph")
@@ -60,6 +60,10 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--checkpoints", action="store_true",
                    help="prefill workload: also keep the state at every 64-token boundary")
+    p.add_argument("--verify-k", type=int, default=5,
+                   help="verify workload: tokens per slot per call (K drafts + 1)")
+    p.add_argument("--no-rollback", action="store_true",
+                   help="verify workload: no per-token rollback states")
     return p.parse_args(argv)
 
 
@@ -462,6 +466,62 @@ class Prefill(Workload):
                             self.tokens_per_step)
 
 
+class Verify(Workload):
+    """Speculative-verify step on slots: K consecutive tokens for each of 1024
+    slots of a 4096-slot, 32-head pool in one call, keeping (by default) the
+    state after every token for rollback."""
+    name = "verify"
+
+    def __init__(self, torch, device, K=5, rollback=True):
+        from rwkv_wkv_gb300 import Pool
+        W = wl.MIXED
+        self.torch, self.W = torch, W
+        self.H, self.N, self.K, self.B = W.H, W.N, K, wl.MIXED_DECODE_B
+        self.rollback = rollback
+        self.pool = Pool(1, W.H, W.n_slots, n_snapshots=self.B * K if rollback else 0,
+                         device=device)
+        g = torch.Generator(device=device).manual_seed(W.seed)
+        self.pool.states.normal_(0.0, 0.1, generator=g)
+        slots = wl.distinct_slots(W.seed, "verify/slots", self.B, W.n_slots)
+        self.ids = torch.as_tensor(slots.astype(np.int32), device=device)
+        self.snaps = (torch.arange(self.B * K, dtype=torch.int32, device=device)
+                      if rollback else None)
+        flat = wl.token_inputs_device(W.seed, self.B * K, W.H, W.N, device, generator_offset=5)
+        self.ins = [x.view(self.B, K, W.H, W.N) for x in flat]
+        self.o = torch.empty(self.B, K, W.H, W.N, dtype=torch.float32, device=device)
+        per_head = 2 * HEAD_BYTES_STATE + K * (W.N * 2 * 6 + W.N * 4)
+        if rollback:
+            per_head += K * HEAD_BYTES_STATE
+        self.phases = ["verify"]
+        self.phase_bytes = {"verify": self.B * W.H * per_head}
+        self.tokens_per_step = self.B * K
+        self.dominant = "verify"
+        self.launches_per_step = 1
+
+    def step(self, ev=None):
+        rec = (lambda name: ev[name].record()) if ev else (lambda name: None)
+        rec("start")
+        self.pool.decode_multi(0, self.ids, *self.ins, o=self.o, step_snap_ids=self.snaps)
+        rec("verify")
+
+    def host_io(self):
+        meta = [self.ids] + ([self.snaps] if self.snaps is not None else [])
+        return meta + list(self.ins), [self.o]
+
+    def config(self):
+        return {"workload": f"speculative verify: {self.K} tokens on each of {self.B} slots of a "
+                f"{self.W.n_slots}-slot pool, 32 heads x 64, 1 layer"
+                + (", state after every token kept for rollback" if self.rollback else ""),
+                "pool_slots": self.W.n_slots, "layers": 1, "heads": self.H, "head_size": self.N,
+                "rows": self.B, "tokens_per_row": self.K, "rollback_states": self.rollback,
+                "state_dtype": "f32", "input_dtype": "bf16", "output_dtype": "f32"}
+
+    def oracle_sample(self, frac_target):
+        # each row is a K-token run of the recurrence: the oracle's prefill form
+        return _head_sample(self.H, frac_target, 0, np.array([self.K] * self.B),
+                            self.tokens_per_step)
+
+
 def make_workload(args, torch, device):
     if args.workload == "mixed":
         return Mixed(torch, device)
@@ -469,6 +529,8 @@ def make_workload(args, torch, device):
         return Decode12(torch, device)
     if args.workload == "prefill":
         return Prefill(torch, device, checkpoints=args.checkpoints)
+    if args.workload == "verify":
+        return Verify(torch, device, K=args.verify_k, rollback=not args.no_rollback)
     return Sweep(torch, device, args.batch)
 
 
@@ -623,6 +685,11 @@ def run_ours(args):
         extra["decode"] = {"slot_steps_per_s": round(n_slot_steps / (phase_ms["decode"] / 1e3), 1),
                            "GB_per_s": phases["decode"]["GB_per_s"],
                            "hbm_frac": phases["decode"]["hbm_frac"]}
+    if "verify" in phase_ms:
+        extra["verify"] = {"slot_token_steps_per_s": round(wk.tokens_per_step
+                                                           / (phase_ms["verify"] / 1e3), 1),
+                           "GB_per_s": phases["verify"]["GB_per_s"],
+                           "hbm_frac": phases["verify"]["hbm_frac"]}
     if "prefill" in phase_ms:
         extra["prefill"] = {"tokens_per_s": round(wk.total / (phase_ms["prefill"] / 1e3), 1),
                             "GB_per_s": phases["prefill"]["GB_per_s"],

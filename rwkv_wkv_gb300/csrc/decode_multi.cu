@@ -14,29 +14,19 @@ namespace {
 
 // K consecutive tokens per (row, head) with the state held in registers
 // throughout: the state is read and written once per call instead of once per
-// token, and only the inputs and readouts scale with K.  The inputs of token
-// k+1 are loaded while token k computes.  With per-token snapshots the state
-// after every token is also streamed to its snapshot (the rollback points of a
-// speculative verify: the rvLLM README, "Speculative decoding", verifies K+1
-// tokens in one pass; wkvm's fork/restore verbs then keep or drop them).
-struct TokIn {
-    float4 a, w, b, k, r;
-    float v[4];
-};
-
-template <bool BF16>
-__device__ __forceinline__ void load_tok(const TokenInputs &in, size_t io, int c, int row0, TokIn &t) {
-    t.a = load4<BF16>(in.a, io + c);
-    t.w = load4<BF16>(in.w, io + c);
-    t.b = load4<BF16>(in.b, io + c);
-    t.k = load4<BF16>(in.k, io + c);
-    t.r = load4<BF16>(in.r, io + c);
-#pragma unroll
-    for (int m = 0; m < 4; ++m) t.v[m] = load1<BF16>(in.v, io + row0 + 16 * m);
-}
+// token, and only the inputs and readouts scale with K.  The inputs of up to
+// kGroup tokens are staged in shared memory (float32) by the whole CTA at once,
+// so their loads overlap each other and the state load instead of sitting on
+// the token chain.  With per-token snapshots the state after every token is also
+// streamed to its snapshot (the rollback points of a speculative verify: the
+// rvLLM README, "Speculative decoding", verifies K+1 tokens in one pass; wkvm's
+// fork/restore verbs then keep or drop them).
+constexpr int kGroup = 8;  // tokens staged per pass
+enum { kR = 0, kW, kK, kV, kA, kB, kInputs };
 
 template <bool BF16, bool SNAPS>
-__global__ void __launch_bounds__(256) decode_multi_kernel(DecodeMultiArgs p) {
+__global__ void __launch_bounds__(256, 5) decode_multi_kernel(DecodeMultiArgs p) {
+    __shared__ __align__(16) float xs[kGroup][kInputs][kHeadSize];
     const int H = p.lv.n_heads;
     const int unit = blockIdx.x;
     const int bi = unit / H;
@@ -60,49 +50,68 @@ __global__ void __launch_bounds__(256) decode_multi_kernel(DecodeMultiArgs p) {
 
     // token k of row bi, head h: [(bi*K + k)*H + h][64]
     auto io_of = [&](int k) { return (static_cast<size_t>(bi) * K + k) * H * kHeadSize + h * kHeadSize; };
-    TokIn cur, nxt;
-    load_tok<BF16>(p.in, io_of(0), c, row0, cur);
 #pragma unroll 1
-    for (int k = 0; k < K; ++k) {
-        if (k + 1 < K) load_tok<BF16>(p.in, io_of(k + 1), c, row0, nxt);
-        float hs[4];
-#pragma unroll
-        for (int m = 0; m < 4; ++m) hs[m] = dot4(s[m], cur.a);
-#pragma unroll
-        for (int off = 8; off >= 1; off >>= 1)
-#pragma unroll
-            for (int m = 0; m < 4; ++m) hs[m] += __shfl_xor_sync(0xffffffffu, hs[m], off);
-        float os[4];
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            s[m].x = fmaf(s[m].x, cur.w.x, fmaf(hs[m], cur.b.x, cur.v[m] * cur.k.x));
-            s[m].y = fmaf(s[m].y, cur.w.y, fmaf(hs[m], cur.b.y, cur.v[m] * cur.k.y));
-            s[m].z = fmaf(s[m].z, cur.w.z, fmaf(hs[m], cur.b.z, cur.v[m] * cur.k.z));
-            s[m].w = fmaf(s[m].w, cur.w.w, fmaf(hs[m], cur.b.w, cur.v[m] * cur.k.w));
-            os[m] = dot4(s[m], cur.r);
+    for (int g0 = 0; g0 < K; g0 += kGroup) {
+        const int ng = min(kGroup, K - g0);
+        if (g0 > 0) __syncthreads();  // the previous group is consumed
+        // stage: ng tokens x 6 inputs x 16 float4 (one float4 per thread per item)
+        for (int e = tid; e < ng * kInputs * 16; e += 256) {
+            const int t = e / (kInputs * 16);
+            const int rem = e - t * (kInputs * 16);
+            const int x = rem >> 4, q = rem & 15;
+            const void *src = x == kR ? p.in.r : x == kW ? p.in.w : x == kK ? p.in.k
+                            : x == kV ? p.in.v : x == kA ? p.in.a : p.in.b;
+            const float4 val = load4<BF16>(src, io_of(g0 + t) + 4 * q);
+            reinterpret_cast<float4 *>(&xs[t][x][0])[q] = val;
         }
-        if (SNAPS) {
-            const int id = __ldg(p.step_snap_ids + static_cast<size_t>(bi) * K + k);
-            if (id >= 0 && id < p.n_snaps) {
-                float *D = p.snaps + static_cast<size_t>(id) * p.lv.slot_stride + p.lv.layer_off +
-                           static_cast<size_t>(h) * kHeadFloats;
+        __syncthreads();
+#pragma unroll 1
+        for (int t = 0; t < ng; ++t) {
+            const int k = g0 + t;
+            const float4 a4 = *reinterpret_cast<const float4 *>(&xs[t][kA][c]);
+            float hs[4];
 #pragma unroll
-                for (int m = 0; m < 4; ++m)
-                    __stcs(reinterpret_cast<float4 *>(D + (row0 + 16 * m) * kHeadSize + c), s[m]);
-            } else if (tid == 0) {
-                flag_status(p.lv.status, WKV7_DEV_BAD_SLOT);
+            for (int m = 0; m < 4; ++m) hs[m] = dot4(s[m], a4);
+#pragma unroll
+            for (int off = 8; off >= 1; off >>= 1)
+#pragma unroll
+                for (int m = 0; m < 4; ++m) hs[m] += __shfl_xor_sync(0xffffffffu, hs[m], off);
+            const float4 w4 = *reinterpret_cast<const float4 *>(&xs[t][kW][c]);
+            const float4 b4 = *reinterpret_cast<const float4 *>(&xs[t][kB][c]);
+            const float4 k4 = *reinterpret_cast<const float4 *>(&xs[t][kK][c]);
+            const float4 r4 = *reinterpret_cast<const float4 *>(&xs[t][kR][c]);
+            float os[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const float vm = xs[t][kV][row0 + 16 * m];
+                s[m].x = fmaf(s[m].x, w4.x, fmaf(hs[m], b4.x, vm * k4.x));
+                s[m].y = fmaf(s[m].y, w4.y, fmaf(hs[m], b4.y, vm * k4.y));
+                s[m].z = fmaf(s[m].z, w4.z, fmaf(hs[m], b4.z, vm * k4.z));
+                s[m].w = fmaf(s[m].w, w4.w, fmaf(hs[m], b4.w, vm * k4.w));
+                os[m] = dot4(s[m], r4);
+            }
+            if (SNAPS) {
+                const int id = __ldg(p.step_snap_ids + static_cast<size_t>(bi) * K + k);
+                if (id >= 0 && id < p.n_snaps) {
+                    float *D = p.snaps + static_cast<size_t>(id) * p.lv.slot_stride + p.lv.layer_off +
+                               static_cast<size_t>(h) * kHeadFloats;
+#pragma unroll
+                    for (int m = 0; m < 4; ++m)
+                        __stcs(reinterpret_cast<float4 *>(D + (row0 + 16 * m) * kHeadSize + c), s[m]);
+                } else if (tid == 0) {
+                    flag_status(p.lv.status, WKV7_DEV_BAD_SLOT);
+                }
+            }
+#pragma unroll
+            for (int off = 8; off >= 1; off >>= 1)
+#pragma unroll
+                for (int m = 0; m < 4; ++m) os[m] += __shfl_xor_sync(0xffffffffu, os[m], off);
+            if ((tid & 15) == 0) {
+                const size_t io = io_of(k);
+#pragma unroll
+                for (int m = 0; m < 4; ++m) p.in.o[io + row0 + 16 * m] = os[m];
             }
         }
-#pragma unroll
-        for (int off = 8; off >= 1; off >>= 1)
-#pragma unroll
-            for (int m = 0; m < 4; ++m) os[m] += __shfl_xor_sync(0xffffffffu, os[m], off);
-        if ((tid & 15) == 0) {
-            const size_t io = io_of(k);
-#pragma unroll
-            for (int m = 0; m < 4; ++m) p.in.o[io + row0 + 16 * m] = os[m];
-        }
-        cur = nxt;
     }
 #pragma unroll
     for (int m = 0; m < 4; ++m)
