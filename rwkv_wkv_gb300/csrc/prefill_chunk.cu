@@ -21,10 +21,12 @@
 // of shared memory and 256 tensor-memory columns each), so one CTA's MMA
 // waits and load latencies are covered by the other's CUDA-core phases.
 // Per chunk:
-//   E   bf16 inputs, TMA-loaded into shared memory during the previous
-//       chunk's last MMA (and prefetched into L2 a chunk before that) ->
+//   E   bf16 inputs, TMA-loaded into shared memory in three pairs as tiles of
+//       the previous chunk go dead (and prefetched into L2 a chunk before
+//       that) ->
 //       log2-decay prefix sums (one warp per 8 tokens, two channels per lane)
-//       -> scaled bf16 operands in 128-byte swizzled K-major tiles.
+//       -> operands scaled in packed bf16 pairs, stored to 128-byte swizzled
+//       K-major tiles.
 // Tensor-memory readbacks give warps w and w+4 the same 32 lanes (rows) and
 // split the columns between them.  Decays inside the Gram products are taken
 //       relative to the chunk midpoint (token 31), so no factor exceeds
@@ -62,6 +64,7 @@ constexpr int kL = 64;
 constexpr int kThreads = 256;  // 8 warps; two CTAs per SM
 constexpr long long kWaitCycles = 4000000000LL;  // about 2 s at 2 GHz
 constexpr float kMaxLog2Range = 120.0f;           // |G - Gm| limit (float exponent range)
+constexpr float kMinDecayRel = 0x1p-120f, kMaxDecayRel = 0x1p120f;  // the same limit on 2^(G - Gm)
 
 // Shared-memory map.  Small items first (from the raw base), then the tiles
 // from the next 1024-byte boundary.  Region R1 is reused through the chunk:
@@ -71,7 +74,7 @@ constexpr uint32_t kTile64 = 8192;    // 64 rows x 128 B (bf16, K = 64)
 constexpr uint32_t kTile128 = 16384;  // 128 rows
 constexpr uint32_t SOFF_TOT = 0;                    // per-warp log2-decay totals [8][64] fp32
 constexpr uint32_t SOFF_GAM = SOFF_TOT + 8 * 64 * 4;  // D(0,L] per channel [64]
-constexpr uint32_t SOFF_BAR = SOFF_GAM + 64 * 4;    // mbarriers: MMA completion, input TMA
+constexpr uint32_t SOFF_BAR = SOFF_GAM + 64 * 4;    // mbarrier: MMA completion
 constexpr uint32_t SOFF_HOLD = SOFF_BAR + 16;       // tensor-memory base
 constexpr uint32_t SOFF_FLAG = SOFF_HOLD + 4;       // abort flag
 constexpr uint32_t kSmallBytes = SOFF_FLAG + 4;
@@ -99,10 +102,12 @@ constexpr uint32_t OFF_R0 = OFF_KHT + kTile64;       // R0 (rows t, K = j)
 constexpr uint32_t OFF_SHI = OFF_R0 + kTile64;       // S0^T hi (rows j, 64 values i; MN-major B)
 constexpr uint32_t OFF_SLO = OFF_SHI + kTile64;      // S0^T lo
 constexpr uint32_t kTileBytes = OFF_SLO + kTile64;
-// Staging of the next chunk's six input boxes ([64 tokens][64 channels] bf16,
-// 8 KB each), loaded by TMA into tiles that are dead from the end of the G34
-// readback until E has read its inputs (E reads them all before its first
-// barrier and writes these tiles only after it).
+// Staging of the next chunk's six inputs ([64 tokens][64 channels] bf16, 8 KB
+// each), TMA-loaded into tiles as they go dead during the current chunk: r, w
+// after G2 (G2A), k, v after G34 (G34B), a, b after the G34 readback (KHT,
+// R0).  All six complete one phase of the input barrier.  The elementwise
+// phase reads them all before its first barrier and writes these tiles only
+// after it.
 __host__ __device__ constexpr uint32_t stage_off(int x) {  // r, w, k, v, a, b
     return x == 0 ? OFF_G2A : x == 1 ? OFF_G2A + kTile64 : x == 2 ? OFF_G34B
          : x == 3 ? OFF_G34B + kTile64 : x == 4 ? OFF_KHT : OFF_R0;
@@ -125,8 +130,17 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&p);
 }
 
-// Hardware base-2 exponential and logarithm (MUFU, ~2 ulp, denormals flushed);
-// the decay factors they produce are rounded to bf16 right after.
+// Product of two bf16 pairs, each lane rounded once to bf16 (nearest even).
+__device__ __forceinline__ uint32_t bmul2(uint32_t x, uint32_t y) {
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(x), "r"(y));
+    return d;
+}
+
+
+// Hardware base-2 exponential, logarithm and reciprocal (MUFU, a few ulp,
+// denormals flushed); the decay factors they produce are rounded to bf16 right
+// after.
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -135,6 +149,11 @@ __device__ __forceinline__ float ex2_approx(float x) {
 __device__ __forceinline__ float lg2_approx(float x) {
     float y;
     asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
 
@@ -288,19 +307,27 @@ __global__ void __launch_bounds__(kThreads, 2)
     auto blk = [base](int b) { return reinterpret_cast<float *>(base + OFF_R1 + b * kSlotBytes); };
 
     if (warp == 0) tmem_alloc(smem_addr(holder), kTmemCols);
-    const uint32_t bar_tma = bar_mma + 8;
     if (tid == 0) {
         mbar_init(bar_mma, 1);
-        mbar_init(bar_tma, 1);
+        mbar_init(bar_mma + 8, 1);  // the input barrier
         fence_mbar_init();
         *flag = 0;
 #pragma unroll
         for (int x = 0; x < 6; ++x) prefetch_tensormap(&maps.m[x]);
-        mbar_arrive_expect_tx(bar_tma, 6 * kTile64);  // chunk 0's inputs
-#pragma unroll
-        for (int x = 0; x < 6; ++x)
-            tma_load_3d(smem_addr(base + stage_off(x)), &maps.m[x], 0, h, t0, bar_tma);
     }
+
+    // TMA loads of inputs x0..x1 (0..5 = r, w, k, v, a, b) of the chunk at token
+    // tcn into their staging tiles, completing on the input barrier (whose
+    // expected byte count, one chunk's six boxes, is set by the first call of
+    // each phase).  Boxes past the last token are zero-filled; the elementwise
+    // phase turns those rows into identity tokens.  Issued by thread 0.
+    const uint32_t bar_in = bar_mma + 8;
+    auto stage_inputs = [&](int x0, int x1, int tcn, bool first) {
+        if (first) mbar_arrive_expect_tx(bar_in, 6 * kTile64);
+        for (int x = x0; x <= x1; ++x)
+            tma_load_3d(smem_addr(base + stage_off(x)), &maps.m[x], 0, h, tcn, bar_in);
+    };
+    if (tid == 0) stage_inputs(0, 5, t0, true);
 
     float *S = p.lv.states + static_cast<size_t>(slot) * p.lv.slot_stride + p.lv.layer_off +
                static_cast<size_t>(h) * kHeadFloats;
@@ -329,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int cpart = 32 * (warp >> 2);      // this thread's 32-column part of each 64-column group
 
     const int n_chunks = (len + kL - 1) / kL;
-    uint32_t ph_mma = 0, ph_tma = 0;
+    uint32_t ph_mma = 0, ph_in = 0;
     bool range_bad = false;
     int prev_c = 0, prev_tc0 = 0, prev_Lc = 0;  // chunk whose state product awaits its readback
 
@@ -395,97 +422,93 @@ __global__ void __launch_bounds__(kThreads, 2)
         {
             const int tb = 8 * warp;  // this warp's 8 tokens; lane: channels 2l, 2l+1
             const int ch = 2 * lane;
-            uint32_t gw[8], ga[8], gb[8], gk[8], gr[8], gv[8];
-            mma_wait(bar_tma, ph_tma, flag);
-            ph_tma ^= 1;
+            uint32_t in_r[8], in_w[8], in_k[8], in_v[8], in_a[8], in_b[8];
+            mma_wait(bar_in, ph_in, flag);  // the staged inputs have landed
+            ph_in ^= 1;
             {
                 auto st = [&](int x, int t) -> uint32_t {
                     return *reinterpret_cast<const uint32_t *>(base + stage_off(x) + t * 128 + 4 * lane);
                 };
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
+                for (int i = 0; i < 8; ++i) {  // tokens past Lc: identity (w = 1, the rest 0)
                     const int t = tb + i;
                     const bool valid = t < Lc;
-                    gr[i] = valid ? st(0, t) : 0u;
-                    gw[i] = valid ? st(1, t) : 0x3F803F80u;  // 1.0, 1.0
-                    gk[i] = valid ? st(2, t) : 0u;
-                    gv[i] = valid ? st(3, t) : 0u;
-                    ga[i] = valid ? st(4, t) : 0u;
-                    gb[i] = valid ? st(5, t) : 0u;
+                    in_r[i] = valid ? st(0, t) : 0u;
+                    in_w[i] = valid ? st(1, t) : 0x3F803F80u;  // 1.0, 1.0
+                    in_k[i] = valid ? st(2, t) : 0u;
+                    in_v[i] = valid ? st(3, t) : 0u;
+                    in_a[i] = valid ? st(4, t) : 0u;
+                    in_b[i] = valid ? st(5, t) : 0u;
                 }
             }
             float s0 = 0.f, s1 = 0.f;  // this warp's log2-decay totals
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                s0 += lg2_approx(bf16_lo(gw[i]));
-                s1 += lg2_approx(bf16_hi(gw[i]));
+                s0 += lg2_approx(bf16_lo(in_w[i]));
+                s1 += lg2_approx(bf16_hi(in_w[i]));
             }
-            tot[warp * 64 + ch] = s0;
-            tot[warp * 64 + ch + 1] = s1;
+            *reinterpret_cast<float2 *>(tot + warp * 64 + ch) = make_float2(s0, s1);
             __syncthreads();
             float G0 = 0.f, G1 = 0.f, Gm0 = 0.f, Gm1 = 0.f, G630 = 0.f, G631 = 0.f;
 #pragma unroll
             for (int w2 = 0; w2 < 8; ++w2) {
-                const float x0 = tot[w2 * 64 + ch], x1 = tot[w2 * 64 + ch + 1];
-                if (w2 < warp) { G0 += x0; G1 += x1; }
-                if (w2 < 4) { Gm0 += x0; Gm1 += x1; }
-                G630 += x0; G631 += x1;
+                const float2 x = *reinterpret_cast<const float2 *>(tot + w2 * 64 + ch);
+                if (w2 < warp) { G0 += x.x; G1 += x.y; }
+                if (w2 < 4) { Gm0 += x.x; Gm1 += x.y; }
+                G630 += x.x; G631 += x.y;
             }
-            if (warp == 0) {
-                gam[ch] = ex2_approx(G630);
-                gam[ch + 1] = ex2_approx(G631);
-            }
+            if (warp == 0) *reinterpret_cast<float2 *>(gam + ch) = make_float2(ex2_approx(G630), ex2_approx(G631));
             if (!(fabsf(G0 - Gm0) <= kMaxLog2Range && fabsf(G1 - Gm1) <= kMaxLog2Range))
                 range_bad = true;  // G[tb-1] (G[-1] = 0 for the first warp)
             const float EL0 = ex2_approx(G630 - Gm0), EL1 = ex2_approx(G631 - Gm1);
             // 2^Gm is a normal float whenever the range check passes (|Gm| <= 120), so
             // the decays from the chunk start are 2^(G - Gm) * 2^Gm.
             const float eGm0 = ex2_approx(Gm0), eGm1 = ex2_approx(Gm1);
-            float ep0 = ex2_approx(G0 - Gm0), ep1 = ex2_approx(G1 - Gm1);  // e_prev
-            float dp0 = ep0 * eGm0, dp1 = ep1 * eGm1;                      // d_prev
+            // e = 2^(G_t - Gm) runs as a product: e_t = e_{t-1} w_t (each e_t lies in
+            // [2^-120, 2^120] when the range check passes, so nothing under- or overflows);
+            // its reciprocal gives 2^(Gm - G_t).
+            float e0 = ex2_approx(G0 - Gm0), e1 = ex2_approx(G1 - Gm1);
+            uint32_t ep2 = pack_bf16(e0, e1);                 // 2^(G_{t-1} - Gm)
+            uint32_t dp2 = pack_bf16(e0 * eGm0, e1 * eGm1);  // D(0, t-1]
             // swizzled byte offset of (row tb + i, column ch)
             const uint32_t xl = static_cast<uint32_t>(lane) >> 2;
             const uint32_t rowbase = 1024u * warp + 4u * (lane & 3);
             uint8_t *g1a = base + OFF_G1A, *g1b = base + OFF_G1B, *r0t = base + OFF_R0;
-            float dmax = 0.f;  // max |G - Gm| over this warp's tokens
-            uint32_t cb[4][2][4];  // channel-major operands [Bhat, Khat, A0, V][channel][pair]
-            float prv[4][2];
+            bool in_range = true;  // every 2^(G_t - Gm) of this warp's tokens within 2^+-120
+            uint32_t cb[4][2][4];  // channel-major operands [Bhat, Khat, A0, V][channel][token pair]
+            uint32_t prv[4];
 #pragma unroll
             for (int ii = 0; ii < 8; ++ii) {
-                G0 += lg2_approx(bf16_lo(gw[ii]));
-                G1 += lg2_approx(bf16_hi(gw[ii]));
-                // padding tokens have w = 1 and leave G unchanged
-                dmax = fmaxf(dmax, fmaxf(fabsf(G0 - Gm0), fabsf(G1 - Gm1)));
-                const float ec0 = ex2_approx(G0 - Gm0), ec1 = ex2_approx(G1 - Gm1);
-                const float iv0 = ex2_approx(Gm0 - G0), iv1 = ex2_approx(Gm1 - G1);
-                const float dc0 = ec0 * eGm0, dc1 = ec1 * eGm1;
-                const float dl0 = EL0 * iv0, dl1 = EL1 * iv1;
-                const float ax = bf16_lo(ga[ii]), ay = bf16_hi(ga[ii]);
-                const float bx = bf16_lo(gb[ii]), by = bf16_hi(gb[ii]);
-                const float kx = bf16_lo(gk[ii]), ky = bf16_hi(gk[ii]);
-                const float rx = bf16_lo(gr[ii]), ry = bf16_hi(gr[ii]);
-                const float vx = bf16_lo(gv[ii]), vy = bf16_hi(gv[ii]);
+                e0 *= bf16_lo(in_w[ii]);  // padding tokens have w = 1
+                e1 *= bf16_hi(in_w[ii]);
+                in_range = in_range && e0 >= kMinDecayRel && e0 <= kMaxDecayRel &&
+                           e1 >= kMinDecayRel && e1 <= kMaxDecayRel;  // false for NaN too
+                const float iv0 = rcp_approx(e0), iv1 = rcp_approx(e1);
+                const uint32_t ec2 = pack_bf16(e0, e1);                  // 2^(G_t - Gm)
+                const uint32_t iv2 = pack_bf16(iv0, iv1);                // 2^(Gm - G_t)
+                const uint32_t dc2 = pack_bf16(e0 * eGm0, e1 * eGm1);    // D(0, t]
+                const uint32_t dl2 = pack_bf16(EL0 * iv0, EL1 * iv1);    // D(t, L]
                 const uint32_t off = rowbase + ii * 128 + ((xl ^ ii) << 4);
-                *reinterpret_cast<uint32_t *>(g1a + off) = pack_bf16(bx * iv0, by * iv1);
-                *reinterpret_cast<uint32_t *>(g1a + 8192 + off) = pack_bf16(kx * iv0, ky * iv1);
-                *reinterpret_cast<uint32_t *>(g1b + off) = pack_bf16(ax * ep0, ay * ep1);
-                *reinterpret_cast<uint32_t *>(g1b + 8192 + off) = pack_bf16(rx * ec0, ry * ec1);
-                *reinterpret_cast<uint32_t *>(r0t + off) = pack_bf16(rx * dc0, ry * dc1);
-                const float cv[4][2] = {{bx * dl0, by * dl1}, {kx * dl0, ky * dl1},
-                                        {ax * dp0, ay * dp1}, {vx, vy}};
+                *reinterpret_cast<uint32_t *>(g1a + off) = bmul2(in_b[ii], iv2);
+                *reinterpret_cast<uint32_t *>(g1a + 8192 + off) = bmul2(in_k[ii], iv2);
+                *reinterpret_cast<uint32_t *>(g1b + off) = bmul2(in_a[ii], ep2);
+                *reinterpret_cast<uint32_t *>(g1b + 8192 + off) = bmul2(in_r[ii], ec2);
+                *reinterpret_cast<uint32_t *>(r0t + off) = bmul2(in_r[ii], dc2);
+                const uint32_t cur[4] = {bmul2(in_b[ii], dl2), bmul2(in_k[ii], dl2),
+                                         bmul2(in_a[ii], dp2), in_v[ii]};
 #pragma unroll
-                for (int o = 0; o < 4; ++o)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        if ((ii & 1) == 0)
-                            prv[o][e] = cv[o][e];
-                        else
-                            cb[o][e][ii >> 1] = pack_bf16(prv[o][e], cv[o][e]);
+                for (int o = 0; o < 4; ++o) {
+                    if ((ii & 1) == 0) {
+                        prv[o] = cur[o];
+                    } else {  // tokens (ii-1, ii) of channel ch, then of channel ch+1
+                        cb[o][0][ii >> 1] = __byte_perm(prv[o], cur[o], 0x5410);
+                        cb[o][1][ii >> 1] = __byte_perm(prv[o], cur[o], 0x7632);
                     }
-                ep0 = ec0; ep1 = ec1;
-                dp0 = dc0; dp1 = dc1;
+                }
+                ep2 = ec2;
+                dp2 = dc2;
             }
-            if (!(dmax <= kMaxLog2Range) || G0 != G0 || G1 != G1) range_bad = true;  // NaN too
+            if (!in_range) range_bad = true;
             uint8_t *dst[4] = {base + OFF_G2A, base + OFF_KHT, base + OFF_G34B, base + OFF_V};
 #pragma unroll
             for (int o = 0; o < 4; ++o)
@@ -762,6 +785,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         mma_wait(bar_mma, ph_mma, flag);
         ph_mma ^= 1;
+        if (tid == 0 && !last) stage_inputs(0, 1, tc0 + kL, true);  // G2A is dead: r, w
         tc_fence_after();
         {
             float v[32];
@@ -783,6 +807,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         mma_wait(bar_mma, ph_mma, flag);
         ph_mma ^= 1;
+        if (tid == 0 && !last) stage_inputs(2, 3, tc0 + kL, false);  // G34B is dead: k, v
         tc_fence_after();
         {
             float v[32], y[32];
@@ -837,13 +862,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             umma_128xNx64_bmn(tmem + kColG5, smem_addr(base + OFF_OPA2), smem_addr(base + OFF_SHI), 64, true);
             umma_128xNx64_bmn(tmem + kColG5, smem_addr(base + OFF_OPA2), smem_addr(base + OFF_SLO), 64, true);
             umma_commit(bar_mma);
-            if (!last) {  // the staging tiles are dead now: fetch the next chunk's inputs
-                mbar_arrive_expect_tx(bar_tma, 6 * kTile64);
-#pragma unroll
-                for (int x = 0; x < 6; ++x)
-                    tma_load_3d(smem_addr(base + stage_off(x)), &maps.m[x], 0, h, tc0 + kL, bar_tma);
-            }
         }
+        if (tid == 0 && !last) stage_inputs(4, 5, tc0 + kL, false);  // KHT, R0 are dead: a, b
         mma_wait(bar_mma, ph_mma, flag);
         ph_mma ^= 1;
         tc_fence_after();
@@ -851,7 +871,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         prev_tc0 = tc0;
         prev_Lc = Lc;
         // The readback of this product waits for the next chunk's first MMA (or the loop end);
-        // R1 and the staging tiles are free for the next chunk's elementwise phase now.
+        // R1 and the operand tiles are free for the next chunk's elementwise phase now.
     }
     __syncthreads();  // every thread sees the same abort flag
     if (!*flag) {
@@ -862,7 +882,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (*flag) {  // a wait gave up: give in-flight MMAs a last chance, then leave
         if (tid == 0) flag_status(p.lv.status, WKV7_DEV_WAIT_TIMEOUT);
         mbar_wait_bounded(bar_mma, ph_mma, kWaitCycles);
-        mbar_wait_bounded(bar_tma, ph_tma, kWaitCycles);
+        mbar_wait_bounded(bar_in, ph_in, kWaitCycles);
     }
     if (range_bad) flag_status(p.lv.status, WKV7_DEV_DECAY_RANGE);
     tc_fence_before();
