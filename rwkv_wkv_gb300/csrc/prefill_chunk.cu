@@ -33,11 +33,12 @@
 //       2^(half-chunk decay); factors that meet S0 are relative to the start.
 //   G1  [Bbar;Kbar] x Am^T  -> Mab, Mak rows        (M=128, N=64,  K=64)
 //   G1' [Am;Rm] x [Bbar;Kbar]^T -> Qb^T, Qk^T rows  (M=128, N=128, K=64)
-//   T   (I - Mab)^-1 in fp32 on the CUDA cores, by 16x16 blocks: the four
-//       diagonal blocks T_ii = (I - M_ii)^-1 by back substitution (two warps,
-//       while the other warps read the rest of G1 back), then N_ij = T_ii M_ij
-//       and the off-diagonal blocks from products of pairs of those blocks
-//       (three barrier steps); T goes to shared memory in bf16
+//   T   (I - Mab)^-1 by 16x16 blocks: the four diagonal blocks
+//       T_ii = (I - M_ii)^-1 in fp32 by back substitution (two warps, while the
+//       other warps read the rest of G1 back), then N_ij = T_ii M_ij and the
+//       off-diagonal blocks from products of pairs of those blocks (three
+//       steps of warp-level TF32 block products); T goes to shared memory in
+//       bf16
 //   G2  [Bhat^T; Qb^T] x T^T -> Z^T                  (M=128, N=64)
 //   G34 Z^T x [A0^T; Mak]^T -> Phi'^T, R''^T, Y'^T   (M=128, N=128)
 //   G5  [Y_Q^T; Y_B^T] x V -> O0^T, Psi^T; then += [R'^T; Phi^T] x S0^T with
@@ -179,6 +180,64 @@ __device__ __forceinline__ void load_row16(const uint8_t *tile, int row, int col
         v[8 * q + 2] = bf16_lo(u.y); v[8 * q + 3] = bf16_hi(u.y);
         v[8 * q + 4] = bf16_lo(u.z); v[8 * q + 5] = bf16_hi(u.z);
         v[8 * q + 6] = bf16_lo(u.w); v[8 * q + 7] = bf16_hi(u.w);
+    }
+}
+
+// ------------------------------------------- 16x16 fp32 block products (TF32)
+// Warp-level D (+)= A B for 16x16 fp32 blocks in shared memory (row pitch
+// kSlotRow floats), on the tensor cores with TF32 operands (rounded to nearest)
+// and fp32 accumulation: two K=8 steps x two 8-column halves of
+// mma.sync.m16n8k8.  Fragment layout of m16n8k8 (g = lane / 4, q = lane % 4):
+// A a0 (g, q), a1 (g+8, q), a2 (g, q+4), a3 (g+8, q+4); B b0 (q, g), b1 (q+4, g);
+// C/D c0 (g, 2q), c1 (g, 2q+1), c2 (g+8, 2q), c3 (g+8, 2q+1) -- per 8-column half.
+__device__ __forceinline__ uint32_t tf32_rn(float x) {
+    uint32_t y;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ void mma_tf32_m16n8k8(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                                 uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// acc[h] (8-column half h of the 16x16 result, C-fragment layout) += A B.
+__device__ __forceinline__ void block_mma_acc(const float *A, const float *B, float (&acc)[2][4],
+                                              int lane) {
+    const int g = lane >> 2, q = lane & 3;
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+        const uint32_t a[4] = {tf32_rn(A[g * 20 + 8 * kk + q]), tf32_rn(A[(g + 8) * 20 + 8 * kk + q]),
+                               tf32_rn(A[g * 20 + 8 * kk + q + 4]),
+                               tf32_rn(A[(g + 8) * 20 + 8 * kk + q + 4])};
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+            mma_tf32_m16n8k8(acc[h], a, tf32_rn(B[(8 * kk + q) * 20 + 8 * h + g]),
+                             tf32_rn(B[(8 * kk + q + 4) * 20 + 8 * h + g]));
+    }
+}
+
+// Load a 16x16 block into the C-fragment layout (or zero it).
+__device__ __forceinline__ void block_frag_load(const float *C, float (&acc)[2][4], int lane) {
+    const int g = lane >> 2, q = lane & 3;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const float2 x0 = *reinterpret_cast<const float2 *>(C + g * 20 + 8 * h + 2 * q);
+        const float2 x1 = *reinterpret_cast<const float2 *>(C + (g + 8) * 20 + 8 * h + 2 * q);
+        acc[h][0] = x0.x; acc[h][1] = x0.y; acc[h][2] = x1.x; acc[h][3] = x1.y;
+    }
+}
+
+__device__ __forceinline__ void block_frag_store(float *D, const float (&acc)[2][4], int lane) {
+    const int g = lane >> 2, q = lane & 3;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        *reinterpret_cast<float2 *>(D + g * 20 + 8 * h + 2 * q) = make_float2(acc[h][0], acc[h][1]);
+        *reinterpret_cast<float2 *>(D + (g + 8) * 20 + 8 * h + 2 * q) = make_float2(acc[h][2], acc[h][3]);
     }
 }
 
@@ -650,129 +709,66 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (*flag) break;
 
         // ------------------------------------------------ T = (I - Mab)^-1
-        // Off-diagonal 16x16 blocks in fp32 on the CUDA cores.  With N_ij = T_ii M_ij
-        // (i < j), T_ij = sum_{i<k<=j} N_ik T_kj; grouping the products in pairs,
+        // Off-diagonal 16x16 blocks, one warp-level TF32 block product each, in
+        // three steps over warps 0-5.  With N_ij = T_ii M_ij (i < j),
+        // T_ij = sum_{i<k<=j} N_ik T_kj; grouping the products in pairs,
         //   T_i,i+1 = N_i,i+1 T_i+1,i+1,  T_02 = R_02 T_22,  T_13 = R_13 T_33,
         //   T_03 = R_02 T_23 + R_03 T_33,
-        // R_02 = N_02 + N_01 N_12, R_03 = N_03 + N_01 N_13, R_13 = N_13 + N_12 N_23:
-        // three steps after the diagonal blocks.
-        if (tid < 192) {  // N_ij: row r, 8 columns
-            const int r = tid & 15, k = tid >> 4;  // k: 0-5 row block 0, 6-9 block 1, 10-11 block 2
-            const int i = k < 6 ? 0 : (k < 10 ? 1 : 2);
-            const int kk = k - (i == 0 ? 0 : (i == 1 ? 6 : 10));
-            const int j = i + 1 + (kk >> 1), c0 = 8 * (kk & 1);
-            const float *trow = blk(i) + r * kSlotRow;
-            const float *m = blk(kSlotM + up_idx(i, j)) + c0;
-            float t[16], acc[8];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float4 y = reinterpret_cast<const float4 *>(trow)[q];
-                t[4 * q] = y.x; t[4 * q + 1] = y.y; t[4 * q + 2] = y.z; t[4 * q + 3] = y.w;
+        // R_02 = N_02 + N_01 N_12, R_03 = N_03 + N_01 N_13, R_13 = N_13 + N_12 N_23.
+        if (warp < 6) {
+            // step 1: N_ij for the six pairs (i, j), i < j, one per warp
+            const int i = warp < 3 ? 0 : (warp < 5 ? 1 : 2);
+            const int j = warp < 3 ? warp + 1 : (warp < 5 ? warp - 1 : 3);
+            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            block_mma_acc(blk(i), blk(kSlotM + up_idx(i, j)), acc, lane);
+            block_frag_store(blk(kSlotN + up_idx(i, j)), acc, lane);
+            bar_sync_named(2, 192);
+            // step 2: T_01, T_12, T_23 (also kept in fp32), R_02, R_03, R_13 (over the dead M_ij)
+            float acc2[2][4];
+            const int g = lane >> 2, q = lane & 3;
+            if (warp < 3) {
+                for (int h = 0; h < 2; ++h)
+                    for (int e = 0; e < 4; ++e) acc2[h][e] = 0.f;
+                block_mma_acc(blk(kSlotN + up_idx(warp, warp + 1)), blk(warp + 1), acc2, lane);
+                if (warp == 2) block_frag_store(blk(kSlotM + kSlotT23), acc2, lane);
+            } else {  // R_02 = N_02 + N_01 N_12, R_03 = N_03 + N_01 N_13, R_13 = N_13 + N_12 N_23
+                const int c0 = warp == 3 ? up_idx(0, 2) : warp == 4 ? up_idx(0, 3) : up_idx(1, 3);
+                const int fa = warp == 5 ? up_idx(1, 2) : up_idx(0, 1);
+                const int fb = warp == 3 ? up_idx(1, 2) : warp == 4 ? up_idx(1, 3) : up_idx(2, 3);
+                block_frag_load(blk(kSlotN + c0), acc2, lane);
+                block_mma_acc(blk(kSlotN + fa), blk(kSlotN + fb), acc2, lane);
+                block_frag_store(blk(kSlotM + (warp == 3 ? kSlotR02 : warp == 4 ? kSlotR03 : kSlotR13)), acc2, lane);
             }
+            if (warp < 3) {  // T_i,i+1 -> bf16 T (rows 16i + g, +8; columns 16(i+1) + 8h + 2q)
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const float4 m0 = reinterpret_cast<const float4 *>(m + u * kSlotRow)[0];
-                const float4 m1 = reinterpret_cast<const float4 *>(m + u * kSlotRow)[1];
-                acc[0] = fmaf(t[u], m0.x, acc[0]); acc[1] = fmaf(t[u], m0.y, acc[1]);
-                acc[2] = fmaf(t[u], m0.z, acc[2]); acc[3] = fmaf(t[u], m0.w, acc[3]);
-                acc[4] = fmaf(t[u], m1.x, acc[4]); acc[5] = fmaf(t[u], m1.y, acc[5]);
-                acc[6] = fmaf(t[u], m1.z, acc[6]); acc[7] = fmaf(t[u], m1.w, acc[7]);
-            }
-            float *dst = blk(kSlotN + up_idx(i, j)) + r * kSlotRow + c0;
-            reinterpret_cast<float4 *>(dst)[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-            reinterpret_cast<float4 *>(dst)[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-        }
-        __syncthreads();
-        if (tid < 192) {
-            // Pair products (one per warp), row r, 8 columns:
-            //   T_01 = N_01 T_11, T_12 = N_12 T_22, T_23 = N_23 T_33,
-            //   R_02 = N_02 + N_01 N_12, R_03 = N_03 + N_01 N_13, R_13 = N_13 + N_12 N_23
-            const int pw = tid >> 5, r = tid & 15, c0 = 8 * ((tid >> 4) & 1);
-            const int ia = pw == 0 ? kSlotN + up_idx(0, 1) : pw == 1 ? kSlotN + up_idx(1, 2)
-                         : pw == 2 ? kSlotN + up_idx(2, 3) : pw == 5 ? kSlotN + up_idx(1, 2)
-                                                                    : kSlotN + up_idx(0, 1);
-            const int ib = pw == 0 ? 1 : pw == 1 ? 2 : pw == 2 ? 3 : pw == 3 ? kSlotN + up_idx(1, 2)
-                         : pw == 4 ? kSlotN + up_idx(1, 3) : kSlotN + up_idx(2, 3);
-            const float *arow = blk(ia) + r * kSlotRow;
-            const float *bcol = blk(ib) + c0;
-            float av[16], acc[8];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float4 y = reinterpret_cast<const float4 *>(arow)[q];
-                av[4 * q] = y.x; av[4 * q + 1] = y.y; av[4 * q + 2] = y.z; av[4 * q + 3] = y.w;
-            }
-            if (pw >= 3) {  // R_0j / R_13 start from N_02, N_03, N_13
-                const int ic = kSlotN + (pw == 3 ? up_idx(0, 2) : pw == 4 ? up_idx(0, 3) : up_idx(1, 3));
-                const float4 y0 = reinterpret_cast<const float4 *>(blk(ic) + r * kSlotRow + c0)[0];
-                const float4 y1 = reinterpret_cast<const float4 *>(blk(ic) + r * kSlotRow + c0)[1];
-                acc[0] = y0.x; acc[1] = y0.y; acc[2] = y0.z; acc[3] = y0.w;
-                acc[4] = y1.x; acc[5] = y1.y; acc[6] = y1.z; acc[7] = y1.w;
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-            }
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const float4 m0 = reinterpret_cast<const float4 *>(bcol + u * kSlotRow)[0];
-                const float4 m1 = reinterpret_cast<const float4 *>(bcol + u * kSlotRow)[1];
-                acc[0] = fmaf(av[u], m0.x, acc[0]); acc[1] = fmaf(av[u], m0.y, acc[1]);
-                acc[2] = fmaf(av[u], m0.z, acc[2]); acc[3] = fmaf(av[u], m0.w, acc[3]);
-                acc[4] = fmaf(av[u], m1.x, acc[4]); acc[5] = fmaf(av[u], m1.y, acc[5]);
-                acc[6] = fmaf(av[u], m1.z, acc[6]); acc[7] = fmaf(av[u], m1.w, acc[7]);
-            }
-            if (pw >= 2) {  // kept in fp32 for the last step (over the dead M_ij blocks)
-                float *dst = blk(kSlotM + pw - 2) + r * kSlotRow + c0;
-                reinterpret_cast<float4 *>(dst)[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-                reinterpret_cast<float4 *>(dst)[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-            }
-            if (pw < 3)  // T_i,i+1 -> bf16 T
-                *reinterpret_cast<uint4 *>(base + OFF_WT + sw128_off(16 * pw + r, 16 * (pw + 1) + c0)) =
-                    make_uint4(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]),
-                               pack_bf16(acc[4], acc[5]), pack_bf16(acc[6], acc[7]));
-        }
-        __syncthreads();
-        if (tid < 128) {  // T_02 = R_02 T_22, T_13 = R_13 T_33: row r, 4 columns
-            const int r = tid & 15, b = tid >> 6, c0 = 4 * ((tid >> 4) & 3);
-            const float *arow = blk(kSlotM + (b == 0 ? kSlotR02 : kSlotR13)) + r * kSlotRow;
-            const float *bcol = blk(2 + b) + c0;
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float4 y = reinterpret_cast<const float4 *>(arow)[q];
-                const float yv[4] = {y.x, y.y, y.z, y.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float4 x = *reinterpret_cast<const float4 *>(bcol + (4 * q + e) * kSlotRow);
-                    acc[0] = fmaf(yv[e], x.x, acc[0]); acc[1] = fmaf(yv[e], x.y, acc[1]);
-                    acc[2] = fmaf(yv[e], x.z, acc[2]); acc[3] = fmaf(yv[e], x.w, acc[3]);
+                for (int h = 0; h < 2; ++h) {
+                    *reinterpret_cast<uint32_t *>(base + OFF_WT + sw128_off(16 * warp + g, 16 * (warp + 1) + 8 * h + 2 * q)) =
+                        pack_bf16(acc2[h][0], acc2[h][1]);
+                    *reinterpret_cast<uint32_t *>(base + OFF_WT + sw128_off(16 * warp + g + 8, 16 * (warp + 1) + 8 * h + 2 * q)) =
+                        pack_bf16(acc2[h][2], acc2[h][3]);
                 }
             }
-            *reinterpret_cast<uint2 *>(base + OFF_WT + sw128_off(16 * b + r, 16 * (b + 2) + c0)) =
-                make_uint2(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]));
-        } else {  // T_03 = R_02 T_23 + R_03 T_33: row r, 2 columns
-            const int r = tid & 15, c0 = 2 * ((tid - 128) >> 4);
-            const float *a1 = blk(kSlotM + kSlotR02) + r * kSlotRow;
-            const float *a2 = blk(kSlotM + kSlotR03) + r * kSlotRow;
-            const float *b1 = blk(kSlotM + kSlotT23) + c0;
-            const float *b2 = blk(3) + c0;
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            bar_sync_named(2, 192);
+            // step 3: T_02 = R_02 T_22, T_13 = R_13 T_33, T_03 = R_02 T_23 + R_03 T_33
+            if (warp < 3) {
+                float acc3[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                if (warp == 0) {
+                    block_mma_acc(blk(kSlotM + kSlotR02), blk(2), acc3, lane);
+                } else if (warp == 1) {
+                    block_mma_acc(blk(kSlotM + kSlotR13), blk(3), acc3, lane);
+                } else {
+                    block_mma_acc(blk(kSlotM + kSlotR02), blk(kSlotM + kSlotT23), acc3, lane);
+                    block_mma_acc(blk(kSlotM + kSlotR03), blk(3), acc3, lane);
+                }
+                const int bi = warp == 1 ? 1 : 0, bj = warp == 0 ? 2 : 3;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float4 y1 = reinterpret_cast<const float4 *>(a1)[q];
-                const float4 y2 = reinterpret_cast<const float4 *>(a2)[q];
-                const float v1[4] = {y1.x, y1.y, y1.z, y1.w}, v2[4] = {y2.x, y2.y, y2.z, y2.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 x1 = *reinterpret_cast<const float2 *>(b1 + (4 * q + e) * kSlotRow);
-                    const float2 x2 = *reinterpret_cast<const float2 *>(b2 + (4 * q + e) * kSlotRow);
-                    acc[0] = fmaf(v1[e], x1.x, acc[0]); acc[1] = fmaf(v1[e], x1.y, acc[1]);
-                    acc[2] = fmaf(v2[e], x2.x, acc[2]); acc[3] = fmaf(v2[e], x2.y, acc[3]);
+                for (int h = 0; h < 2; ++h) {
+                    *reinterpret_cast<uint32_t *>(base + OFF_WT + sw128_off(16 * bi + g, 16 * bj + 8 * h + 2 * q)) =
+                        pack_bf16(acc3[h][0], acc3[h][1]);
+                    *reinterpret_cast<uint32_t *>(base + OFF_WT + sw128_off(16 * bi + g + 8, 16 * bj + 8 * h + 2 * q)) =
+                        pack_bf16(acc3[h][2], acc3[h][3]);
                 }
             }
-            *reinterpret_cast<uint32_t *>(base + OFF_WT + sw128_off(r, 48 + c0)) =
-                pack_bf16(acc[0] + acc[2], acc[1] + acc[3]);
         }
         fence_proxy_async_smem();
         __syncthreads();
