@@ -21,30 +21,32 @@
 // of shared memory and 256 tensor-memory columns each), so one CTA's MMA
 // waits and load latencies are covered by the other's CUDA-core phases.
 // Per chunk:
-//   E   bf16 inputs, TMA-loaded into shared memory in three pairs as tiles of
-//       the previous chunk go dead (and prefetched into L2 a chunk before
-//       that) ->
-//       log2-decay prefix sums (one warp per 8 tokens, two channels per lane)
-//       -> operands scaled in packed bf16 pairs, stored to 128-byte swizzled
-//       K-major tiles.
+//   E   bf16 inputs, TMA-loaded into shared memory as soon as the previous
+//       chunk's G2 completes (early enough that an L2 prefetch would only
+//       compete with the loads for the TMA unit) -> log2-decay prefix sums (one
+//       warp per 8 tokens, two channels per lane) -> operands scaled in packed
+//       bf16 pairs, stored to 128-byte swizzled tiles.  Decays inside the Gram
+//       products are taken relative to the chunk midpoint (token 31), so no
+//       factor exceeds 2^(half-chunk decay); factors that meet S0 are relative
+//       to the start.
 // Tensor-memory readbacks give warps w and w+4 the same 32 lanes (rows) and
-// split the columns between them.  Decays inside the Gram products are taken
-//       relative to the chunk midpoint (token 31), so no factor exceeds
-//       2^(half-chunk decay); factors that meet S0 are relative to the start.
-//   G1  [Bbar;Kbar] x Am^T  -> Mab, Mak rows        (M=128, N=64,  K=64)
-//   G1' [Am;Rm] x [Bbar;Kbar]^T -> Qb^T, Qk^T rows  (M=128, N=128, K=64)
+// split the columns between them.
+//   G1  [Bbar;Kbar] x Am^T -> Mab rows s              (M=128, N=64, K=64)
+//   G1' [Am;Rm] x [Bbar;Kbar]^T -> rows t: Mak^T; rows t': Qb^T, Qk^T
+//                                                    (M=128, N=128, K=64)
 //   T   (I - Mab)^-1 by 16x16 blocks: the four diagonal blocks
-//       T_ii = (I - M_ii)^-1 in fp32 by back substitution (two warps, while the
-//       other warps read the rest of G1 back), then N_ij = T_ii M_ij and the
-//       off-diagonal blocks from products of pairs of those blocks (three
-//       steps of warp-level TF32 block products); T goes to shared memory in
-//       bf16
+//       T_ii = (I - M_ii)^-1 in fp32 by back substitution (two warps), then
+//       N_ij = T_ii M_ij and the off-diagonal blocks from products of pairs of
+//       those blocks (three steps of warp-level TF32 block products); T goes
+//       to shared memory in bf16
 //   G2  [Bhat^T; Qb^T] x T^T -> Z^T                  (M=128, N=64)
-//   G34 Z^T x [A0^T; Mak]^T -> Phi'^T, R''^T, Y'^T   (M=128, N=128)
-//   G5  [Y_Q^T; Y_B^T] x V -> O0^T, Psi^T; then += [R'^T; Phi^T] x S0^T with
-//       S0 split into bf16 hi + lo (two MMAs, B = S0^T rows read MN-major,
-//       so the accumulator's S_L^T rows are written back as they come)
-//                                                    (M=128, N=64)
+//   G34 Z^T (in tensor memory) x [A0 | Mak^T] (MN-major) -> Phi'^T, R''^T, Y'^T
+//                                                    (M=128, N=128)
+//   G5  [Phi^T; R'^T] x (S0_hi + S0_lo)^T + [Y_B^T; Y_Q^T] x V -> [S_L^T; O^T],
+//       both A operands in tensor memory, S0 split into bf16 hi + lo (B read
+//       MN-major)                                    (M=128, N=64)
+// The A operands of G34 and G5 go from the readback registers straight back
+// into tensor memory as bf16; they never touch shared memory.
 // Accumulators live in tensor memory (256 columns); the float32 state leaves
 // the accumulator each chunk, is written back as the next chunk's bf16 hi/lo
 // operand pair and, after the last chunk, to the slot in float32.
@@ -92,11 +94,10 @@ constexpr int kSlotT23 = 0, kSlotR02 = 1, kSlotR03 = 2, kSlotR13 = 3;  // from k
 constexpr uint32_t OFF_WT = OFF_R1 + 3 * kTile64;   // T in bf16 (rows s, K = t)
 static_assert(16 * kSlotBytes <= OFF_WT - OFF_R1, "inverse blocks overlap T");
 constexpr uint32_t OFF_G2B = OFF_WT;
-constexpr uint32_t OFF_OPZ = OFF_R1;
-constexpr uint32_t OFF_OPY = OFF_R1;
-constexpr uint32_t OFF_OPA2 = OFF_R1 + kTile128;
 constexpr uint32_t OFF_G2A = OFF_R1 + 2 * kTile128;  // [Bhat^T; Qb^T]
-constexpr uint32_t OFF_G34B = OFF_G2A + kTile128;    // [A0^T; Mak]
+constexpr uint32_t OFF_G34B = OFF_G2A + kTile128;    // B of G34, MN-major: [A0 | Mak^T] (rows u)
+constexpr uint32_t OFF_A0 = OFF_G34B;                // A0 (rows u, 64 key channels j')
+constexpr uint32_t OFF_MAKT = OFF_G34B + kTile64;    // Mak^T (rows u, 64 tokens s)
 constexpr uint32_t OFF_V = OFF_G34B + kTile128;      // V^T (rows i, K = s)
 constexpr uint32_t OFF_KHT = OFF_V + kTile64;        // Khat^T (rows j, K = s)
 constexpr uint32_t OFF_R0 = OFF_KHT + kTile64;       // R0 (rows t, K = j)
@@ -104,23 +105,26 @@ constexpr uint32_t OFF_SHI = OFF_R0 + kTile64;       // S0^T hi (rows j, 64 valu
 constexpr uint32_t OFF_SLO = OFF_SHI + kTile64;      // S0^T lo
 constexpr uint32_t kTileBytes = OFF_SLO + kTile64;
 // Staging of the next chunk's six inputs ([64 tokens][64 channels] bf16, 8 KB
-// each), TMA-loaded into tiles as they go dead during the current chunk: r, w
-// after G2 (G2A), k, v after G34 (G34B), a, b after the G34 readback (KHT,
-// R0).  All six complete one phase of the input barrier.  The elementwise
-// phase reads them all before its first barrier and writes these tiles only
-// after it.
+// each), TMA-loaded as soon as G2 completes: from then on the current chunk
+// needs neither G2A nor region R1 (G34 and G5 take their A operands from
+// tensor memory).  r, w go to G2A, k, v, a, b to R1.  The elementwise phase
+// reads them all before its first barrier and writes these tiles only after
+// it.
 __host__ __device__ constexpr uint32_t stage_off(int x) {  // r, w, k, v, a, b
-    return x == 0 ? OFF_G2A : x == 1 ? OFF_G2A + kTile64 : x == 2 ? OFF_G34B
-         : x == 3 ? OFF_G34B + kTile64 : x == 4 ? OFF_KHT : OFF_R0;
+    return x < 2 ? OFF_G2A + x * kTile64 : OFF_R1 + (x - 2) * kTile64;
 }
 // Index of the strictly-upper 16x16 block (i, j), i < j < 4, in 0..5.
 __device__ __forceinline__ int up_idx(int i, int j) { return i * (7 - i) / 2 + (j - i - 1); }
 constexpr uint32_t kSmemBytes = kSmallBytes + 1024 + kTileBytes;  // + worst-case alignment
 static_assert(2 * (kSmemBytes + 1024) <= 228 * 1024, "two CTAs per SM");
 constexpr uint32_t kTmemCols = 256;
-// Tensor-memory columns: G1 0-63, G1' 128-255 (Q_k^T at 192-255 until the G34 readback),
-// G2 0-63, G34 0-127, G5 64-127 (its readback overlaps the next chunk's G1).
-constexpr uint32_t kColG5 = 64;
+// Tensor-memory columns: G1 64-127 and G1' 128-255 (Q_k^T at 192-255 until the
+// G34 readback); G2 0-63; Z^T, the bf16 A operand of G34, 128-159; G34 0-127;
+// the bf16 A operands of G5, [Phi^T; R'^T] 128-159 and Y^T 160-191; G5 0-63,
+// read back while the next chunk's G1 and G1' run.
+// A bf16 A operand in tensor memory holds row m in lane m with K elements 2c,
+// 2c+1 packed in column c.
+constexpr uint32_t kColG1 = 64, kColG1p = 128, kColZA = 128, kColA2 = 128, kColYA = 160, kColQk = 192;
 
 struct InputMaps {
     CUtensorMap m[6];  // r, w, k, v, a, b
@@ -419,16 +423,16 @@ __global__ void __launch_bounds__(kThreads, 2)
     bool range_bad = false;
     int prev_c = 0, prev_tc0 = 0, prev_Lc = 0;  // chunk whose state product awaits its readback
 
-    // Readback of the state product [O^T; S_L^T] (tensor-memory columns kColG5..+63):
-    // O rows to the output, S_L^T rows to the bf16 hi/lo operand tiles of the next
-    // chunk, after the last chunk the float32 state to the slot, and after a full
-    // chunk the float32 state to its checkpoint snapshot when checkpoints are asked for.
+    // Readback of the state product [S_L^T; O^T] (tensor-memory columns 0-63): O rows to the output, S_L^T rows to the bf16 hi/lo
+    // operand tiles of the next chunk, after the last chunk the float32 state to
+    // the slot, and after a full chunk the float32 state to its checkpoint
+    // snapshot when checkpoints are asked for.
     auto readback_state_product = [&](int occ, int otc0, int oLc, bool final) {
         float v[32];
-        tmem_ld32(tmem + lane_base + kColG5 + cpart, v);
+        tmem_ld32(tmem + lane_base + cpart, v);
         tmem_ld_wait();
-        if (row < 64) {  // O row t' -> o[otc0 + t'][h][cpart ..]
-            const int tq = row;
+        if (row >= 64) {  // O row t' -> o[otc0 + t'][h][cpart ..]
+            const int tq = row - 64;
             float *dst = p.in.o + (static_cast<size_t>(otc0 + tq) * H + h) * kHeadSize + cpart;
             if (tq < oLc) {
 #pragma unroll
@@ -437,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                         make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
             }
         } else {  // S_L^T row j (values i of this thread's part)
-            const int j = row - 64;
+            const int j = row;
             if (p.ck.cu_ckpt && oLc == kL) {  // the state at token 64 (occ + 1) of the sequence
                 const int id = __ldg(p.ck.ckpt_ids + ck0 + occ);
                 if (id >= 0 && id < p.ck.n_snaps) {
@@ -534,8 +538,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             const uint32_t rowbase = 1024u * warp + 4u * (lane & 3);
             uint8_t *g1a = base + OFF_G1A, *g1b = base + OFF_G1B, *r0t = base + OFF_R0;
             bool in_range = true;  // every 2^(G_t - Gm) of this warp's tokens within 2^+-120
-            uint32_t cb[4][2][4];  // channel-major operands [Bhat, Khat, A0, V][channel][token pair]
-            uint32_t prv[4];
+            uint32_t cb[3][2][4];  // channel-major operands [Bhat, Khat, V][channel][token pair]
+            uint32_t prv[3];
 #pragma unroll
             for (int ii = 0; ii < 8; ++ii) {
                 e0 *= bf16_lo(in_w[ii]);  // padding tokens have w = 1
@@ -553,10 +557,10 @@ __global__ void __launch_bounds__(kThreads, 2)
                 *reinterpret_cast<uint32_t *>(g1b + off) = bmul2(in_a[ii], ep2);
                 *reinterpret_cast<uint32_t *>(g1b + 8192 + off) = bmul2(in_r[ii], ec2);
                 *reinterpret_cast<uint32_t *>(r0t + off) = bmul2(in_r[ii], dc2);
-                const uint32_t cur[4] = {bmul2(in_b[ii], dl2), bmul2(in_k[ii], dl2),
-                                         bmul2(in_a[ii], dp2), in_v[ii]};
+                *reinterpret_cast<uint32_t *>(base + OFF_A0 + off) = bmul2(in_a[ii], dp2);
+                const uint32_t cur[3] = {bmul2(in_b[ii], dl2), bmul2(in_k[ii], dl2), in_v[ii]};
 #pragma unroll
-                for (int o = 0; o < 4; ++o) {
+                for (int o = 0; o < 3; ++o) {
                     if ((ii & 1) == 0) {
                         prv[o] = cur[o];
                     } else {  // tokens (ii-1, ii) of channel ch, then of channel ch+1
@@ -568,9 +572,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                 dp2 = dc2;
             }
             if (!in_range) range_bad = true;
-            uint8_t *dst[4] = {base + OFF_G2A, base + OFF_KHT, base + OFF_G34B, base + OFF_V};
+            uint8_t *dst[3] = {base + OFF_G2A, base + OFF_KHT, base + OFF_V};
 #pragma unroll
-            for (int o = 0; o < 4; ++o)
+            for (int o = 0; o < 3; ++o)
 #pragma unroll
                 for (int e = 0; e < 2; ++e)  // 8 tokens of channel-major row ch + e
                     *reinterpret_cast<uint4 *>(dst[o] + sw128_off(ch + e, tb)) =
@@ -582,15 +586,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         // --------------------------------------------------- G1 and G1'
         if (tid == 0) {
             tc_fence_after();
-            umma_128xNx64(tmem + 0, smem_addr(base + OFF_G1A), smem_addr(base + OFF_G1B), 64, false);
-            umma_128xNx64(tmem + 128, smem_addr(base + OFF_G1B), smem_addr(base + OFF_G1A), 128, false);
+            umma_128xNx64(tmem + kColG1, smem_addr(base + OFF_G1A), smem_addr(base + OFF_G1B), 64, false);
+            umma_128xNx64(tmem + kColG1p, smem_addr(base + OFF_G1B), smem_addr(base + OFF_G1A), 128, false);
             umma_commit(bar_mma);
-            if (!last) {  // warm L2 with the next chunk's inputs while the MMAs run
-#pragma unroll
-                for (int x = 0; x < 6; ++x) tma_prefetch_l2_3d(&maps.m[x], 0, h, tc0 + kL);
-            }
         }
-        if (c > 0) {  // the previous chunk's state product, read back while G1 runs
+        if (c > 0) {  // the previous chunk's state product, read back while G1 and G1' run
             tc_fence_after();
             readback_state_product(prev_c, prev_tc0, prev_Lc, false);
         }
@@ -599,9 +599,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         tc_fence_after();
         {
             float v[32];
-            if (row < 64) {  // Mab row s -> fp32 block slots (strictly upper part only)
-                const int s = row, ps = s >> 4, r = s & 15;
-                tmem_ld32(tmem + lane_base + cpart, v);
+            if (row < 64) {  // G1 row s: Mab -> fp32 block slots (strictly upper part);
+                             // then G1' row t: Mak^T (s < t) -> the MN-major half of G34's B
+                const int s0 = row, ps = s0 >> 4, r = s0 & 15;
+                tmem_ld32(tmem + lane_base + kColG1 + cpart, v);
                 tmem_ld_wait();
 #pragma unroll
                 for (int g = 0; g < 2; ++g) {
@@ -614,8 +615,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                             const int c = c00 + 4 * q;
                             const float *x = v + 16 * g + 4 * q;
                             reinterpret_cast<float4 *>(dst)[q] =
-                                make_float4(c > s ? x[0] : 0.f, c + 1 > s ? x[1] : 0.f,
-                                            c + 2 > s ? x[2] : 0.f, c + 3 > s ? x[3] : 0.f);
+                                make_float4(c > s0 ? x[0] : 0.f, c + 1 > s0 ? x[1] : 0.f,
+                                            c + 2 > s0 ? x[2] : 0.f, c + 3 > s0 ? x[3] : 0.f);
                         }
                     }
                 }
@@ -687,21 +688,21 @@ __global__ void __launch_bounds__(kThreads, 2)
                     for (int q = 0; q < 2 * (s2 >> 4); ++q)
                         *reinterpret_cast<uint4 *>(base + OFF_WT + sw128_off(s2, 8 * q)) = z;
                 }
-            } else {  // Mak row s' (keep s > s'), and Qb^T row t' (keep s <= t')
-                const int s = row - 64;
-                float qb[32];
-                tmem_ld32(tmem + lane_base + cpart, v);
-                tmem_ld32(tmem + lane_base + 128 + cpart, qb);
+                // G1' row t: Mak^T (s < t), read after the diagonal blocks are under way
+                tmem_ld32(tmem + lane_base + kColG1p + 64 + cpart, v);
                 tmem_ld_wait();
 #pragma unroll
-                for (int q = 0; q < 32; ++q) {
-                    v[q] = (cpart + q > s) ? v[q] : 0.f;
-                    qb[q] = (cpart + q <= s) ? qb[q] : 0.f;
-                }
-                store_row16(base + OFF_G34B, 64 + s, cpart, v);
-                store_row16(base + OFF_G34B, 64 + s, cpart + 16, v + 16);
-                store_row16(base + OFF_G2A, 64 + s, cpart, qb);
-                store_row16(base + OFF_G2A, 64 + s, cpart + 16, qb + 16);
+                for (int q = 0; q < 32; ++q) v[q] = cpart + q < row ? v[q] : 0.f;
+                store_row16(base + OFF_MAKT, row, cpart, v);
+                store_row16(base + OFF_MAKT, row, cpart + 16, v + 16);
+            } else {  // Qb^T row t' (keep s <= t') -> lower half of G2's A
+                const int tq = row - 64;
+                tmem_ld32(tmem + lane_base + kColG1p + cpart, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int q = 0; q < 32; ++q) v[q] = (cpart + q <= tq) ? v[q] : 0.f;
+                store_row16(base + OFF_G2A, 64 + tq, cpart, v);
+                store_row16(base + OFF_G2A, 64 + tq, cpart + 16, v + 16);
             }
         }
         tc_fence_before();
@@ -781,85 +782,88 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         mma_wait(bar_mma, ph_mma, flag);
         ph_mma ^= 1;
-        if (tid == 0 && !last) stage_inputs(0, 1, tc0 + kL, true);  // G2A is dead: r, w
+        if (tid == 0 && !last) stage_inputs(0, 5, tc0 + kL, true);  // G2A and R1 are dead
         tc_fence_after();
-        {
+        {  // Z^T row (this thread's 32 columns) -> bf16 A operand of G34 in tensor memory
             float v[32];
             tmem_ld32(tmem + lane_base + cpart, v);
             tmem_ld_wait();
-            store_row16(base + OFF_OPZ, row, cpart, v);
-            store_row16(base + OFF_OPZ, row, cpart + 16, v + 16);
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) pk[e] = pack_bf16(v[2 * e], v[2 * e + 1]);
+            tmem_st16(tmem + lane_base + kColZA + cpart / 2, pk);
+            tmem_st_wait();
         }
         tc_fence_before();
-        fence_proxy_async_smem();
         __syncthreads();
         if (*flag) break;
 
         // ------------------------------------------------------------ G34
         if (tid == 0) {
             tc_fence_after();
-            umma_128xNx64(tmem + 0, smem_addr(base + OFF_OPZ), smem_addr(base + OFF_G34B), 128, false);
+            umma_ta_128xNx64(tmem + 0, tmem + kColZA, smem_addr(base + OFF_G34B), 128, false, true);
             umma_commit(bar_mma);
         }
         mma_wait(bar_mma, ph_mma, flag);
         ph_mma ^= 1;
-        if (tid == 0 && !last) stage_inputs(2, 3, tc0 + kL, false);  // G34B is dead: k, v
         tc_fence_after();
-        {
+        {  // -> the bf16 A operands of G5 in tensor memory: [Phi^T; R'^T] and [Y_B^T; Y_Q^T]
             float v[32], y[32];
-            if (row < 64) {  // row j: Phi^T = Phi'^T + diag(gamma); Y_B^T = Y'^T + Khat^T
-                const int j = row;
-                const float gj = gam[j];
-                tmem_ld32(tmem + lane_base + cpart, v);
-                tmem_ld32(tmem + lane_base + 64 + cpart, y);
-                tmem_ld_wait();
+            tmem_ld32(tmem + lane_base + cpart, v);
+            tmem_ld32(tmem + lane_base + 64 + cpart, y);
+            tmem_ld_wait();
+            {
+                uint32_t pa[16];
+                if (row < 64) {  // row j: Phi^T = Phi'^T + diag(gamma)
+                    const float gj = gam[row];
 #pragma unroll
-                for (int q = 0; q < 32; ++q) v[q] += (cpart + q == j) ? gj : 0.f;
-                store_row16(base + OFF_OPA2, 64 + j, cpart, v);
-                store_row16(base + OFF_OPA2, 64 + j, cpart + 16, v + 16);
+                    for (int q = 0; q < 32; ++q) v[q] += (cpart + q == row) ? gj : 0.f;
+                } else {  // row t': R'^T = R''^T + R0
+#pragma unroll
+                    for (int g = 0; g < 2; ++g) {
+                        float add[16];
+                        load_row16(base + OFF_R0, row - 64, cpart + 16 * g, add);
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) v[16 * g + q] += add[q];
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < 16; ++e) pa[e] = pack_bf16(v[2 * e], v[2 * e + 1]);
+                tmem_st16(tmem + lane_base + kColA2 + cpart / 2, pa);
+                tmem_st_wait();
+            }
+            if (row < 64) {  // row j: Y_B^T = Y'^T + Khat^T
 #pragma unroll
                 for (int g = 0; g < 2; ++g) {
                     float add[16];
-                    load_row16(base + OFF_KHT, j, cpart + 16 * g, add);
+                    load_row16(base + OFF_KHT, row, cpart + 16 * g, add);
 #pragma unroll
                     for (int q = 0; q < 16; ++q) y[16 * g + q] += add[q];
-                    store_row16(base + OFF_OPY, 64 + j, cpart + 16 * g, y + 16 * g);
                 }
-            } else {  // row t': R'^T = R''^T + R0; Y_Q^T = Y'^T + Qk^T (causal: s <= t')
-                const int tq = row - 64;
-                tmem_ld32(tmem + lane_base + cpart, v);
-                tmem_ld32(tmem + lane_base + 64 + cpart, y);
+            } else {  // row t': Y_Q^T = Y'^T + Qk^T (causal: s <= t')
+                tmem_ld32(tmem + lane_base + kColQk + cpart, v);
                 tmem_ld_wait();
 #pragma unroll
-                for (int g = 0; g < 2; ++g) {
-                    float add[16];
-                    load_row16(base + OFF_R0, tq, cpart + 16 * g, add);
-#pragma unroll
-                    for (int q = 0; q < 16; ++q) v[16 * g + q] += add[q];
-                    store_row16(base + OFF_OPA2, tq, cpart + 16 * g, v + 16 * g);
-                }
-                tmem_ld32(tmem + lane_base + 192 + cpart, v);  // Qk^T
-                tmem_ld_wait();
-#pragma unroll
-                for (int q = 0; q < 32; ++q) y[q] += (cpart + q <= tq) ? v[q] : 0.f;
-                store_row16(base + OFF_OPY, tq, cpart, y);
-                store_row16(base + OFF_OPY, tq, cpart + 16, y + 16);
+                for (int q = 0; q < 32; ++q) y[q] += (cpart + q <= row - 64) ? v[q] : 0.f;
             }
+            uint32_t py[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) py[e] = pack_bf16(y[2 * e], y[2 * e + 1]);
+            tmem_st16(tmem + lane_base + kColYA + cpart / 2, py);
+            tmem_st_wait();
         }
         tc_fence_before();
-        fence_proxy_async_smem();
         __syncthreads();
         if (*flag) break;
 
-        // ---------------------------------- G5 and the state product S0 [R'|Phi]
+        // ------------------- G5: [S_L^T; O^T] = [Phi^T; R'^T] [S0_hi | S0_lo]^T + Y^T V^T
         if (tid == 0) {
             tc_fence_after();
-            umma_128xNx64(tmem + kColG5, smem_addr(base + OFF_OPY), smem_addr(base + OFF_V), 64, false);
-            umma_128xNx64_bmn(tmem + kColG5, smem_addr(base + OFF_OPA2), smem_addr(base + OFF_SHI), 64, true);
-            umma_128xNx64_bmn(tmem + kColG5, smem_addr(base + OFF_OPA2), smem_addr(base + OFF_SLO), 64, true);
+            umma_ta_128xNx64(tmem + 0, tmem + kColA2, smem_addr(base + OFF_SHI), 64, false, true);
+            umma_ta_128xNx64(tmem + 0, tmem + kColA2, smem_addr(base + OFF_SLO), 64, true, true);
+            umma_ta_128xNx64(tmem + 0, tmem + kColYA, smem_addr(base + OFF_V), 64, true, false);
             umma_commit(bar_mma);
         }
-        if (tid == 0 && !last) stage_inputs(4, 5, tc0 + kL, false);  // KHT, R0 are dead: a, b
         mma_wait(bar_mma, ph_mma, flag);
         ph_mma ^= 1;
         tc_fence_after();

@@ -159,6 +159,21 @@ __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Store 16 consecutive 32-bit columns of this warp's 32 lanes (lane l of the
+// warp writes row lane base + l).  Complete with tmem_st_wait.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // -------------------------------------------------------------------- UMMA
 // Shared-memory matrix descriptor for a K-major operand stored with the
 // 128-byte swizzle: rows of 128 bytes (64 bf16 of K), 8-row atoms of 1024
@@ -210,6 +225,19 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint6
         : "memory");
 }
 
+// As umma_bf16 with A (M rows x 16 bf16 of K) in tensor memory at a_tmem: row m
+// in lane m, K elements 2c and 2c+1 packed (low, high) in column c, so one K=16
+// slice spans 8 columns.
+__device__ __forceinline__ void umma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                             uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive on `bar` once every tcgen05 operation issued so far by this thread
 // has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
@@ -243,6 +271,21 @@ __device__ __forceinline__ void umma_128xNx64_bmn(uint32_t d_tmem, uint32_t a_sa
         umma_bf16(d_tmem, desc_sw128(a_saddr + 32 * k),
                   desc_sw128_mn(b_saddr + 2048 * k, b_atom_stride), idesc,
                   (accumulate || k > 0) ? 1u : 0u);
+    }
+}
+
+// D (M=128) (+)= A (128 x 64 bf16 in tensor memory from column a_tmem, 32
+// columns) * B^T, B N x 64 in shared memory: K-major (b_mn = false) or MN-major
+// with 64-wide N atoms `b_atom_stride` bytes apart (b_mn = true).
+__device__ __forceinline__ void umma_ta_128xNx64(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_saddr,
+                                                 uint32_t N, bool accumulate, bool b_mn,
+                                                 uint32_t b_atom_stride = 8192) {
+    const uint32_t idesc = idesc_bf16_f32(128, N, b_mn ? 1u : 0u);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint64_t bd = b_mn ? desc_sw128_mn(b_saddr + 2048 * k, b_atom_stride)
+                                 : desc_sw128(b_saddr + 32 * k);
+        umma_bf16_ta(d_tmem, a_tmem + 8 * k, bd, idesc, (accumulate || k > 0) ? 1u : 0u);
     }
 }
 
