@@ -482,10 +482,15 @@ __global__ void __launch_bounds__(kThreads, 2)
         const bool last = (c + 1 == n_chunks);
 
         // ---------------------------------------------------------- E phase
+        // E1 builds the Gram operands of G1 and G1'; E2 (below, while those MMAs
+        // run) the remaining operands from the same registers.
+        const int tb = 8 * warp;  // this warp's 8 tokens; lane: channels 2l, 2l+1
+        const int ch = 2 * lane;
+        const uint32_t xl = static_cast<uint32_t>(lane) >> 2;  // swizzled offset of (row tb + i, column ch):
+        const uint32_t rowbase = 1024u * warp + 4u * (lane & 3);  // rowbase + i * 128 + ((xl ^ i) << 4)
+        uint32_t in_r[8], in_w[8], in_k[8], in_v[8], in_a[8], in_b[8];
+        float e0s, e1s, eGm0, eGm1, EL0, EL1;  // 2^(G_{tb-1} - Gm), 2^Gm, 2^(G_L - Gm) per channel
         {
-            const int tb = 8 * warp;  // this warp's 8 tokens; lane: channels 2l, 2l+1
-            const int ch = 2 * lane;
-            uint32_t in_r[8], in_w[8], in_k[8], in_v[8], in_a[8], in_b[8];
             mma_wait(bar_in, ph_in, flag);  // the staged inputs have landed
             ph_in ^= 1;
             {
@@ -523,39 +528,61 @@ __global__ void __launch_bounds__(kThreads, 2)
             if (warp == 0) *reinterpret_cast<float2 *>(gam + ch) = make_float2(ex2_approx(G630), ex2_approx(G631));
             if (!(fabsf(G0 - Gm0) <= kMaxLog2Range && fabsf(G1 - Gm1) <= kMaxLog2Range))
                 range_bad = true;  // G[tb-1] (G[-1] = 0 for the first warp)
-            const float EL0 = ex2_approx(G630 - Gm0), EL1 = ex2_approx(G631 - Gm1);
+            EL0 = ex2_approx(G630 - Gm0);
+            EL1 = ex2_approx(G631 - Gm1);
             // 2^Gm is a normal float whenever the range check passes (|Gm| <= 120), so
             // the decays from the chunk start are 2^(G - Gm) * 2^Gm.
-            const float eGm0 = ex2_approx(Gm0), eGm1 = ex2_approx(Gm1);
+            eGm0 = ex2_approx(Gm0);
+            eGm1 = ex2_approx(Gm1);
             // e = 2^(G_t - Gm) runs as a product: e_t = e_{t-1} w_t (each e_t lies in
             // [2^-120, 2^120] when the range check passes, so nothing under- or overflows);
             // its reciprocal gives 2^(Gm - G_t).
-            float e0 = ex2_approx(G0 - Gm0), e1 = ex2_approx(G1 - Gm1);
-            uint32_t ep2 = pack_bf16(e0, e1);                 // 2^(G_{t-1} - Gm)
-            uint32_t dp2 = pack_bf16(e0 * eGm0, e1 * eGm1);  // D(0, t-1]
-            // swizzled byte offset of (row tb + i, column ch)
-            const uint32_t xl = static_cast<uint32_t>(lane) >> 2;
-            const uint32_t rowbase = 1024u * warp + 4u * (lane & 3);
-            uint8_t *g1a = base + OFF_G1A, *g1b = base + OFF_G1B, *r0t = base + OFF_R0;
+            e0s = ex2_approx(G0 - Gm0);
+            e1s = ex2_approx(G1 - Gm1);
+            float e0 = e0s, e1 = e1s;
+            uint32_t ep2 = pack_bf16(e0, e1);  // 2^(G_{t-1} - Gm)
+            uint8_t *g1a = base + OFF_G1A, *g1b = base + OFF_G1B;
             bool in_range = true;  // every 2^(G_t - Gm) of this warp's tokens within 2^+-120
-            uint32_t cb[3][2][4];  // channel-major operands [Bhat, Khat, V][channel][token pair]
-            uint32_t prv[3];
 #pragma unroll
             for (int ii = 0; ii < 8; ++ii) {
                 e0 *= bf16_lo(in_w[ii]);  // padding tokens have w = 1
                 e1 *= bf16_hi(in_w[ii]);
                 in_range = in_range && e0 >= kMinDecayRel && e0 <= kMaxDecayRel &&
                            e1 >= kMinDecayRel && e1 <= kMaxDecayRel;  // false for NaN too
-                const float iv0 = rcp_approx(e0), iv1 = rcp_approx(e1);
-                const uint32_t ec2 = pack_bf16(e0, e1);                  // 2^(G_t - Gm)
-                const uint32_t iv2 = pack_bf16(iv0, iv1);                // 2^(Gm - G_t)
-                const uint32_t dc2 = pack_bf16(e0 * eGm0, e1 * eGm1);    // D(0, t]
-                const uint32_t dl2 = pack_bf16(EL0 * iv0, EL1 * iv1);    // D(t, L]
+                const uint32_t ec2 = pack_bf16(e0, e1);                              // 2^(G_t - Gm)
+                const uint32_t iv2 = pack_bf16(rcp_approx(e0), rcp_approx(e1));    // 2^(Gm - G_t)
                 const uint32_t off = rowbase + ii * 128 + ((xl ^ ii) << 4);
                 *reinterpret_cast<uint32_t *>(g1a + off) = bmul2(in_b[ii], iv2);
                 *reinterpret_cast<uint32_t *>(g1a + 8192 + off) = bmul2(in_k[ii], iv2);
                 *reinterpret_cast<uint32_t *>(g1b + off) = bmul2(in_a[ii], ep2);
                 *reinterpret_cast<uint32_t *>(g1b + 8192 + off) = bmul2(in_r[ii], ec2);
+                ep2 = ec2;
+            }
+            if (!in_range) range_bad = true;
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+
+        // --------------------------------------------------- G1 and G1'
+        if (tid == 0) {
+            tc_fence_after();
+            umma_128xNx64(tmem + kColG1, smem_addr(base + OFF_G1A), smem_addr(base + OFF_G1B), 64, false);
+            umma_128xNx64(tmem + kColG1p, smem_addr(base + OFF_G1B), smem_addr(base + OFF_G1A), 128, false);
+            umma_commit(bar_mma);
+        }
+        {  // E2, while G1 and G1' run: R0, A0 (row-major), Bhat^T, Khat^T, V^T (channel-major)
+            float e0 = e0s, e1 = e1s;
+            uint32_t dp2 = pack_bf16(e0 * eGm0, e1 * eGm1);  // D(0, t-1]
+            uint8_t *r0t = base + OFF_R0;
+            uint32_t cb[3][2][4];  // channel-major operands [Bhat, Khat, V][channel][token pair]
+            uint32_t prv[3];
+#pragma unroll
+            for (int ii = 0; ii < 8; ++ii) {
+                e0 *= bf16_lo(in_w[ii]);
+                e1 *= bf16_hi(in_w[ii]);
+                const uint32_t dc2 = pack_bf16(e0 * eGm0, e1 * eGm1);                           // D(0, t]
+                const uint32_t dl2 = pack_bf16(EL0 * rcp_approx(e0), EL1 * rcp_approx(e1));  // D(t, L]
+                const uint32_t off = rowbase + ii * 128 + ((xl ^ ii) << 4);
                 *reinterpret_cast<uint32_t *>(r0t + off) = bmul2(in_r[ii], dc2);
                 *reinterpret_cast<uint32_t *>(base + OFF_A0 + off) = bmul2(in_a[ii], dp2);
                 const uint32_t cur[3] = {bmul2(in_b[ii], dl2), bmul2(in_k[ii], dl2), in_v[ii]};
@@ -568,10 +595,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                         cb[o][1][ii >> 1] = __byte_perm(prv[o], cur[o], 0x7632);
                     }
                 }
-                ep2 = ec2;
                 dp2 = dc2;
             }
-            if (!in_range) range_bad = true;
             uint8_t *dst[3] = {base + OFF_G2A, base + OFF_KHT, base + OFF_V};
 #pragma unroll
             for (int o = 0; o < 3; ++o)
@@ -579,16 +604,6 @@ __global__ void __launch_bounds__(kThreads, 2)
                 for (int e = 0; e < 2; ++e)  // 8 tokens of channel-major row ch + e
                     *reinterpret_cast<uint4 *>(dst[o] + sw128_off(ch + e, tb)) =
                         make_uint4(cb[o][e][0], cb[o][e][1], cb[o][e][2], cb[o][e][3]);
-        }
-        fence_proxy_async_smem();
-        __syncthreads();
-
-        // --------------------------------------------------- G1 and G1'
-        if (tid == 0) {
-            tc_fence_after();
-            umma_128xNx64(tmem + kColG1, smem_addr(base + OFF_G1A), smem_addr(base + OFF_G1B), 64, false);
-            umma_128xNx64(tmem + kColG1p, smem_addr(base + OFF_G1B), smem_addr(base + OFF_G1A), 128, false);
-            umma_commit(bar_mma);
         }
         if (c > 0) {  // the previous chunk's state product, read back while G1 and G1' run
             tc_fence_after();
