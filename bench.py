@@ -2,7 +2,7 @@
 """Benchmark of the WKV-7 state-slot hot path on one GB300 (or N replicas).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload mixed|decode12|prefill|sweep] [--batch B] [--graph]
+                    [--workload mixed|decode12|prefill|sweep|verify|hibernate] [--batch B] [--graph]
 
 Default workload ("mixed", one step = every part of the hot path): on a
 4096-slot pool of 32 heads x 64 (1 layer) -- create 64 fresh slots, snapshot
@@ -52,7 +52,8 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=["mixed", "decode12", "prefill", "sweep", "verify"],
+    p.add_argument("--workload", choices=["mixed", "decode12", "prefill", "sweep", "verify",
+                                          "hibernate"],
                    default="mixed")
     p.add_argument("--batch", type=int, default=4096, help="sweep batch size")
     p.add_argument("--graph", action="store_true", help="replay each step as a CUDA graph")
@@ -522,6 +523,74 @@ class Verify(Workload):
                             self.tokens_per_step)
 
 
+class Hibernate(Workload):
+    """Hibernate 1024 slots of the mixed step's pool (4096 slots x 32 heads, 512 KiB
+    each) to pinned host memory and resume them, one call each per step.  The bound
+    is the device's link to host memory, so the roofline peak is a contiguous
+    pinned copy of the same bytes measured in the same run."""
+    name = "hibernate_1024_of_4096"
+    unit = "slots/s"
+
+    def __init__(self, torch, device, batch=1024):
+        from rwkv_wkv_gb300 import Pool
+        W = wl.MIXED
+        self.torch, self.device = torch, device
+        self.H, self.N, self.B = W.H, W.N, batch
+        self.pool = Pool(1, W.H, W.n_slots, device=device)
+        g = torch.Generator(device=device).manual_seed(W.seed)
+        self.pool.states.normal_(0.0, 0.1, generator=g)
+        plan = wl.mixed_plan()
+        self.ids = torch.as_tensor(plan["decode"][:batch].astype(np.int32), device=device)
+        self.host = torch.empty(batch * self.pool.slot_bytes, dtype=torch.uint8, pin_memory=True)
+        self.phases = ["hibernate", "resume"]
+        link = batch * self.pool.slot_bytes
+        self.phase_bytes = {"hibernate": link, "resume": link}
+        self.tokens_per_step = 2 * batch
+        self.dominant = "hibernate"
+        self.launches_per_step = 2
+        self.no_e2e = True
+
+    def step(self, ev=None):
+        rec = (lambda name: ev[name].record()) if ev else (lambda name: None)
+        rec("start")
+        self.pool.hibernate(self.ids, self.host)
+        rec("hibernate")
+        self.pool.resume(self.host, self.ids)
+        rec("resume")
+
+    def link_peak(self):
+        """GB/s of contiguous pinned copies of the same bytes, device->host and back."""
+        torch = self.torch
+        dev = torch.empty(self.host.numel(), dtype=torch.uint8, device=self.device)
+        out = {}
+        for name, fn in (("d2h", lambda: self.host.copy_(dev, non_blocking=True)),
+                         ("h2d", lambda: dev.copy_(self.host, non_blocking=True))):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            for _ in range(10):
+                fn()
+            e.record()
+            torch.cuda.synchronize()
+            out[name] = self.host.numel() * 10 / (s.elapsed_time(e) / 1e3) / 1e9
+        del dev
+        return out
+
+    def host_io(self):
+        return [self.ids], []
+
+    def config(self):
+        return {"workload": "hibernate + resume of 1024 slots (32 heads x 64, 1 layer, "
+                            "512 KiB per slot) of a 4096-slot pool to pinned host memory",
+                "pool_slots": wl.MIXED.n_slots, "layers": 1, "heads": self.H,
+                "head_size": self.N, "verb_slots": self.B, "state_dtype": "f32"}
+
+    def oracle_sample(self, frac_target):
+        return None
+
+
 def make_workload(args, torch, device):
     if args.workload == "mixed":
         return Mixed(torch, device)
@@ -531,6 +600,8 @@ def make_workload(args, torch, device):
         return Prefill(torch, device, checkpoints=args.checkpoints)
     if args.workload == "verify":
         return Verify(torch, device, K=args.verify_k, rollback=not args.no_rollback)
+    if args.workload == "hibernate":
+        return Hibernate(torch, device)
     return Sweep(torch, device, args.batch)
 
 
@@ -677,6 +748,19 @@ def run_ours(args):
         gbs = wk.phase_bytes[n] / (ms / 1e3) / 1e9
         phases[n] = {"ms": round(ms, 4), "GB_per_s": round(gbs, 1),
                      "hbm_frac": round(gbs / hbm, 4)}
+    if hasattr(wk, "link_peak"):  # bound by the link to host memory, not by HBM
+        link = wk.link_peak()
+        for n, direction in (("hibernate", "d2h"), ("resume", "h2d")):
+            phases[n] = {"ms": phases[n]["ms"], "GB_per_s": phases[n]["GB_per_s"],
+                         "link_frac": round(phases[n]["GB_per_s"] / link[direction], 4),
+                         "link_peak_GB_per_s": round(link[direction], 1)}
+        roofline = {"bound": "host link", "kernel": "slot_copy_kernel (hibernate)",
+                    "achieved": phases["hibernate"]["GB_per_s"], "peak": round(link["d2h"], 1),
+                    "unit": "GB/s", "frac": phases["hibernate"]["link_frac"],
+                    "peak_source": "measured in this run: contiguous pinned device->host copy "
+                                   "of the same bytes (cudaMemcpyAsync through torch)",
+                    "bytes_per_launch": wk.phase_bytes["hibernate"],
+                    "ms_per_launch": phases["hibernate"]["ms"], "traffic": None}
     extra = {}
     if "decode" in phase_ms:
         rows = wk.phase_bytes["decode"]
@@ -697,15 +781,15 @@ def run_ours(args):
                             "bound": "hbm"}
 
     e2e = None
-    if not args.no_e2e and graph is None:
+    if not args.no_e2e and graph is None and not getattr(wk, "no_e2e", False):
         e2e = run_e2e(torch, wk, args, world, device)
 
     cpu_base = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and wk.oracle_sample(0.01):
         cpu_base = cpu_baseline(wk, target_seconds=8.0)
 
     line = {
-        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
+        "metric": METRIC, "value": round(value, 1), "unit": getattr(wk, "unit", "tokens/s"),
         "n_gpus": world, "steps": args.steps, "warmup": max(3, args.warmup),
         "ms_per_step": round(elapsed_max * 1e3 / args.steps, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -775,6 +859,9 @@ def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return None
+    if args.workload == "hibernate":
+        return {"impl": "reference", "unavailable": "the oracle computes the recurrence only; "
+                "a slot copy to host memory has no CPU reference computation"}
     # The oracle needs the workload's shapes only: built without a GPU.
     wk = _shapes_only(args)
     per_step = min(5.0, 90.0 / max(1, args.steps + args.warmup))

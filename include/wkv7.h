@@ -179,6 +179,28 @@ wkv7_status wkv7_slot_restore(wkv7_pool *pool, const int32_t *snap_ids_dev,
 wkv7_status wkv7_slot_fork(wkv7_pool *pool, const int32_t *src_ids_dev,
                            const int32_t *dst_ids_dev, int32_t n, cudaStream_t stream);
 
+/* hibernate: copy slot slot_ids_dev[i] -> bytes [i*slot_bytes, (i+1)*slot_bytes)
+ * of host_dst, i < n, bit for bit; resume: those bytes of host_src -> slot
+ * slot_ids_dev[i].  The verbs "hibernate" and "resume" of "wkvm: state-slot
+ * inference for RWKV, GDN and Mamba hybrids", section "The allocation unit
+ * wkvm changes": a fixed-size slot can be parked off the GPU and brought back.
+ * host_dst / host_src is caller-owned page-locked host memory that the device
+ * can address (cudaHostAlloc / cudaMallocHost, or cudaHostRegister with the
+ * mapped flag), 16-byte aligned, of host_bytes >= n * wkv7_slot_bytes(pool)
+ * bytes, packed slot after slot.  One kernel gathers (or scatters) the slots
+ * over the device's link to host memory; asynchronous on `stream` like every
+ * verb, so the host must not read host_dst (or change host_src) before the
+ * stream has passed the call.  The slot table is not changed: freeing a
+ * hibernated slot's id, and taking one for its resume, are the caller's.
+ * Errors: INVALID_ARG (NULL pointers, host_bytes too small, host memory that
+ * is not page-locked and device-mapped or not 16-byte aligned), CUDA.  Device:
+ * WKV7_DEV_BAD_SLOT for an out-of-range id (that slot is not copied).  n == 0
+ * is a no-op. */
+wkv7_status wkv7_slot_hibernate(wkv7_pool *pool, const int32_t *slot_ids_dev, int32_t n,
+                                void *host_dst, size_t host_bytes, cudaStream_t stream);
+wkv7_status wkv7_slot_resume(wkv7_pool *pool, const void *host_src, size_t host_bytes,
+                             const int32_t *slot_ids_dev, int32_t n, cudaStream_t stream);
+
 /* --------------------------------------------------------- recurrence ---- */
 
 /* decode: one token for each of n slots at one layer.  For b < n and every

@@ -300,7 +300,7 @@ wkv7_status wkv7_slot_reset(wkv7_pool *pool, const int32_t *slot_ids_dev, int32_
 static wkv7_status copy_verb(wkv7_pool *pool, float *dst, int n_dst, const int32_t *dst_ids,
                              const float *src, int n_src, const int32_t *src_ids, int32_t n,
                              cudaStream_t stream, const char *what) {
-    if (!pool || n < 0 || (n > 0 && (!dst_ids || !src_ids))) return WKV7_ERR_INVALID_ARG;
+    if (!pool || n < 0) return WKV7_ERR_INVALID_ARG;  // null ids: checked by the callers
     if (n == 0) return WKV7_OK;
     if (n_dst == 0 || n_src == 0) return WKV7_ERR_INVALID_ARG;  // no snapshot store
     wkv7::CopyArgs a;
@@ -320,23 +320,60 @@ static wkv7_status copy_verb(wkv7_pool *pool, float *dst, int n_dst, const int32
 
 wkv7_status wkv7_slot_snapshot(wkv7_pool *pool, const int32_t *slot_ids_dev,
                                const int32_t *snap_ids_dev, int32_t n, cudaStream_t stream) {
-    if (!pool) return WKV7_ERR_INVALID_ARG;
+    if (!pool || (n > 0 && (!slot_ids_dev || !snap_ids_dev))) return WKV7_ERR_INVALID_ARG;
     return copy_verb(pool, pool->snaps, pool->desc.n_snapshots, snap_ids_dev, pool->states,
                      pool->desc.n_slots, slot_ids_dev, n, stream, "slot_snapshot");
 }
 
 wkv7_status wkv7_slot_restore(wkv7_pool *pool, const int32_t *snap_ids_dev,
                               const int32_t *slot_ids_dev, int32_t n, cudaStream_t stream) {
-    if (!pool) return WKV7_ERR_INVALID_ARG;
+    if (!pool || (n > 0 && (!slot_ids_dev || !snap_ids_dev))) return WKV7_ERR_INVALID_ARG;
     return copy_verb(pool, pool->states, pool->desc.n_slots, slot_ids_dev, pool->snaps,
                      pool->desc.n_snapshots, snap_ids_dev, n, stream, "slot_restore");
 }
 
 wkv7_status wkv7_slot_fork(wkv7_pool *pool, const int32_t *src_ids_dev, const int32_t *dst_ids_dev,
                            int32_t n, cudaStream_t stream) {
-    if (!pool) return WKV7_ERR_INVALID_ARG;
+    if (!pool || (n > 0 && (!src_ids_dev || !dst_ids_dev))) return WKV7_ERR_INVALID_ARG;
     return copy_verb(pool, pool->states, pool->desc.n_slots, dst_ids_dev, pool->states,
                      pool->desc.n_slots, src_ids_dev, n, stream, "slot_fork");
+}
+
+// Device address of a caller's pinned (page-locked, mapped) host buffer, or
+// nullptr when the pointer is not such memory or is not 16-byte aligned.
+static void *pinned_host_device_ptr(const void *host) {
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, host) != cudaSuccess) {
+        cudaGetLastError();  // clear the sticky-free error state of this query
+        return nullptr;
+    }
+    if (attr.type != cudaMemoryTypeHost || !attr.devicePointer) return nullptr;
+    if (reinterpret_cast<uintptr_t>(attr.devicePointer) % 16 != 0) return nullptr;
+    return attr.devicePointer;
+}
+
+wkv7_status wkv7_slot_hibernate(wkv7_pool *pool, const int32_t *slot_ids_dev, int32_t n,
+                                void *host_dst, size_t host_bytes, cudaStream_t stream) {
+    if (!pool || n < 0 || (n > 0 && (!slot_ids_dev || !host_dst))) return WKV7_ERR_INVALID_ARG;
+    if (n == 0) return WKV7_OK;
+    const size_t slot_bytes = static_cast<size_t>(pool->slot_floats) * sizeof(float);
+    if (host_bytes / slot_bytes < static_cast<size_t>(n)) return WKV7_ERR_INVALID_ARG;
+    void *dev = pinned_host_device_ptr(host_dst);
+    if (!dev) return WKV7_ERR_INVALID_ARG;
+    return copy_verb(pool, static_cast<float *>(dev), n, nullptr, pool->states, pool->desc.n_slots,
+                     slot_ids_dev, n, stream, "slot_hibernate");
+}
+
+wkv7_status wkv7_slot_resume(wkv7_pool *pool, const void *host_src, size_t host_bytes,
+                             const int32_t *slot_ids_dev, int32_t n, cudaStream_t stream) {
+    if (!pool || n < 0 || (n > 0 && (!slot_ids_dev || !host_src))) return WKV7_ERR_INVALID_ARG;
+    if (n == 0) return WKV7_OK;
+    const size_t slot_bytes = static_cast<size_t>(pool->slot_floats) * sizeof(float);
+    if (host_bytes / slot_bytes < static_cast<size_t>(n)) return WKV7_ERR_INVALID_ARG;
+    const void *dev = pinned_host_device_ptr(host_src);
+    if (!dev) return WKV7_ERR_INVALID_ARG;
+    return copy_verb(pool, pool->states, pool->desc.n_slots, slot_ids_dev,
+                     static_cast<const float *>(dev), n, nullptr, n, stream, "slot_resume");
 }
 
 // ------------------------------------------------------------- recurrence --

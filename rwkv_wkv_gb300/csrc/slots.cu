@@ -1,6 +1,7 @@
 // Slot verbs as device copies ("wkvm: state-slot inference for RWKV, GDN and
 // Mamba hybrids", "The allocation unit wkvm changes": create, snapshot, fork,
-// resume).  A slot is one contiguous range of float32 states (every layer and
+// hibernate, resume; hibernate and resume move slots to and from a pinned host
+// buffer that the kernel reaches through its mapped device address).  A slot is one contiguous range of float32 states (every layer and
 // head), so every verb is a whole-range copy or fill.  Each CTA moves 32 KiB
 // of one slot with 128-bit streaming loads/stores; grid.y walks the slot
 // pairs.  HBM-bound: 2 x slot_bytes per copied slot, 1 x per zeroed slot.
@@ -17,8 +18,8 @@ constexpr int kMaxGridY = 65535;
 
 __global__ void __launch_bounds__(kThreads) slot_copy_kernel(CopyArgs a, int pair0) {
     const int pair = pair0 + blockIdx.y;
-    const int d = __ldg(a.dst_ids + pair);
-    const int s = __ldg(a.src_ids + pair);
+    const int d = a.dst_ids ? __ldg(a.dst_ids + pair) : pair;  // no id array: the i-th slot of a packed buffer
+    const int s = a.src_ids ? __ldg(a.src_ids + pair) : pair;
     if (d < 0 || d >= a.n_dst || s < 0 || s >= a.n_src) {
         if (blockIdx.x == 0 && threadIdx.x == 0) flag_status(a.status, WKV7_DEV_BAD_SLOT);
         return;

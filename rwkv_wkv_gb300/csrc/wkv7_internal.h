@@ -68,7 +68,8 @@ struct PrefillArgs {
     CheckpointArgs ck;
 };
 
-// Whole-slot copies: dst[dst_ids[i]] <- src[src_ids[i]], slot_floats each.
+// Whole-slot copies: dst[dst_ids[i]] <- src[src_ids[i]], slot_floats each; a
+// null id array stands for the identity (the i-th slot of a packed buffer).
 struct CopyArgs {
     float *dst;
     const float *src;

@@ -67,6 +67,8 @@ _SIGS = {
     "wkv7_slot_snapshot": (ctypes.c_int, [_P, _VP, _VP, _I32, _VP]),
     "wkv7_slot_restore": (ctypes.c_int, [_P, _VP, _VP, _I32, _VP]),
     "wkv7_slot_fork": (ctypes.c_int, [_P, _VP, _VP, _I32, _VP]),
+    "wkv7_slot_hibernate": (ctypes.c_int, [_P, _VP, _I32, _VP, ctypes.c_size_t, _VP]),
+    "wkv7_slot_resume": (ctypes.c_int, [_P, _VP, ctypes.c_size_t, _VP, _I32, _VP]),
     "wkv7_decode_step": (ctypes.c_int, [_P, _I32, _VP, _I32, ctypes.c_int] + [_VP] * 7 + [_VP]),
     "wkv7_prefill": (ctypes.c_int, [_P, _I32, _VP, _VP, _I32, _I32, _I32, ctypes.c_int]
                      + [_VP] * 7 + [_VP]),
@@ -245,6 +247,31 @@ class Pool:
 
     def fork(self, src_ids: torch.Tensor, dst_ids: torch.Tensor, stream=None) -> None:
         self._pairs("wkv7_slot_fork", src_ids, dst_ids, stream)
+
+    def _host_buffer(self, host: torch.Tensor, n: int) -> tuple[int, int]:
+        if not isinstance(host, torch.Tensor) or host.is_cuda or not host.is_contiguous():
+            raise TypeError("host buffer must be a contiguous CPU tensor (pinned memory)")
+        nbytes = host.numel() * host.element_size()
+        if nbytes < n * self.slot_bytes:
+            raise ValueError(f"host buffer holds {nbytes} bytes, {n} slots need {n * self.slot_bytes}")
+        return host.data_ptr(), nbytes
+
+    def hibernate(self, slot_ids: torch.Tensor, host: torch.Tensor, stream=None) -> None:
+        """Copy the slots slot_ids[i] into pinned host memory `host`, packed slot after slot
+        (asynchronous on the stream; see wkv7_slot_hibernate)."""
+        n = slot_ids.numel()
+        ptr, nbytes = self._host_buffer(host, n)
+        _check(self._lib.wkv7_slot_hibernate(self._h, _dev_i32(slot_ids, "slot_ids", self.device), n,
+                                             ptr, nbytes, _stream_handle(stream, self.device)),
+               "slot_hibernate")
+
+    def resume(self, host: torch.Tensor, slot_ids: torch.Tensor, stream=None) -> None:
+        """Copy packed slot images from pinned host memory `host` into the slots slot_ids[i]."""
+        n = slot_ids.numel()
+        ptr, nbytes = self._host_buffer(host, n)
+        _check(self._lib.wkv7_slot_resume(self._h, ptr, nbytes,
+                                          _dev_i32(slot_ids, "slot_ids", self.device), n,
+                                          _stream_handle(stream, self.device)), "slot_resume")
 
     def _pairs(self, fn, first, second, stream):
         if first.numel() != second.numel():

@@ -162,6 +162,17 @@ def test_host_checks_return_before_launch(lib):
         assert lib.wkv7_slot_fork(h, None, x, 1, None) == 1
         assert lib.wkv7_slot_snapshot(h, x, x, -1, None) == 1
         assert lib.wkv7_slot_restore(h, x, x, 0, None) == 0
+        # hibernate / resume: NULL ids or host buffer, n < 0, a host buffer too small
+        sb = lib.wkv7_slot_bytes(h)
+        assert lib.wkv7_slot_hibernate(h, None, 1, x, sb, None) == 1
+        assert lib.wkv7_slot_hibernate(h, x, 1, None, sb, None) == 1
+        assert lib.wkv7_slot_hibernate(h, x, -1, x, sb, None) == 1
+        assert lib.wkv7_slot_hibernate(h, x, 2, x, 2 * sb - 1, None) == 1
+        assert lib.wkv7_slot_hibernate(h, x, 0, None, 0, None) == 0  # empty: no-op
+        assert lib.wkv7_slot_resume(h, None, sb, x, 1, None) == 1
+        assert lib.wkv7_slot_resume(h, x, sb, None, 1, None) == 1
+        assert lib.wkv7_slot_resume(h, x, sb - 16, x, 1, None) == 1
+        assert lib.wkv7_slot_resume(h, x, 0, x, 0, None) == 0
         ids = (ctypes.c_int32 * 9)()
         assert lib.wkv7_slot_create(h, 9, ids, None) == 4     # POOL_FULL, nothing allocated
         assert lib.wkv7_slot_count_free(h) == 8
