@@ -65,6 +65,8 @@ def parse_args(argv=None):
                    help="verify workload: tokens per slot per call (K drafts + 1)")
     p.add_argument("--no-rollback", action="store_true",
                    help="verify workload: no per-token rollback states")
+    p.add_argument("--state-dtype", choices=["f32", "bf16"], default="f32",
+                   help="sweep workload: state storage (bf16 halves the state bytes)")
     return p.parse_args(argv)
 
 
@@ -364,20 +366,23 @@ class Decode12(Workload):
 class Sweep(Workload):
     name = wl.SWEEP_32L.name
 
-    def __init__(self, torch, device, batch):
+    def __init__(self, torch, device, batch, state_dtype="f32"):
         from rwkv_wkv_gb300 import Pool
         W = wl.SWEEP_32L
         self.torch, self.W = torch, W
         self.H, self.N, self.L, self.B = W.H, W.N, W.n_layers, batch
-        self.pool = Pool(W.n_layers, W.H, W.n_slots, device=device)
+        self.state_dtype = state_dtype
+        self.state_head_bytes = HEAD_BYTES_STATE // (2 if state_dtype == "bf16" else 1)
+        self.pool = Pool(W.n_layers, W.H, W.n_slots, device=device, state_dtype=state_dtype)
         g = torch.Generator(device=device).manual_seed(W.seed)
-        self.pool.states.normal_(0.0, 0.1, generator=g)
+        for l0 in range(0, W.n_slots, 256):  # in pieces: no float32 temporary of a bf16 pool
+            self.pool.states[l0:l0 + 256].normal_(0.0, 0.1, generator=g)
         slots = wl.distinct_slots(W.seed, f"sweep/slots{batch}", batch, W.n_slots)
         self.ids = torch.as_tensor(slots.astype(np.int32), device=device)
         self.ins = wl.token_inputs_device(W.seed, batch, W.H, W.N, device)
         self.o = torch.empty(batch, W.H, W.N, dtype=torch.float32, device=device)
         self.phases = ["decode"]
-        row = W.H * (2 * HEAD_BYTES_STATE + W.N * 2 * 6 + W.N * 4)
+        row = W.H * (2 * self.state_head_bytes + W.N * 2 * 6 + W.N * 4)
         self.phase_bytes = {"decode": self.L * self.B * row}
         self.tokens_per_step = self.L * self.B
         self.dominant = "decode"
@@ -395,10 +400,12 @@ class Sweep(Workload):
         return [self.ids] + list(self.ins), [self.o]
 
     def config(self):
-        return {"workload": self.W.description + f"; batch {self.B}", "pool_slots": self.W.n_slots,
+        return {"workload": self.W.description + f"; batch {self.B}"
+                + ("; bf16 state storage" if self.state_dtype == "bf16" else ""),
+                "pool_slots": self.W.n_slots,
                 "layers": self.L, "heads": self.H, "head_size": self.N, "decode_slots": self.B,
-                "state_bytes_per_slot_layer": self.H * HEAD_BYTES_STATE,
-                "state_dtype": "f32", "input_dtype": "bf16", "output_dtype": "f32"}
+                "state_bytes_per_slot_layer": self.H * self.state_head_bytes,
+                "state_dtype": self.state_dtype, "input_dtype": "bf16", "output_dtype": "f32"}
 
     def oracle_sample(self, frac_target):
         return _head_sample(self.H, frac_target, self.B, None, self.tokens_per_step,
@@ -602,7 +609,7 @@ def make_workload(args, torch, device):
         return Verify(torch, device, K=args.verify_k, rollback=not args.no_rollback)
     if args.workload == "hibernate":
         return Hibernate(torch, device)
-    return Sweep(torch, device, args.batch)
+    return Sweep(torch, device, args.batch, args.state_dtype)
 
 
 # ------------------------------------------------------------- oracle timing
@@ -764,7 +771,7 @@ def run_ours(args):
     extra = {}
     if "decode" in phase_ms:
         rows = wk.phase_bytes["decode"]
-        per_row = wk.H * (2 * HEAD_BYTES_STATE + wk.N * 2 * 6 + wk.N * 4)
+        per_row = wk.H * (2 * getattr(wk, "state_head_bytes", HEAD_BYTES_STATE) + wk.N * 2 * 6 + wk.N * 4)
         n_slot_steps = rows // per_row
         extra["decode"] = {"slot_steps_per_s": round(n_slot_steps / (phase_ms["decode"] / 1e3), 1),
                            "GB_per_s": phases["decode"]["GB_per_s"],
@@ -793,15 +800,19 @@ def run_ours(args):
         "n_gpus": world, "steps": args.steps, "warmup": max(3, args.warmup),
         "ms_per_step": round(elapsed_max * 1e3 / args.steps, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32+bf16", "data": "synthetic",
+        "dtype": "bf16 state, f32 arithmetic" if getattr(wk, "state_dtype", "f32") == "bf16"
+                 else "f32+bf16", "data": "synthetic",
         "config": dict(wk.config(), parallelism=f"replicas x{world}" if world > 1 else "1 gpu",
                        l2="inputs larger than L2 (every step moves > 129 MB)",
                        graph=bool(graph)),
         "roofline": roofline, "phases": phases, **extra,
         "e2e": e2e, "gpu_launches": int(launches), "clocks": clk,
         "cpu_baseline": cpu_base,
-        "dtype_note": "state, decode arithmetic and outputs float32; prefill contractions "
-                      "bf16 tensor-core operands with float32 accumulation; inputs bf16",
+        "dtype_note": ("state stored in bf16 (each step computed in float32, the new state rounded "
+                       "to bf16); decode arithmetic and outputs float32; inputs bf16"
+                       if getattr(wk, "state_dtype", "f32") == "bf16" else
+                       "state, decode arithmetic and outputs float32; prefill contractions "
+                       "bf16 tensor-core operands with float32 accumulation; inputs bf16"),
     }
     if world > 1:
         torch.distributed.destroy_process_group()

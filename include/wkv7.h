@@ -19,8 +19,9 @@
  * fork and resume (restore).  A pool owns n_slots live slots and n_snapshots
  * parked copies.  One slot holds the states of every layer and head:
  *
- *     slot layout  [layer][head][i][j]  float32, row-major, contiguous
- *     slot bytes   n_layers * n_heads * head_size^2 * 4
+ *     slot layout  [layer][head][i][j]  float32 (or bf16, see state_dtype),
+ *                  row-major, contiguous
+ *     slot bytes   n_layers * n_heads * head_size^2 * 4 (2 for bf16 states)
  *     pool layout  [slot][layer][head][i][j]; snapshots use the same layout
  *
  * Token inputs are packed [rows][n_heads][head_size] (row = batch entry for
@@ -96,6 +97,14 @@ typedef struct {
                             wkv7_pool_required_bytes() bytes, 256-byte aligned,
                             that must outlive the pool. */
     size_t buffer_bytes; /* size of device_buffer (ignored when it is NULL) */
+    int32_t state_dtype; /* WKV7_F32 (0, the default when zero-initialised): float32
+                            states.  WKV7_BF16: states stored in bf16 -- half the
+                            bytes per slot and per decode step; each decode step
+                            is computed in float32 and rounds the new state to bf16
+                            (nearest even), the readout coming from the unrounded
+                            float32 state.  A bf16-state pool offers the slot table,
+                            every verb and wkv7_decode_step; the other recurrence
+                            calls return WKV7_ERR_UNSUPPORTED. */
 } wkv7_pool_desc;
 
 /* ---------------------------------------------------------------- pool ---- */
@@ -120,11 +129,14 @@ wkv7_status wkv7_pool_destroy(wkv7_pool *pool);
 /* Copy the pool's description (device_buffer = the buffer actually used). */
 wkv7_status wkv7_pool_get_desc(const wkv7_pool *pool, wkv7_pool_desc *out);
 
-/* Bytes of one slot (and of one snapshot): n_layers*n_heads*head_size^2*4. */
+/* Bytes of one slot (and of one snapshot): n_layers*n_heads*head_size^2*4
+ * (*2 instead of *4 for a bf16-state pool). */
 size_t wkv7_slot_bytes(const wkv7_pool *pool);
 
 /* Device address of the float32 [n_heads][head_size][head_size] state of
- * (slot, layer), or of a snapshot.  For tests and for initialising states.
+ * (slot, layer), or of a snapshot (for a bf16-state pool the address of the
+ * bf16 states, returned through the same float pointer type).  For tests and
+ * for initialising states.
  * Errors: INVALID_ARG, BAD_SLOT (index out of range; allocation state is not
  * checked). */
 wkv7_status wkv7_pool_state_ptr(wkv7_pool *pool, int32_t slot, int32_t layer, float **dev_ptr);

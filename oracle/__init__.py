@@ -157,6 +157,37 @@ def decode_step(states, r, w, k, v, a, b, n_threads: int = 1):
     return o.reshape(B, H, N), S.reshape(B, H, N, N)
 
 
+def round_bf16(x) -> np.ndarray:
+    """Round float64 values to the nearest bfloat16 value, ties to even, in one
+    step (no intermediate float32 rounding).  bfloat16 keeps the float32
+    exponent range with 8 significant bits: a finite x with 2^e <= |x| < 2^(e+1)
+    is a multiple of 2^(e-7); below 2^-126 the spacing stays 2^-133 (subnormal
+    values); magnitudes that round past the largest finite value become inf."""
+    x = np.asarray(x, dtype=np.float64)
+    out = x.copy()
+    fin = np.isfinite(x) & (x != 0.0)
+    xf = x[fin]
+    e = np.floor(np.log2(np.abs(xf)))
+    # log2 can misplace exact powers of two by one ulp: fix e so 2^e <= |x| < 2^(e+1)
+    e = np.where(np.abs(xf) < np.exp2(e), e - 1, e)
+    e = np.where(np.abs(xf) >= np.exp2(e + 1), e + 1, e)
+    q = np.exp2(np.maximum(e - 7, -133.0))   # spacing of bf16 values around x
+    y = np.rint(xf / q) * q                   # rint: nearest, ties to even
+    big = np.abs(y) > 3.3895313892515355e38   # (2 - 2^-7) * 2^127, the largest finite
+    y = np.where(big, np.copysign(np.inf, y), y)
+    out[fin] = y
+    return out
+
+
+def decode_step_bf16_state(states, r, w, k, v, a, b, n_threads: int = 1):
+    """One decode token for a pool whose states are stored in bfloat16: the step
+    runs in float64 from the (exactly widened) stored state, o is read from the
+    unrounded new state, and the new state is stored rounded to bfloat16.
+    Returns (o [B, H, N], new stored states [B, H, N, N]) in float64."""
+    o, S = decode_step(states, r, w, k, v, a, b, n_threads)
+    return o, round_bf16(S)
+
+
 def prefill(states, cu_seqlens, r, w, k, v, a, b, n_threads: int = 1):
     """Ragged prefill: sequence s covers tokens cu_seqlens[s]..cu_seqlens[s+1].
 

@@ -78,12 +78,14 @@ struct IdTable {
 
 bool desc_valid(const wkv7_pool_desc *d) {
     return d && d->n_layers >= 1 && d->n_heads >= 1 && d->head_size >= 1 && d->n_slots >= 1 &&
-           d->n_snapshots >= 0;
+           d->n_snapshots >= 0 && (d->state_dtype == WKV7_F32 || d->state_dtype == WKV7_BF16);
 }
+
+size_t state_elem_bytes(const wkv7_pool_desc *d) { return d->state_dtype == WKV7_BF16 ? 2 : 4; }
 
 size_t slot_bytes_of(const wkv7_pool_desc *d) {
     return static_cast<size_t>(d->n_layers) * static_cast<size_t>(d->n_heads) *
-           static_cast<size_t>(d->head_size) * static_cast<size_t>(d->head_size) * sizeof(float);
+           static_cast<size_t>(d->head_size) * static_cast<size_t>(d->head_size) * state_elem_bytes(d);
 }
 
 }  // namespace
@@ -95,7 +97,8 @@ struct wkv7_pool {
     int32_t *status = nullptr;
     float *states = nullptr;
     float *snaps = nullptr;
-    long long slot_floats = 0;
+    long long slot_floats = 0;  // slot bytes / 4: the unit of the byte-copy verbs
+    bool state_bf16 = false;
     std::mutex mu;
     IdTable slots;
     IdTable snapshots;
@@ -105,8 +108,8 @@ namespace {
 
 wkv7::LayerView layer_view(wkv7_pool *p, int32_t layer) {
     wkv7::LayerView lv;
-    lv.states = p->states;
-    lv.slot_stride = p->slot_floats;
+    lv.states = p->states;  // strides below count state elements (float32 or bf16)
+    lv.slot_stride = p->state_bf16 ? 2 * p->slot_floats : p->slot_floats;
     lv.layer_off = static_cast<long long>(layer) * p->desc.n_heads * wkv7::kHeadFloats;
     lv.n_slots = p->desc.n_slots;
     lv.n_heads = p->desc.n_heads;
@@ -171,6 +174,7 @@ wkv7_status wkv7_pool_create(const wkv7_pool_desc *desc, wkv7_pool **out) {
     p->status = reinterpret_cast<int32_t *>(p->base);
     p->states = reinterpret_cast<float *>(p->base + kHeaderBytes);
     p->slot_floats = static_cast<long long>(slot_bytes_of(desc) / sizeof(float));
+    p->state_bf16 = desc->state_dtype == WKV7_BF16;
     p->snaps = p->states + static_cast<size_t>(p->slot_floats) * static_cast<size_t>(desc->n_slots);
     try {
         p->slots.init(desc->n_slots);
@@ -212,8 +216,9 @@ wkv7_status wkv7_pool_state_ptr(wkv7_pool *pool, int32_t slot, int32_t layer, fl
     if (!pool || !dev_ptr) return WKV7_ERR_INVALID_ARG;
     if (layer < 0 || layer >= pool->desc.n_layers) return WKV7_ERR_INVALID_ARG;
     if (slot < 0 || slot >= pool->desc.n_slots) return WKV7_ERR_BAD_SLOT;
-    *dev_ptr = pool->states + static_cast<size_t>(slot) * static_cast<size_t>(pool->slot_floats) +
-               static_cast<size_t>(layer) * pool->desc.n_heads * wkv7::kHeadFloats;
+    *dev_ptr = reinterpret_cast<float *>(
+        reinterpret_cast<char *>(pool->states + static_cast<size_t>(slot) * static_cast<size_t>(pool->slot_floats)) +
+        static_cast<size_t>(layer) * pool->desc.n_heads * wkv7::kHeadFloats * state_elem_bytes(&pool->desc));
     return WKV7_OK;
 }
 
@@ -221,8 +226,9 @@ wkv7_status wkv7_pool_snapshot_ptr(wkv7_pool *pool, int32_t snap, int32_t layer,
     if (!pool || !dev_ptr) return WKV7_ERR_INVALID_ARG;
     if (layer < 0 || layer >= pool->desc.n_layers) return WKV7_ERR_INVALID_ARG;
     if (snap < 0 || snap >= pool->desc.n_snapshots) return WKV7_ERR_BAD_SLOT;
-    *dev_ptr = pool->snaps + static_cast<size_t>(snap) * static_cast<size_t>(pool->slot_floats) +
-               static_cast<size_t>(layer) * pool->desc.n_heads * wkv7::kHeadFloats;
+    *dev_ptr = reinterpret_cast<float *>(
+        reinterpret_cast<char *>(pool->snaps + static_cast<size_t>(snap) * static_cast<size_t>(pool->slot_floats)) +
+        static_cast<size_t>(layer) * pool->desc.n_heads * wkv7::kHeadFloats * state_elem_bytes(&pool->desc));
     return WKV7_OK;
 }
 
@@ -392,6 +398,7 @@ wkv7_status wkv7_decode_step(wkv7_pool *pool, int32_t layer, const int32_t *slot
     da.slot_ids = slot_ids_dev;
     da.n = n;
     da.in = {r, w, k, v, a, b, in_dtype == WKV7_BF16, o};
+    da.state_bf16 = pool->state_bf16;
     int launches = 0;
     cudaError_t e = wkv7::launch_decode(da, stream, &launches);
     return cuda_status("decode_step", e, launches);
@@ -405,6 +412,7 @@ wkv7_status wkv7_decode_multi(wkv7_pool *pool, int32_t layer, const int32_t *slo
     if (!pool || layer < 0 || layer >= pool->desc.n_layers || n < 0 || n_tokens < 1)
         return WKV7_ERR_INVALID_ARG;
     if (!dtype_valid(in_dtype)) return WKV7_ERR_INVALID_ARG;
+    if (pool->state_bf16) return WKV7_ERR_UNSUPPORTED;  // float32 states only
     if (n > pool->desc.n_slots) return WKV7_ERR_INVALID_ARG;
     if (n == 0) return WKV7_OK;
     if (!slot_ids_dev || !inputs_present(r, w, k, v, a, b, o)) return WKV7_ERR_INVALID_ARG;
@@ -434,6 +442,7 @@ static wkv7_status prefill_common(wkv7_pool *pool, int32_t layer, const int32_t 
     if (!pool || layer < 0 || layer >= pool->desc.n_layers) return WKV7_ERR_INVALID_ARG;
     if (n_seqs < 0 || total_tokens < 0 || max_seqlen < 0) return WKV7_ERR_INVALID_ARG;
     if (!dtype_valid(in_dtype)) return WKV7_ERR_INVALID_ARG;
+    if (pool->state_bf16) return WKV7_ERR_UNSUPPORTED;  // float32 states only
     if (n_seqs > pool->desc.n_slots) return WKV7_ERR_INVALID_ARG;
     if (max_seqlen > total_tokens) return WKV7_ERR_BAD_SEQLENS;
     if (n_seqs == 0) return WKV7_OK;

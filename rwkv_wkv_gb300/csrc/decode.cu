@@ -13,6 +13,8 @@
 // of contiguous memory.  A row's 64 columns sit in one half-warp, so both
 // row reductions (S a before the update, S' r after it) are 4-level xor
 // shuffles inside the half-warp, and the state never touches shared memory.
+#include <cuda_bf16.h>
+
 #include "device_common.cuh"
 #include "wkv7_internal.h"
 
@@ -83,6 +85,97 @@ __global__ void __launch_bounds__(256) decode_kernel(DecodeArgs p) {
     }
 }
 
+// Decode over a pool whose states are stored in bf16 (half the bytes of the
+// float32 kernel's traffic): the step is computed in float32 from the widened
+// state and the new state is rounded to bf16 (nearest even) on the way back;
+// the readout o = S' r is taken from the unrounded float32 S'.  One CTA of
+// 512 / kBf16Rows threads advances one (batch row, head) unit: thread t holds
+// key columns 8*(t%8)..+7 (16 bytes) of value rows t/8 + (64/kBf16Rows)*m,
+// m < kBf16Rows, and issues all its loads first.  Every CTA load/store
+// instruction covers contiguous memory, and a row's 64 columns sit in 8
+// consecutive lanes, so both row reductions are 3-level xor shuffles.
+constexpr int kBf16Rows = 4;  // value rows per thread (4: 128-thread CTAs, best measured of 2, 4, 8)
+constexpr int kBf16Threads = 8 * kHeadSize / kBf16Rows;
+constexpr int kBf16RowStep = kHeadSize / kBf16Rows;
+
+template <bool BF16>
+__global__ void __launch_bounds__(kBf16Threads) decode_bf16state_kernel(DecodeArgs p) {
+    const int H = p.lv.n_heads;
+    const int unit = blockIdx.x;
+    const int bi = unit / H;
+    const int h = unit - bi * H;
+    const int slot = __ldg(p.slot_ids + bi);
+    if (slot < 0 || slot >= p.lv.n_slots) {
+        if (threadIdx.x == 0) flag_status(p.lv.status, WKV7_DEV_BAD_SLOT);
+        return;
+    }
+    uint16_t *S = reinterpret_cast<uint16_t *>(p.lv.states) + static_cast<size_t>(slot) * p.lv.slot_stride +
+                  p.lv.layer_off + static_cast<size_t>(h) * kHeadFloats;
+    const int tid = threadIdx.x;
+    const int c = (tid & 7) * 8;  // first key column held by this thread
+    const int row0 = tid >> 3;    // value rows row0 + kBf16RowStep*m
+
+    uint4 raw[kBf16Rows];
+#pragma unroll
+    for (int m = 0; m < kBf16Rows; ++m)
+        raw[m] = __ldcs(reinterpret_cast<const uint4 *>(S + (row0 + kBf16RowStep * m) * kHeadSize + c));
+
+    const size_t io = static_cast<size_t>(unit) * kHeadSize;
+    float a8[8], w8[8], b8[8], k8[8], r8[8];
+    load8<BF16>(p.in.a, io + c, a8);
+    load8<BF16>(p.in.w, io + c, w8);
+    load8<BF16>(p.in.b, io + c, b8);
+    load8<BF16>(p.in.k, io + c, k8);
+    load8<BF16>(p.in.r, io + c, r8);
+
+    float hs[kBf16Rows], vv[kBf16Rows];
+#pragma unroll
+    for (int m = 0; m < kBf16Rows; ++m) {  // delta read on the old state: h_i = sum_j S_ij a_j
+        vv[m] = load1<BF16>(p.in.v, io + row0 + kBf16RowStep * m);
+        const uint32_t q[4] = {raw[m].x, raw[m].y, raw[m].z, raw[m].w};
+        float acc = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            acc = fmaf(bf16_lo(q[e]), a8[2 * e], acc);
+            acc = fmaf(bf16_hi(q[e]), a8[2 * e + 1], acc);
+        }
+        hs[m] = acc;
+    }
+#pragma unroll
+    for (int off = 4; off >= 1; off >>= 1)
+#pragma unroll
+        for (int m = 0; m < kBf16Rows; ++m) hs[m] += __shfl_xor_sync(0xffffffffu, hs[m], off);
+
+    // decay, delta write, kv write; the readout on the unrounded new state
+    float os[kBf16Rows];
+#pragma unroll
+    for (int m = 0; m < kBf16Rows; ++m) {
+        const uint32_t q[4] = {raw[m].x, raw[m].y, raw[m].z, raw[m].w};
+        uint32_t outw[4];
+        float acc = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float x0 = fmaf(bf16_lo(q[e]), w8[2 * e], fmaf(hs[m], b8[2 * e], vv[m] * k8[2 * e]));
+            const float x1 =
+                fmaf(bf16_hi(q[e]), w8[2 * e + 1], fmaf(hs[m], b8[2 * e + 1], vv[m] * k8[2 * e + 1]));
+            acc = fmaf(x0, r8[2 * e], acc);
+            acc = fmaf(x1, r8[2 * e + 1], acc);
+            outw[e] = pack_bf16_rn(x0, x1);
+        }
+        os[m] = acc;
+        __stcs(reinterpret_cast<uint4 *>(S + (row0 + kBf16RowStep * m) * kHeadSize + c),
+               make_uint4(outw[0], outw[1], outw[2], outw[3]));
+    }
+#pragma unroll
+    for (int off = 4; off >= 1; off >>= 1)
+#pragma unroll
+        for (int m = 0; m < kBf16Rows; ++m) os[m] += __shfl_xor_sync(0xffffffffu, os[m], off);
+    if ((tid & 7) == 0) {
+#pragma unroll
+        for (int m = 0; m < kBf16Rows; ++m) p.in.o[io + row0 + kBf16RowStep * m] = os[m];
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s, int *launches) {
@@ -90,10 +183,16 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s, int *launches) {
     if (units <= 0) return cudaSuccess;
     if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
     dim3 grid(static_cast<unsigned>(units));
-    if (a.in.bf16)
+    if (a.state_bf16) {
+        if (a.in.bf16)
+            decode_bf16state_kernel<true><<<grid, kBf16Threads, 0, s>>>(a);
+        else
+            decode_bf16state_kernel<false><<<grid, kBf16Threads, 0, s>>>(a);
+    } else if (a.in.bf16) {
         decode_kernel<true><<<grid, 256, 0, s>>>(a);
-    else
+    } else {
         decode_kernel<false><<<grid, 256, 0, s>>>(a);
+    }
     ++*launches;
     return cudaGetLastError();
 }

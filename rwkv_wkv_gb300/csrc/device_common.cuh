@@ -3,6 +3,7 @@
 
 #include <cstdint>
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "wkv7.h"
@@ -12,6 +13,12 @@ namespace wkv7 {
 // Record a device fault in the sticky status word; the first fault wins.
 __device__ __forceinline__ void flag_status(int *status, int code) {
     atomicCAS(status, 0, code);
+}
+
+// Two floats -> a bf16 pair (low, high), each rounded to nearest even.
+__device__ __forceinline__ uint32_t pack_bf16_rn(float lo, float hi) {
+    __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&p);
 }
 
 // bf16 bits -> float (exact).

@@ -27,10 +27,11 @@ struct TokenInputs {
 };
 
 struct DecodeArgs {
-    LayerView lv;
+    LayerView lv;  // for a bf16-state pool, states/slot_stride/layer_off count bf16 elements
     const int *slot_ids;
     int n;
     TokenInputs in;
+    bool state_bf16;
 };
 
 // K consecutive tokens per slot: inputs and o are [n][K][H][64]; with

@@ -41,7 +41,7 @@ class PoolDesc(ctypes.Structure):
     _fields_ = [("n_layers", ctypes.c_int32), ("n_heads", ctypes.c_int32),
                 ("head_size", ctypes.c_int32), ("n_slots", ctypes.c_int32),
                 ("n_snapshots", ctypes.c_int32), ("device_buffer", ctypes.c_void_p),
-                ("buffer_bytes", ctypes.c_size_t)]
+                ("buffer_bytes", ctypes.c_size_t), ("state_dtype", ctypes.c_int32)]
 
 
 # name -> (restype, argtypes)
@@ -144,18 +144,23 @@ class Pool:
     """A pool of fixed-size WKV-7 state slots on one GPU.
 
     States live in one torch-allocated device buffer: ``states`` is a float32
-    view [n_slots, n_layers, n_heads, 64, 64] and ``snapshots`` the same for
-    the parked copies (S[i][j]: i = value row, j = key column).
+    (or, with state_dtype="bf16", bfloat16) view [n_slots, n_layers, n_heads,
+    64, 64] and ``snapshots`` the same for the parked copies (S[i][j]: i =
+    value row, j = key column).
     """
 
     def __init__(self, n_layers: int, n_heads: int, n_slots: int, n_snapshots: int = 0,
-                 head_size: int = HEAD_SIZE, device=None):
+                 head_size: int = HEAD_SIZE, device=None, state_dtype: str = "f32"):
         self._lib = load_library()
         self.device = torch.device("cuda", torch.cuda.current_device()) if device is None \
             else torch.device(device)
         self.n_layers, self.n_heads, self.head_size = n_layers, n_heads, head_size
         self.n_slots, self.n_snapshots = n_slots, n_snapshots
-        desc = PoolDesc(n_layers, n_heads, head_size, n_slots, n_snapshots, None, 0)
+        if state_dtype not in ("f32", "bf16"):
+            raise ValueError("state_dtype must be 'f32' or 'bf16'")
+        self.state_dtype = state_dtype
+        desc = PoolDesc(n_layers, n_heads, head_size, n_slots, n_snapshots, None, 0,
+                        BF16 if state_dtype == "bf16" else F32)
         nbytes = self._lib.wkv7_pool_required_bytes(ctypes.byref(desc))
         if nbytes == 0:
             raise Wkv7Error(1, "Pool", "invalid description")
@@ -167,8 +172,9 @@ class Pool:
         _check(self._lib.wkv7_pool_create(ctypes.byref(desc), ctypes.byref(handle)), "pool_create")
         self._h = handle
         self.slot_bytes = int(self._lib.wkv7_slot_bytes(self._h))
-        per_slot = self.slot_bytes // 4
-        body = self.buffer[_HEADER_BYTES:].view(torch.float32)
+        tdt = torch.bfloat16 if state_dtype == "bf16" else torch.float32
+        per_slot = self.slot_bytes // tdt.itemsize
+        body = self.buffer[_HEADER_BYTES:].view(tdt)
         shape = (n_layers, n_heads, head_size, head_size)
         self.states = body[: n_slots * per_slot].view(n_slots, *shape)
         self.snapshots = body[n_slots * per_slot:(n_slots + n_snapshots) * per_slot].view(

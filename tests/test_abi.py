@@ -45,10 +45,10 @@ def test_version_and_strings(lib):
 
 
 def _desc(**kw):
-    d = dict(n_layers=2, n_heads=3, head_size=64, n_slots=8, n_snapshots=4)
+    d = dict(n_layers=2, n_heads=3, head_size=64, n_slots=8, n_snapshots=4, state_dtype=0)
     d.update(kw)
     return wkv7.PoolDesc(d["n_layers"], d["n_heads"], d["head_size"], d["n_slots"],
-                         d["n_snapshots"], None, 0)
+                         d["n_snapshots"], None, 0, d["state_dtype"])
 
 
 def _fake_pool(lib, **kw):
@@ -188,5 +188,35 @@ def test_snapshot_verbs_need_a_snapshot_store(lib):
     try:
         assert lib.wkv7_slot_snapshot(h, x, x, 1, None) == 1
         assert lib.wkv7_slot_restore(h, x, x, 1, None) == 1
+    finally:
+        lib.wkv7_pool_destroy(h)
+
+
+def test_bf16_state_pool(lib):
+    """A bf16-state pool: half the bytes per slot, state pointers step in bf16,
+    decode and the verbs are offered, the other recurrence calls are not."""
+    d16 = _desc(state_dtype=1)
+    d32 = _desc()
+    body32 = lib.wkv7_pool_required_bytes(ctypes.byref(d32)) - 256
+    assert lib.wkv7_pool_required_bytes(ctypes.byref(d16)) - 256 == body32 // 2
+    assert lib.wkv7_pool_required_bytes(ctypes.byref(_desc(state_dtype=2))) == 0
+    st, h = _fake_pool(lib, state_dtype=1)
+    assert st == 0
+    x = ctypes.c_void_p(FAKE_DEVICE_ADDR)
+    ins = [x] * 6
+    try:
+        sb = lib.wkv7_slot_bytes(h)
+        assert sb == 2 * 3 * 64 * 64 * 2
+        p00, p21 = ctypes.c_void_p(), ctypes.c_void_p()
+        assert lib.wkv7_pool_state_ptr(h, 0, 0, ctypes.byref(p00)) == 0
+        assert lib.wkv7_pool_state_ptr(h, 2, 1, ctypes.byref(p21)) == 0
+        assert p00.value == FAKE_DEVICE_ADDR + 256
+        assert p21.value - p00.value == 2 * sb + 3 * 64 * 64 * 2
+        assert lib.wkv7_prefill(h, 0, x, x, 1, 10, 10, 1, *ins, x, None) == 7
+        assert lib.wkv7_prefill_sequential(h, 0, x, x, 1, 10, 10, 1, *ins, x, None) == 7
+        assert lib.wkv7_decode_multi(h, 0, x, 1, 2, 1, *ins, x, None, None) == 7
+        assert lib.wkv7_decode_step(h, 0, x, 0, 1, *ins, x, None) == 0  # offered (empty: no-op)
+        desc = wkv7.PoolDesc()
+        assert lib.wkv7_pool_get_desc(h, ctypes.byref(desc)) == 0 and desc.state_dtype == 1
     finally:
         lib.wkv7_pool_destroy(h)

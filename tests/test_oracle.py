@@ -335,3 +335,62 @@ def test_pins_catch_planted_mistakes(golden_dir, mistake):
     expected_o = np.stack([g["o_t1"], g["o_t2"]])
     expected_S = np.stack([g["S2_0"], g["S2_1"]])
     assert not (np.array_equal(o, expected_o) and np.array_equal(S2, expected_S))
+
+
+# ------------------------------------------------ bf16 state storage (rounding)
+def test_round_bf16_hand_values():
+    """Values worked out from the bfloat16 format (8 significant bits, float32
+    exponent range): ties go to the even significand, the subnormal spacing is
+    2^-133, overflow goes to inf, and a value just above a tie rounds up even
+    where a detour through float32 would first land it on the tie."""
+    cases = [
+        (1.0, 1.0),
+        (1 + 2**-8, 1.0),                   # tie between 1 and 1 + 2^-7: even is 1
+        (1 + 3 * 2**-8, 1 + 2**-6),         # tie between 1 + 2^-7 (odd) and 1 + 2^-6 (even)
+        (1 + 2**-8 + 2**-30, 1 + 2**-7),    # above the tie (float32 would round to the tie)
+        (-(1 + 5 * 2**-9), -(1 + 2**-7)),   # 1.009765625 -> nearest is 1 + 2^-7
+        (1.5 * 2**-130, 1.5 * 2**-130),     # subnormal, a multiple of 2^-133
+        (2**-134, 0.0),                     # half the smallest subnormal: tie, to even (0)
+        (3 * 2**-134, 2 * 2**-133),         # tie between 2^-133 (odd) and 2^-132 (even)
+        (3.4e38, np.inf),
+        (-3.0e38, -(2**127) * (226 / 128)),  # 3.0e38 / 2^127 * 128 = 225.7 -> 226
+        (0.0, 0.0),
+    ]
+    x = np.array([c[0] for c in cases])
+    want = np.array([c[1] for c in cases])
+    got = oracle.round_bf16(x)
+    assert np.array_equal(got, want), list(zip(x, got, want))
+    assert np.isnan(oracle.round_bf16(np.array([np.nan]))[0])
+
+
+def test_round_bf16_matches_the_library_conversion_on_float32_values():
+    """On values that are exact in float32 the one-step rounding must equal the
+    library's float32 -> bfloat16 conversion (round to nearest even)."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(7)
+    x = (rng.standard_normal(200000) * np.exp2(rng.integers(-60, 60, 200000))).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(oracle.round_bf16(x.astype(np.float64)), ref)
+
+
+def test_bf16_state_decode_is_the_float64_step_then_rounding():
+    """The bf16-state step reads o from the unrounded state and stores the rounded
+    state: with w = 1, a = b = 0 and bf16 inputs whose products are exact in
+    8 bits, nothing needs rounding and it equals the plain step."""
+    rng = np.random.default_rng(3)
+    B, H, N = 2, 2, 8
+    S0 = oracle.round_bf16(rng.standard_normal((B, H, N, N)) * 0.25)
+    small = lambda: rng.integers(-3, 4, (B, H, N)).astype(np.float64)  # noqa: E731
+    r, k, v = small(), small(), small() * 0.0  # v = 0: S keeps its bf16 values
+    w = np.ones((B, H, N))
+    a = b = np.zeros((B, H, N))
+    o1, S1 = oracle.decode_step_bf16_state(S0, r, w, k, v, a, b)
+    o2, S2 = oracle.decode_step(S0, r, w, k, v, a, b)
+    assert np.array_equal(S1, S2) and np.array_equal(S1, S0)
+    assert np.allclose(o1, o2, rtol=0, atol=0)
+    # with rounding needed, the stored state is the rounded plain step and o is unrounded
+    v = rng.standard_normal((B, H, N))
+    o1, S1 = oracle.decode_step_bf16_state(S0, r, w, k, v, a, b)
+    o2, S2 = oracle.decode_step(S0, r, w, k, v, a, b)
+    assert np.array_equal(o1, o2)
+    assert np.array_equal(S1, oracle.round_bf16(S2)) and not np.array_equal(S1, S2)
