@@ -40,7 +40,9 @@
 //       those blocks (three steps of warp-level TF32 block products); T goes
 //       to shared memory in bf16
 //   G2  [Bhat^T; Qb^T] x T^T -> Z^T                  (M=128, N=64)
-//   G34 Z^T (in tensor memory) x [A0 | Mak^T] (MN-major) -> Phi'^T, R''^T, Y'^T
+//   G34 Z^T (in tensor memory) x [A0 | Mak^T] (MN-major), accumulated onto
+//       [diag(gamma) | Khat^T; R0 | Qk^T] (written into the accumulator during
+//       the inverse by warps that are idle then) -> Phi^T, Y_B^T, R'^T, Y_Q^T
 //                                                    (M=128, N=128)
 //   G5  [Phi^T; R'^T] x (S0_hi + S0_lo)^T + [Y_B^T; Y_Q^T] x V -> [S_L^T; O^T],
 //       both A operands in tensor memory, S0 split into bf16 hi + lo (B read
@@ -118,13 +120,15 @@ __device__ __forceinline__ int up_idx(int i, int j) { return i * (7 - i) / 2 + (
 constexpr uint32_t kSmemBytes = kSmallBytes + 1024 + kTileBytes;  // + worst-case alignment
 static_assert(2 * (kSmemBytes + 1024) <= 228 * 1024, "two CTAs per SM");
 constexpr uint32_t kTmemCols = 256;
-// Tensor-memory columns: G1 64-127 and G1' 128-255 (Q_k^T at 192-255 until the
-// G34 readback); G2 0-63; Z^T, the bf16 A operand of G34, 128-159; G34 0-127;
-// the bf16 A operands of G5, [Phi^T; R'^T] 128-159 and Y^T 160-191; G5 0-63,
-// read back while the next chunk's G1 and G1' run.
+// Tensor-memory columns: G1 64-127 and G1' 128-255 (Q_k^T at 192-255 until it
+// is moved into G34's accumulator); G34's accumulator 0-127, loaded with its
+// additive terms during the inverse; G2 128-191; Z^T, the bf16 A operand of
+// G34, 192-223; the bf16 A operands of G5, [Phi^T; R'^T] 128-159 and Y^T
+// 160-191; G5 0-63, read back while the next chunk's G1 and G1' run.
 // A bf16 A operand in tensor memory holds row m in lane m with K elements 2c,
 // 2c+1 packed in column c.
-constexpr uint32_t kColG1 = 64, kColG1p = 128, kColZA = 128, kColA2 = 128, kColYA = 160, kColQk = 192;
+constexpr uint32_t kColG1 = 64, kColG1p = 128, kColG2 = 128, kColZA = 192, kColA2 = 128, kColYA = 160,
+                   kColQk = 192;
 
 struct InputMaps {
     CUtensorMap m[6];  // r, w, k, v, a, b
@@ -476,6 +480,59 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
     };
 
+    // G34's additive terms, written into its accumulator (columns 0-127) before
+    // it runs, so that G34 accumulates onto them: rows j (warps 4, 5) get
+    // diag(gamma) and Khat^T, rows t' (warps 6, 7) R0 and the causal part of
+    // Q_k^T (s <= t'), taken from G1'.
+    auto preload_g34_rows_j = [&]() {
+        const int j = row;
+        const float gj = gam[j];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            uint32_t r[16];
+#pragma unroll
+            for (int q = 0; q < 16; ++q) r[q] = __float_as_uint(16 * g + q == j ? gj : 0.f);
+            tmem_st16(tmem + lane_base + 16 * g, r);
+        }
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            float add[16];
+            uint32_t r[16];
+            load_row16(base + OFF_KHT, j, 16 * g, add);
+#pragma unroll
+            for (int q = 0; q < 16; ++q) r[q] = __float_as_uint(add[q]);
+            tmem_st16(tmem + lane_base + 64 + 16 * g, r);
+        }
+        tmem_st_wait();
+    };
+    auto preload_g34_rows_t = [&]() {
+        const int tq = row - 64;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            float add[16];
+            uint32_t r[16];
+            load_row16(base + OFF_R0, tq, 16 * g, add);
+#pragma unroll
+            for (int q = 0; q < 16; ++q) r[q] = __float_as_uint(add[q]);
+            tmem_st16(tmem + lane_base + 16 * g, r);
+        }
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            float qk[32];
+            tmem_ld32(tmem + lane_base + kColQk + 32 * hh, qk);
+            tmem_ld_wait();
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+                uint32_t r[16];
+#pragma unroll
+                for (int q = 0; q < 16; ++q)
+                    r[q] = __float_as_uint(32 * hh + 16 * g + q <= tq ? qk[16 * g + q] : 0.f);
+                tmem_st16(tmem + lane_base + 64 + 32 * hh + 16 * g, r);
+            }
+        }
+        tmem_st_wait();
+    };
+
     for (int c = 0; c < n_chunks; ++c) {
         const int tc0 = t0 + c * kL;
         const int Lc = min(kL, t1 - tc0);
@@ -766,6 +823,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
             bar_sync_named(2, 192);
             // step 3: T_02 = R_02 T_22, T_13 = R_13 T_33, T_03 = R_02 T_23 + R_03 T_33
+            if (warp >= 4) preload_g34_rows_j();  // idle in this step
             if (warp < 3) {
                 float acc3[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
                 if (warp == 0) {
@@ -785,14 +843,17 @@ __global__ void __launch_bounds__(kThreads, 2)
                         pack_bf16(acc3[h][2], acc3[h][3]);
                 }
             }
+        } else {
+            preload_g34_rows_t();  // warps 6, 7 take no part in the inverse
         }
+        tc_fence_before();
         fence_proxy_async_smem();
         __syncthreads();
 
         // ------------------------------------------------------------- G2
         if (tid == 0) {
             tc_fence_after();
-            umma_128xNx64(tmem + 0, smem_addr(base + OFF_G2A), smem_addr(base + OFF_G2B), 64, false);
+            umma_128xNx64(tmem + kColG2, smem_addr(base + OFF_G2A), smem_addr(base + OFF_G2B), 64, false);
             umma_commit(bar_mma);
         }
         mma_wait(bar_mma, ph_mma, flag);
@@ -801,7 +862,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         tc_fence_after();
         {  // Z^T row (this thread's 32 columns) -> bf16 A operand of G34 in tensor memory
             float v[32];
-            tmem_ld32(tmem + lane_base + cpart, v);
+            tmem_ld32(tmem + lane_base + kColG2 + cpart, v);
             tmem_ld_wait();
             uint32_t pk[16];
 #pragma unroll
@@ -816,54 +877,25 @@ __global__ void __launch_bounds__(kThreads, 2)
         // ------------------------------------------------------------ G34
         if (tid == 0) {
             tc_fence_after();
-            umma_ta_128xNx64(tmem + 0, tmem + kColZA, smem_addr(base + OFF_G34B), 128, false, true);
+            // accumulates onto the additive terms loaded during the inverse
+            umma_ta_128xNx64(tmem + 0, tmem + kColZA, smem_addr(base + OFF_G34B), 128, true, true);
             umma_commit(bar_mma);
         }
         mma_wait(bar_mma, ph_mma, flag);
         ph_mma ^= 1;
         tc_fence_after();
-        {  // -> the bf16 A operands of G5 in tensor memory: [Phi^T; R'^T] and [Y_B^T; Y_Q^T]
+        {  // [Phi^T; R'^T] and [Y_B^T; Y_Q^T] rows -> the bf16 A operands of G5 in tensor memory
             float v[32], y[32];
             tmem_ld32(tmem + lane_base + cpart, v);
             tmem_ld32(tmem + lane_base + 64 + cpart, y);
             tmem_ld_wait();
-            {
-                uint32_t pa[16];
-                if (row < 64) {  // row j: Phi^T = Phi'^T + diag(gamma)
-                    const float gj = gam[row];
+            uint32_t pa[16], py[16];
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) v[q] += (cpart + q == row) ? gj : 0.f;
-                } else {  // row t': R'^T = R''^T + R0
-#pragma unroll
-                    for (int g = 0; g < 2; ++g) {
-                        float add[16];
-                        load_row16(base + OFF_R0, row - 64, cpart + 16 * g, add);
-#pragma unroll
-                        for (int q = 0; q < 16; ++q) v[16 * g + q] += add[q];
-                    }
-                }
-#pragma unroll
-                for (int e = 0; e < 16; ++e) pa[e] = pack_bf16(v[2 * e], v[2 * e + 1]);
-                tmem_st16(tmem + lane_base + kColA2 + cpart / 2, pa);
-                tmem_st_wait();
+            for (int e = 0; e < 16; ++e) {
+                pa[e] = pack_bf16(v[2 * e], v[2 * e + 1]);
+                py[e] = pack_bf16(y[2 * e], y[2 * e + 1]);
             }
-            if (row < 64) {  // row j: Y_B^T = Y'^T + Khat^T
-#pragma unroll
-                for (int g = 0; g < 2; ++g) {
-                    float add[16];
-                    load_row16(base + OFF_KHT, row, cpart + 16 * g, add);
-#pragma unroll
-                    for (int q = 0; q < 16; ++q) y[16 * g + q] += add[q];
-                }
-            } else {  // row t': Y_Q^T = Y'^T + Qk^T (causal: s <= t')
-                tmem_ld32(tmem + lane_base + kColQk + cpart, v);
-                tmem_ld_wait();
-#pragma unroll
-                for (int q = 0; q < 32; ++q) y[q] += (cpart + q <= row - 64) ? v[q] : 0.f;
-            }
-            uint32_t py[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) py[e] = pack_bf16(y[2 * e], y[2 * e + 1]);
+            tmem_st16(tmem + lane_base + kColA2 + cpart / 2, pa);
             tmem_st16(tmem + lane_base + kColYA + cpart / 2, py);
             tmem_st_wait();
         }
