@@ -215,12 +215,16 @@ wkv7_status wkv7_slot_resume(wkv7_pool *pool, const void *host_src, size_t host_
 
 /* --------------------------------------------------------- recurrence ---- */
 
+/* Every call in this section reads its inputs and writes o with vector loads
+ * and stores, so the six input bases and o must be 16-byte aligned; a base
+ * that is not is reported as UNSUPPORTED before any launch. */
+
 /* decode: one token for each of n slots at one layer.  For b < n and every
  * head h, the state at (slot_ids_dev[b], layer, h) takes one step of the
  * recurrence with inputs x[b][h][:] (x = r, w, k, v, a, b; [n][n_heads][64],
  * dtype in_dtype) and o[b][h][:] (float32) receives the readout.  The state is
  * read once and written once.  Errors: INVALID_ARG (including n > n_slots),
- * UNSUPPORTED, CUDA.  Device: WKV7_DEV_BAD_SLOT for an out-of-range id (that
+ * UNSUPPORTED (a misaligned base), CUDA.  Device: WKV7_DEV_BAD_SLOT for an out-of-range id (that
  * row's state and o are untouched). */
 wkv7_status wkv7_decode_step(wkv7_pool *pool, int32_t layer, const int32_t *slot_ids_dev,
                              int32_t n, wkv7_dtype in_dtype, const void *r, const void *w,
@@ -261,7 +265,7 @@ wkv7_status wkv7_decode_multi(wkv7_pool *pool, int32_t layer, const int32_t *slo
  * 64 tokens anchored at each sequence's first token, with bf16 tensor-core
  * operands and a float32 state carried between chunks.  max_seqlen bounds
  * every sequence length.  Errors: INVALID_ARG, UNSUPPORTED (in_dtype must be
- * WKV7_BF16; the six input bases must be 16-byte aligned), CUDA.  Device:
+ * WKV7_BF16; a misaligned base), CUDA.  Device:
  * WKV7_DEV_BAD_SLOT, WKV7_DEV_BAD_SEQLENS (that sequence is skipped),
  * WKV7_DEV_DECAY_RANGE (the decay over half a chunk, 32 tokens, exceeds
  * 2^120 in some channel: that sequence's results are not reliable),

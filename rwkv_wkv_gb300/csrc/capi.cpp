@@ -124,6 +124,17 @@ bool inputs_present(const void *r, const void *w, const void *k, const void *v, 
     return r && w && k && v && a && b && o;
 }
 
+// The recurrence kernels read inputs and write o with 8- to 32-byte vector
+// accesses (the chunked prefill's tensor maps also need 16-byte bases); every
+// access offset is a multiple of 16 bytes from its base.
+bool inputs_aligned(const void *r, const void *w, const void *k, const void *v, const void *a,
+                    const void *b, const float *o) {
+    const void *x[7] = {r, w, k, v, a, b, o};
+    for (const void *p : x)
+        if (reinterpret_cast<uintptr_t>(p) % 16 != 0) return false;
+    return true;
+}
+
 }  // namespace
 
 extern "C" {
@@ -393,6 +404,7 @@ wkv7_status wkv7_decode_step(wkv7_pool *pool, int32_t layer, const int32_t *slot
     if (n > pool->desc.n_slots) return WKV7_ERR_INVALID_ARG;
     if (n == 0) return WKV7_OK;
     if (!slot_ids_dev || !inputs_present(r, w, k, v, a, b, o)) return WKV7_ERR_INVALID_ARG;
+    if (!inputs_aligned(r, w, k, v, a, b, o)) return WKV7_ERR_UNSUPPORTED;
     wkv7::DecodeArgs da;
     da.lv = layer_view(pool, layer);
     da.slot_ids = slot_ids_dev;
@@ -416,6 +428,7 @@ wkv7_status wkv7_decode_multi(wkv7_pool *pool, int32_t layer, const int32_t *slo
     if (n > pool->desc.n_slots) return WKV7_ERR_INVALID_ARG;
     if (n == 0) return WKV7_OK;
     if (!slot_ids_dev || !inputs_present(r, w, k, v, a, b, o)) return WKV7_ERR_INVALID_ARG;
+    if (!inputs_aligned(r, w, k, v, a, b, o)) return WKV7_ERR_UNSUPPORTED;
     if (step_snap_ids_dev && pool->desc.n_snapshots == 0) return WKV7_ERR_INVALID_ARG;
     if (static_cast<long long>(n) * n_tokens > 0x7fffffffLL) return WKV7_ERR_INVALID_ARG;
     wkv7::DecodeMultiArgs da;
@@ -449,11 +462,7 @@ static wkv7_status prefill_common(wkv7_pool *pool, int32_t layer, const int32_t 
     if (!slot_ids_dev || !cu_seqlens_dev) return WKV7_ERR_INVALID_ARG;
     if (total_tokens > 0 && !inputs_present(r, w, k, v, a, b, o)) return WKV7_ERR_INVALID_ARG;
     if (chunked && in_dtype != WKV7_BF16) return WKV7_ERR_UNSUPPORTED;
-    if (chunked && total_tokens > 0) {  // tensor-map loads need 16-byte aligned bases
-        const void *ins[6] = {r, w, k, v, a, b};
-        for (const void *x : ins)
-            if (reinterpret_cast<uintptr_t>(x) % 16 != 0) return WKV7_ERR_UNSUPPORTED;
-    }
+    if (total_tokens > 0 && !inputs_aligned(r, w, k, v, a, b, o)) return WKV7_ERR_UNSUPPORTED;
     wkv7::PrefillArgs pa;
     pa.lv = layer_view(pool, layer);
     pa.slot_ids = slot_ids_dev;

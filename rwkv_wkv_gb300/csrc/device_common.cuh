@@ -63,6 +63,14 @@ __device__ __forceinline__ void load8(const void *p, size_t off, float *x) {
     }
 }
 
+// Eight floats to global memory in one 32-byte store (sm_100 and later); p must
+// be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(float *p, const float *v) {
+    asm volatile("st.global.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "f"(v[0]), "f"(v[1]),
+                 "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7])
+                 : "memory");
+}
+
 __device__ __forceinline__ float dot4(float4 a, float4 b) {
     return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
 }

@@ -423,6 +423,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int cpart = 32 * (warp >> 2);      // this thread's 32-column part of each 64-column group
 
     const int n_chunks = (len + kL - 1) / kL;
+    // Every output row starts a multiple of 128 bytes past o (which the host
+    // checks is 16-byte aligned), so o's own alignment decides the store width.
+    const bool o_v8 = (reinterpret_cast<uintptr_t>(p.in.o) & 31u) == 0;
     uint32_t ph_mma = 0, ph_in = 0;
     bool range_bad = false;
     int prev_c = 0, prev_tc0 = 0, prev_Lc = 0;  // chunk whose state product awaits its readback
@@ -438,11 +441,16 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (row >= 64) {  // O row t' -> o[otc0 + t'][h][cpart ..]
             const int tq = row - 64;
             float *dst = p.in.o + (static_cast<size_t>(otc0 + tq) * H + h) * kHeadSize + cpart;
-            if (tq < oLc) {
+            if (tq < oLc) {  // 128 bytes per thread: 32-byte stores when o allows them
+                if (o_v8) {
 #pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    reinterpret_cast<float4 *>(dst)[q] =
-                        make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                    for (int q = 0; q < 4; ++q) st_global_v8(dst + 8 * q, v + 8 * q);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        reinterpret_cast<float4 *>(dst)[q] =
+                            make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                }
             }
         } else {  // S_L^T row j (values i of this thread's part)
             const int j = row;

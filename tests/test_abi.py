@@ -158,6 +158,15 @@ def test_host_checks_return_before_launch(lib):
         assert lib.wkv7_prefill(h, 0, x, x, 9, 10, 10, 1, *ins, x, None) == 1
         assert lib.wkv7_prefill(h, 0, x, x, 0, 0, 0, 1, *ins, x, None) == 0
         assert lib.wkv7_prefill_sequential(h, 3, x, x, 1, 10, 10, 0, *ins, x, None) == 1
+        # every input base and o 16-byte aligned, on every recurrence call
+        odd = ctypes.c_void_p(FAKE_DEVICE_ADDR + 8)
+        for bad in range(7):
+            args = [odd if i == bad else x for i in range(7)]
+            assert lib.wkv7_decode_step(h, 0, x, 1, 1, *args, None) == 7
+            assert lib.wkv7_decode_multi(h, 0, x, 1, 2, 1, *args, None, None) == 7
+            assert lib.wkv7_prefill(h, 0, x, x, 1, 10, 10, 1, *args, None) == 7
+            assert lib.wkv7_prefill_sequential(h, 0, x, x, 1, 10, 10, 0, *args, None) == 7
+        assert lib.wkv7_prefill(h, 0, x, x, 0, 0, 0, 1, *ins, odd, None) == 0  # nothing to write
         # verbs
         assert lib.wkv7_slot_fork(h, None, x, 1, None) == 1
         assert lib.wkv7_slot_snapshot(h, x, x, -1, None) == 1

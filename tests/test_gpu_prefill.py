@@ -202,3 +202,29 @@ def test_chunked_prefill_is_deterministic():
             runs.append((o, pool.states.cpu().numpy()))
     np.testing.assert_array_equal(runs[0][0], runs[1][0])
     np.testing.assert_array_equal(runs[0][1], runs[1][1])
+
+
+def test_output_alignment_does_not_change_results():
+    """o 32-byte aligned takes 32-byte stores, o only 16-byte aligned 16-byte
+    ones; both write the same bits."""
+    H = 4
+    lengths = [130, 64, 7]
+    cu = wl.cu_seqlens(lengths)
+    ins = wl.token_inputs(41, "prefill/align", int(cu[-1]), H, 64, dtype="bf16")
+    S0 = wl.slot_states(41, "prefill/align/s0", range(3), 1, H, 64)[:, 0]
+    dev = dev_inputs(ins, "bf16")
+    outs, states = [], []
+    for shift in (0, 4):  # floats: 0 -> 256-byte aligned, 4 -> 16 bytes past it
+        buf = torch.full((int(cu[-1]) * H * 64 + 8,), float("nan"), device="cuda")
+        o = buf[shift:shift + int(cu[-1]) * H * 64].view(int(cu[-1]), H, 64)
+        assert o.data_ptr() % 32 == (0 if shift == 0 else 16)
+        with Pool(1, H, 3) as pool:
+            pool.states[:, 0] = torch.from_numpy(S0).cuda()
+            pool.prefill(0, i32([0, 1, 2]), i32(cu), *dev, o=o, max_seqlen=max(lengths))
+            assert pool.device_status() == 0
+            states.append(pool.states.clone())
+        outs.append(o.clone())
+        assert bool(torch.isnan(buf[:shift]).all()) and bool(torch.isnan(buf[shift + o.numel():]).all())
+    assert torch.equal(outs[0], outs[1]) and torch.equal(states[0], states[1])
+    o_ref, _ = oracle.prefill(S0.astype(np.float64), cu, *host_inputs(ins))
+    assert rel(outs[1].cpu().numpy(), o_ref) < PREFILL_TOL
