@@ -66,7 +66,7 @@ def parse_args(argv=None):
     p.add_argument("--no-rollback", action="store_true",
                    help="verify workload: no per-token rollback states")
     p.add_argument("--state-dtype", choices=["f32", "bf16"], default="f32",
-                   help="sweep workload: state storage (bf16 halves the state bytes)")
+                   help="mixed and sweep workloads: state storage (bf16 halves the state bytes)")
     return p.parse_args(argv)
 
 
@@ -206,16 +206,19 @@ class Workload:
 class Mixed(Workload):
     name = wl.MIXED.name
 
-    def __init__(self, torch, device, seed=wl.MIXED.seed):
+    def __init__(self, torch, device, seed=wl.MIXED.seed, state_dtype="f32"):
         from rwkv_wkv_gb300 import Pool
         W = wl.MIXED
+        self.state_dtype = state_dtype
+        self.state_head_bytes = HEAD_BYTES_STATE // (2 if state_dtype == "bf16" else 1)
         self.torch, self.device = torch, device
         self.H, self.N = W.H, W.N
         plan = wl.mixed_plan(seed)
         self.plan = plan
         self.lengths = plan["lengths"].astype(np.int64)
         self.total = int(self.lengths.sum())
-        self.pool = Pool(1, W.H, W.n_slots, n_snapshots=wl.MIXED_VERB_N, device=device)
+        self.pool = Pool(1, W.H, W.n_slots, n_snapshots=wl.MIXED_VERB_N, device=device,
+                         state_dtype=state_dtype)
         g = torch.Generator(device=device).manual_seed(seed)
         self.pool.states.normal_(0.0, 0.1, generator=g)
         # slot table: every id in use except the prefill targets, which each
@@ -243,9 +246,9 @@ class Mixed(Workload):
         self.phase_bytes = {
             "create": wl.MIXED_PREFILL_SEQS * slot_bytes,
             "snapshot": 2 * nv * slot_bytes,
-            "decode": B * (W.H * 2 * HEAD_BYTES_STATE + in_row + out_row),
+            "decode": B * (W.H * 2 * self.state_head_bytes + in_row + out_row),
             "prefill": self.total * (in_row + out_row)
-            + wl.MIXED_PREFILL_SEQS * W.H * 2 * HEAD_BYTES_STATE,
+            + wl.MIXED_PREFILL_SEQS * W.H * 2 * self.state_head_bytes,
             "fork": 2 * nv * slot_bytes,
             "restore": 2 * nv * slot_bytes,
         }
@@ -283,11 +286,13 @@ class Mixed(Workload):
         return ins, [self.o_dec, self.o_pre]
 
     def config(self):
-        return {"workload": wl.MIXED.description, "pool_slots": wl.MIXED.n_slots,
+        return {"workload": wl.MIXED.description
+                + ("; bf16 state storage" if self.state_dtype == "bf16" else ""),
+                "pool_slots": wl.MIXED.n_slots,
                 "layers": 1, "heads": self.H, "head_size": self.N,
                 "decode_slots": wl.MIXED_DECODE_B, "prefill_seqs": wl.MIXED_PREFILL_SEQS,
                 "prefill_tokens": self.total, "verb_slots": wl.MIXED_VERB_N,
-                "state_dtype": "f32", "input_dtype": "bf16", "output_dtype": "f32"}
+                "state_dtype": self.state_dtype, "input_dtype": "bf16", "output_dtype": "f32"}
 
     def oracle_sample(self, frac_target: float):
         """Sample of the step for the CPU oracle: every decode row and prefill
@@ -600,7 +605,7 @@ class Hibernate(Workload):
 
 def make_workload(args, torch, device):
     if args.workload == "mixed":
-        return Mixed(torch, device)
+        return Mixed(torch, device, state_dtype=args.state_dtype)
     if args.workload == "decode12":
         return Decode12(torch, device)
     if args.workload == "prefill":
@@ -746,7 +751,8 @@ def run_ours(args):
                 "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
                 "peak_source": peaks["source"] + " (hbm copy)",
                 "bytes_per_launch": wk.phase_bytes[dom], "ms_per_launch": round(dom_ms, 4),
-                "traffic": profiled_traffic(dom, args.workload)}
+                "traffic": profiled_traffic(dom, args.workload)
+                if getattr(wk, "state_dtype", "f32") == "f32" else None}
     phases = {}
     for n in wk.phases:
         ms = phase_ms.get(n)

@@ -102,9 +102,15 @@ typedef struct {
                             bytes per slot and per decode step; each decode step
                             is computed in float32 and rounds the new state to bf16
                             (nearest even), the readout coming from the unrounded
-                            float32 state.  A bf16-state pool offers the slot table,
-                            every verb and wkv7_decode_step; the other recurrence
-                            calls return WKV7_ERR_UNSUPPORTED. */
+                            float32 state.  Every call works on a bf16-state pool,
+                            computing in float32 and rounding what it stores:
+                            wkv7_decode_multi is K such steps (rounded after every
+                            token; its rollback snapshots hold the rounded states);
+                            the prefill calls read the start state exactly, carry
+                            float32 inside a sequence and round the final state
+                            and every checkpoint, and at a checkpoint the carry
+                            continues from the rounded value, so that resuming from
+                            a checkpoint still reproduces the uninterrupted run. */
 } wkv7_pool_desc;
 
 /* ---------------------------------------------------------------- pool ---- */

@@ -424,7 +424,6 @@ wkv7_status wkv7_decode_multi(wkv7_pool *pool, int32_t layer, const int32_t *slo
     if (!pool || layer < 0 || layer >= pool->desc.n_layers || n < 0 || n_tokens < 1)
         return WKV7_ERR_INVALID_ARG;
     if (!dtype_valid(in_dtype)) return WKV7_ERR_INVALID_ARG;
-    if (pool->state_bf16) return WKV7_ERR_UNSUPPORTED;  // float32 states only
     if (n > pool->desc.n_slots) return WKV7_ERR_INVALID_ARG;
     if (n == 0) return WKV7_OK;
     if (!slot_ids_dev || !inputs_present(r, w, k, v, a, b, o)) return WKV7_ERR_INVALID_ARG;
@@ -440,6 +439,7 @@ wkv7_status wkv7_decode_multi(wkv7_pool *pool, int32_t layer, const int32_t *slo
     da.snaps = pool->snaps;
     da.n_snaps = pool->desc.n_snapshots;
     da.step_snap_ids = step_snap_ids_dev;
+    da.state_bf16 = pool->state_bf16;
     int launches = 0;
     cudaError_t e = wkv7::launch_decode_multi(da, stream, &launches);
     return cuda_status("decode_multi", e, launches);
@@ -455,7 +455,6 @@ static wkv7_status prefill_common(wkv7_pool *pool, int32_t layer, const int32_t 
     if (!pool || layer < 0 || layer >= pool->desc.n_layers) return WKV7_ERR_INVALID_ARG;
     if (n_seqs < 0 || total_tokens < 0 || max_seqlen < 0) return WKV7_ERR_INVALID_ARG;
     if (!dtype_valid(in_dtype)) return WKV7_ERR_INVALID_ARG;
-    if (pool->state_bf16) return WKV7_ERR_UNSUPPORTED;  // float32 states only
     if (n_seqs > pool->desc.n_slots) return WKV7_ERR_INVALID_ARG;
     if (max_seqlen > total_tokens) return WKV7_ERR_BAD_SEQLENS;
     if (n_seqs == 0) return WKV7_OK;
@@ -472,6 +471,7 @@ static wkv7_status prefill_common(wkv7_pool *pool, int32_t layer, const int32_t 
     pa.max_seqlen = max_seqlen;
     pa.in = {r, w, k, v, a, b, in_dtype == WKV7_BF16, o};
     pa.ck = {pool->snaps, pool->desc.n_snapshots, cu_ckpt_dev, ckpt_snap_ids_dev};
+    pa.state_bf16 = pool->state_bf16;
     int launches = 0;
     cudaError_t e = chunked ? wkv7::launch_prefill_chunked(pa, stream, &launches)
                             : wkv7::launch_prefill_sequential(pa, stream, &launches);

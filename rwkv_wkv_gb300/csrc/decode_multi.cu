@@ -20,12 +20,15 @@ namespace {
 // the token chain.  With per-token snapshots the state after every token is also
 // streamed to its snapshot (the rollback points of a speculative verify: the
 // rvLLM README, "Speculative decoding", verifies K+1 tokens in one pass; wkvm's
-// fork/restore verbs then keep or drop them).
+// fork/restore verbs then keep or drop them).  On a bf16-state pool (SBF16) the
+// call is K decode steps: the state is rounded to bf16 after every token, as a
+// single-token step stores it, and carried on rounded; the readout of each token
+// uses its unrounded state, and the rollback snapshots hold the rounded states.
 constexpr int kGroup = 8;  // tokens staged per pass
 enum { kR = 0, kW, kK, kV, kA, kB, kInputs };
 
-template <bool BF16, bool SNAPS>
-__global__ void __launch_bounds__(256, 5) decode_multi_kernel(DecodeMultiArgs p) {
+template <bool BF16, bool SNAPS, bool SBF16>
+__global__ void __launch_bounds__(256, (SNAPS && SBF16) ? 4 : 5) decode_multi_kernel(DecodeMultiArgs p) {
     __shared__ __align__(16) float xs[kGroup][kInputs][kHeadSize];
     const int H = p.lv.n_heads;
     const int unit = blockIdx.x;
@@ -36,8 +39,10 @@ __global__ void __launch_bounds__(256, 5) decode_multi_kernel(DecodeMultiArgs p)
         if (threadIdx.x == 0) flag_status(p.lv.status, WKV7_DEV_BAD_SLOT);
         return;
     }
-    float *S = p.lv.states + static_cast<size_t>(slot) * p.lv.slot_stride + p.lv.layer_off +
-               static_cast<size_t>(h) * kHeadFloats;
+    // element offset of this (slot, layer, head) state; elements are bf16 with SBF16
+    const size_t s_off = static_cast<size_t>(slot) * p.lv.slot_stride + p.lv.layer_off +
+                         static_cast<size_t>(h) * kHeadFloats;
+    float *S = p.lv.states + s_off;  // float32 states only
     const int tid = threadIdx.x;
     const int c = (tid & 15) * 4;
     const int row0 = tid >> 4;
@@ -45,8 +50,12 @@ __global__ void __launch_bounds__(256, 5) decode_multi_kernel(DecodeMultiArgs p)
 
     float4 s[4];
 #pragma unroll
-    for (int m = 0; m < 4; ++m)
-        s[m] = __ldcs(reinterpret_cast<const float4 *>(S + (row0 + 16 * m) * kHeadSize + c));
+    for (int m = 0; m < 4; ++m) {
+        if constexpr (SBF16)
+            s[m] = load_state4<true>(p.lv.states, s_off + (row0 + 16 * m) * kHeadSize + c);
+        else
+            s[m] = __ldcs(reinterpret_cast<const float4 *>(S + (row0 + 16 * m) * kHeadSize + c));
+    }
 
     // token k of row bi, head h: [(bi*K + k)*H + h][64]
     auto io_of = [&](int k) { return (static_cast<size_t>(bi) * K + k) * H * kHeadSize + h * kHeadSize; };
@@ -89,15 +98,23 @@ __global__ void __launch_bounds__(256, 5) decode_multi_kernel(DecodeMultiArgs p)
                 s[m].z = fmaf(s[m].z, w4.z, fmaf(hs[m], b4.z, vm * k4.z));
                 s[m].w = fmaf(s[m].w, w4.w, fmaf(hs[m], b4.w, vm * k4.w));
                 os[m] = dot4(s[m], r4);
+                if constexpr (SBF16)
+                    s[m] = make_float4(round_bf16(s[m].x), round_bf16(s[m].y), round_bf16(s[m].z),
+                                       round_bf16(s[m].w));
             }
             if (SNAPS) {
                 const int id = __ldg(p.step_snap_ids + static_cast<size_t>(bi) * K + k);
                 if (id >= 0 && id < p.n_snaps) {
-                    float *D = p.snaps + static_cast<size_t>(id) * p.lv.slot_stride + p.lv.layer_off +
-                               static_cast<size_t>(h) * kHeadFloats;
+                    const size_t d_off = static_cast<size_t>(id) * p.lv.slot_stride + p.lv.layer_off +
+                                         static_cast<size_t>(h) * kHeadFloats;
 #pragma unroll
-                    for (int m = 0; m < 4; ++m)
-                        __stcs(reinterpret_cast<float4 *>(D + (row0 + 16 * m) * kHeadSize + c), s[m]);
+                    for (int m = 0; m < 4; ++m) {
+                        if constexpr (SBF16)
+                            store_state4<true>(p.snaps, d_off + (row0 + 16 * m) * kHeadSize + c, s[m]);
+                        else
+                            __stcs(reinterpret_cast<float4 *>(p.snaps + d_off + (row0 + 16 * m) * kHeadSize + c),
+                                   s[m]);
+                    }
                 } else if (tid == 0) {
                     flag_status(p.lv.status, WKV7_DEV_BAD_SLOT);
                 }
@@ -114,8 +131,12 @@ __global__ void __launch_bounds__(256, 5) decode_multi_kernel(DecodeMultiArgs p)
         }
     }
 #pragma unroll
-    for (int m = 0; m < 4; ++m)
-        __stcs(reinterpret_cast<float4 *>(S + (row0 + 16 * m) * kHeadSize + c), s[m]);
+    for (int m = 0; m < 4; ++m) {
+        if constexpr (SBF16)
+            store_state4<true>(p.lv.states, s_off + (row0 + 16 * m) * kHeadSize + c, s[m]);
+        else
+            __stcs(reinterpret_cast<float4 *>(S + (row0 + 16 * m) * kHeadSize + c), s[m]);
+    }
 }
 
 }  // namespace
@@ -127,12 +148,16 @@ cudaError_t launch_decode_multi(const DecodeMultiArgs &a, cudaStream_t s, int *l
     if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
     dim3 grid(static_cast<unsigned>(units));
     const bool snaps = a.step_snap_ids != nullptr;
-    if (a.in.bf16) {
-        if (snaps) decode_multi_kernel<true, true><<<grid, 256, 0, s>>>(a);
-        else decode_multi_kernel<true, false><<<grid, 256, 0, s>>>(a);
-    } else {
-        if (snaps) decode_multi_kernel<false, true><<<grid, 256, 0, s>>>(a);
-        else decode_multi_kernel<false, false><<<grid, 256, 0, s>>>(a);
+    const int variant = (a.in.bf16 ? 4 : 0) | (snaps ? 2 : 0) | (a.state_bf16 ? 1 : 0);
+    switch (variant) {
+        case 0: decode_multi_kernel<false, false, false><<<grid, 256, 0, s>>>(a); break;
+        case 1: decode_multi_kernel<false, false, true><<<grid, 256, 0, s>>>(a); break;
+        case 2: decode_multi_kernel<false, true, false><<<grid, 256, 0, s>>>(a); break;
+        case 3: decode_multi_kernel<false, true, true><<<grid, 256, 0, s>>>(a); break;
+        case 4: decode_multi_kernel<true, false, false><<<grid, 256, 0, s>>>(a); break;
+        case 5: decode_multi_kernel<true, false, true><<<grid, 256, 0, s>>>(a); break;
+        case 6: decode_multi_kernel<true, true, false><<<grid, 256, 0, s>>>(a); break;
+        default: decode_multi_kernel<true, true, true><<<grid, 256, 0, s>>>(a); break;
     }
     ++*launches;
     return cudaGetLastError();

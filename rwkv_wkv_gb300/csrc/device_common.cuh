@@ -63,6 +63,32 @@ __device__ __forceinline__ void load8(const void *p, size_t off, float *x) {
     }
 }
 
+// x rounded to the nearest bf16 value (ties to even), as a float.
+__device__ __forceinline__ float round_bf16(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+
+// Four consecutive state entries at element offset `off` of a float32 state
+// array or, with SBF16, a bf16 one (16- or 8-byte aligned).
+template <bool SBF16>
+__device__ __forceinline__ float4 load_state4(const float *states, size_t off) {
+    if constexpr (SBF16) {
+        const uint2 u = *reinterpret_cast<const uint2 *>(reinterpret_cast<const uint16_t *>(states) + off);
+        return make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
+    } else {
+        return *reinterpret_cast<const float4 *>(states + off);
+    }
+}
+
+// The store counterpart: with SBF16 each entry is rounded to bf16 (nearest even).
+template <bool SBF16>
+__device__ __forceinline__ void store_state4(float *states, size_t off, float4 x) {
+    if constexpr (SBF16) {
+        *reinterpret_cast<uint2 *>(reinterpret_cast<uint16_t *>(states) + off) =
+            make_uint2(pack_bf16_rn(x.x, x.y), pack_bf16_rn(x.z, x.w));
+    } else {
+        *reinterpret_cast<float4 *>(states + off) = x;
+    }
+}
+
 // Eight floats to global memory in one 32-byte store (sm_100 and later); p must
 // be 32-byte aligned.
 __device__ __forceinline__ void st_global_v8(float *p, const float *v) {

@@ -115,6 +115,14 @@ constexpr uint32_t kTileBytes = OFF_SLO + kTile64;
 __host__ __device__ constexpr uint32_t stage_off(int x) {  // r, w, k, v, a, b
     return x < 2 ? OFF_G2A + x * kTile64 : OFF_R1 + (x - 2) * kTile64;
 }
+// One column of a bf16 state array (32 entries, element stride 64 from element
+// `off`), each rounded to bf16 (nearest even).
+__device__ __forceinline__ void store_state_column32_bf16(float *states, size_t off, const float *v) {
+    __nv_bfloat16 *d = reinterpret_cast<__nv_bfloat16 *>(states) + off;
+#pragma unroll
+    for (int q = 0; q < 32; ++q) d[q * kHeadSize] = __float2bfloat16_rn(v[q]);
+}
+
 // Index of the strictly-upper 16x16 block (i, j), i < j < 4, in 0..5.
 __device__ __forceinline__ int up_idx(int i, int j) { return i * (7 - i) / 2 + (j - i - 1); }
 constexpr uint32_t kSmemBytes = kSmallBytes + 1024 + kTileBytes;  // + worst-case alignment
@@ -327,6 +335,8 @@ __device__ __forceinline__ void mma_wait(uint32_t bar, uint32_t parity, volatile
     if (!mbar_wait_bounded(bar, parity, kWaitCycles)) *flag = 1;
 }
 
+// SBF16: the pool stores its states in bf16 (see the store paths of the readback).
+template <bool SBF16>
 __global__ void __launch_bounds__(kThreads, 2)
     prefill_chunk_kernel(const PrefillArgs p, const __grid_constant__ InputMaps maps) {
     extern __shared__ uint8_t smem_raw[];
@@ -396,14 +406,23 @@ __global__ void __launch_bounds__(kThreads, 2)
     };
     if (tid == 0) stage_inputs(0, 5, t0, true);
 
-    float *S = p.lv.states + static_cast<size_t>(slot) * p.lv.slot_stride + p.lv.layer_off +
-               static_cast<size_t>(h) * kHeadFloats;
+    // element offset of this (slot, layer, head) state; elements are bf16 on a
+    // bf16-state pool (read exactly here; stored states are rounded to bf16)
+    const size_t s_off = static_cast<size_t>(slot) * p.lv.slot_stride + p.lv.layer_off +
+                         static_cast<size_t>(h) * kHeadFloats;
+    float *S = p.lv.states + s_off;  // float32 states only
     {  // start state -> bf16 hi/lo tiles of S^T (rows j = key, 64 value entries i per row):
        // the MN-major B operand of the state product
         const int j = tid & 63, i0 = 16 * (tid >> 6);
         float xs[16];  // all loads issued before any shared-memory store
 #pragma unroll
-        for (int q = 0; q < 16; ++q) xs[q] = __ldcg(S + (i0 + q) * kHeadSize + j);
+        for (int q = 0; q < 16; ++q) {
+            if constexpr (SBF16)
+                xs[q] = __uint_as_float(static_cast<uint32_t>(__ldcg(reinterpret_cast<const unsigned short *>(
+                                            p.lv.states) + s_off + (i0 + q) * kHeadSize + j)) << 16);
+            else
+                xs[q] = __ldcg(S + (i0 + q) * kHeadSize + j);
+        }
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
             const int i = i0 + q;
@@ -454,21 +473,33 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
         } else {  // S_L^T row j (values i of this thread's part)
             const int j = row;
+            const bool round_carry = SBF16 && p.ck.cu_ckpt && oLc == kL;
             if (p.ck.cu_ckpt && oLc == kL) {  // the state at token 64 (occ + 1) of the sequence
                 const int id = __ldg(p.ck.ckpt_ids + ck0 + occ);
                 if (id >= 0 && id < p.ck.n_snaps) {
-                    float *cp = p.ck.snaps + static_cast<size_t>(id) * p.lv.slot_stride + p.lv.layer_off +
-                                static_cast<size_t>(h) * kHeadFloats + cpart * kHeadSize + j;
+                    if constexpr (SBF16) {
+                        store_state_column32_bf16(p.ck.snaps,
+                                                  static_cast<size_t>(id) * p.lv.slot_stride + p.lv.layer_off +
+                                                      static_cast<size_t>(h) * kHeadFloats + cpart * kHeadSize + j,
+                                                  v);
+                    } else {
+                        float *cp = p.ck.snaps + static_cast<size_t>(id) * p.lv.slot_stride + p.lv.layer_off +
+                                    static_cast<size_t>(h) * kHeadFloats + cpart * kHeadSize + j;
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) cp[q * kHeadSize] = v[q];
+                        for (int q = 0; q < 32; ++q) cp[q * kHeadSize] = v[q];
+                    }
                 } else if (j == 0) {
                     flag_status(p.lv.status, WKV7_DEV_BAD_SLOT);
                 }
             }
-            if (final) {
-                float *sp = S + cpart * kHeadSize + j;  // column j of S, rows cpart..
+            if (final) {  // column j of S, rows cpart..
+                if constexpr (SBF16) {
+                    store_state_column32_bf16(p.lv.states, s_off + cpart * kHeadSize + j, v);
+                } else {
+                    float *sp = S + cpart * kHeadSize + j;
 #pragma unroll
-                for (int q = 0; q < 32; ++q) sp[q * kHeadSize] = v[q];
+                    for (int q = 0; q < 32; ++q) sp[q * kHeadSize] = v[q];
+                }
             } else {
 #pragma unroll
                 for (int q8 = 0; q8 < 4; ++q8) {  // 8 values: bf16 hi and the bf16 of the remainder
@@ -477,7 +508,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                     for (int e = 0; e < 4; ++e) {
                         const float x0 = v[8 * q8 + 2 * e], x1 = v[8 * q8 + 2 * e + 1];
                         hw[e] = pack_bf16(x0, x1);
-                        lw[e] = pack_bf16(x0 - bf16_lo(hw[e]), x1 - bf16_hi(hw[e]));
+                        // on a bf16-state pool a checkpointed state carries on as stored
+                        lw[e] = round_carry ? 0u : pack_bf16(x0 - bf16_lo(hw[e]), x1 - bf16_hi(hw[e]));
                     }
                     const uint32_t off = sw128_off(j, cpart + 8 * q8);
                     *reinterpret_cast<uint4 *>(base + OFF_SHI + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
@@ -995,12 +1027,12 @@ cudaError_t launch_prefill_chunked(const PrefillArgs &a, cudaStream_t s, int *la
     for (int x = 0; x < 6; ++x)
         if (!encode_input_map(&maps.m[x], src[x], a.lv.n_heads, a.total_tokens))
             return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(prefill_chunk_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    auto kernel = a.state_bf16 ? prefill_chunk_kernel<true> : prefill_chunk_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     const unsigned ny = static_cast<unsigned>(a.n_seqs) < kGridY ? static_cast<unsigned>(a.n_seqs) : kGridY;
     const dim3 grid(static_cast<unsigned>(a.lv.n_heads), ny, (static_cast<unsigned>(a.n_seqs) + kGridY - 1) / kGridY);
-    prefill_chunk_kernel<<<grid, kThreads, kSmemBytes, s>>>(a, maps);
+    kernel<<<grid, kThreads, kSmemBytes, s>>>(a, maps);
     ++*launches;
     return cudaGetLastError();
 }

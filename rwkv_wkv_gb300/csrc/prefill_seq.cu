@@ -9,7 +9,9 @@
 // all 64 rows); the two row reductions per token are 2-level xor shuffles.
 //
 // This is the exact-to-float32 path (wkv7_prefill_sequential); the chunked
-// tensor-core path is wkv7_prefill.
+// tensor-core path is wkv7_prefill.  With SBF16 (a bf16-state pool) the start
+// state is read as bf16 and every stored state is rounded to bf16; at a
+// checkpoint boundary the carry continues from the rounded checkpoint.
 #include "device_common.cuh"
 #include "wkv7_internal.h"
 
@@ -20,7 +22,7 @@ constexpr int kTile = 16;  // tokens staged per pass
 constexpr int kQS = 20;    // floats per 16-column group (padded: conflict-free float4 reads)
 enum { kA = 0, kW = 1, kB = 2, kK = 3, kR = 4, kKeyInputs = 5 };
 
-template <bool BF16>
+template <bool BF16, bool SBF16>
 __global__ void __launch_bounds__(256) prefill_seq_kernel(PrefillArgs p) {
     __shared__ __align__(16) float key_s[kTile][kKeyInputs][4][kQS];
     __shared__ __align__(16) float v_s[kTile][kHeadSize];
@@ -47,8 +49,9 @@ __global__ void __launch_bounds__(256) prefill_seq_kernel(PrefillArgs p) {
             return;
         }
     }
-    float *S = p.lv.states + static_cast<size_t>(slot) * p.lv.slot_stride + p.lv.layer_off +
-               static_cast<size_t>(h) * kHeadFloats;
+    // element offset of this (slot, layer, head) state; elements are bf16 with SBF16
+    const size_t s_off = static_cast<size_t>(slot) * p.lv.slot_stride + p.lv.layer_off +
+                         static_cast<size_t>(h) * kHeadFloats;
     const int tid = threadIdx.x;
     const int i = tid >> 2;  // value row
     const int q = tid & 3;   // key columns 16q .. 16q+15
@@ -56,7 +59,7 @@ __global__ void __launch_bounds__(256) prefill_seq_kernel(PrefillArgs p) {
     float s[16];
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
-        float4 x = *reinterpret_cast<const float4 *>(S + i * kHeadSize + 16 * q + 4 * m);
+        const float4 x = load_state4<SBF16>(p.lv.states, s_off + i * kHeadSize + 16 * q + 4 * m);
         s[4 * m + 0] = x.x; s[4 * m + 1] = x.y; s[4 * m + 2] = x.z; s[4 * m + 3] = x.w;
     }
 
@@ -117,21 +120,25 @@ __global__ void __launch_bounds__(256) prefill_seq_kernel(PrefillArgs p) {
         if (p.ck.cu_ckpt && n_tok == kTile && (done & 63) == 0) {  // a 64-token boundary
             const int id = __ldg(p.ck.ckpt_ids + ck0 + done / 64 - 1);
             if (id >= 0 && id < p.ck.n_snaps) {
-                float *cp = p.ck.snaps + static_cast<size_t>(id) * p.lv.slot_stride + p.lv.layer_off +
-                            static_cast<size_t>(h) * kHeadFloats + i * kHeadSize + 16 * q;
+                const size_t c_off = static_cast<size_t>(id) * p.lv.slot_stride + p.lv.layer_off +
+                                     static_cast<size_t>(h) * kHeadFloats + i * kHeadSize + 16 * q;
 #pragma unroll
                 for (int m = 0; m < 4; ++m)
-                    reinterpret_cast<float4 *>(cp)[m] =
-                        make_float4(s[4 * m], s[4 * m + 1], s[4 * m + 2], s[4 * m + 3]);
+                    store_state4<SBF16>(p.ck.snaps, c_off + 4 * m,
+                                        make_float4(s[4 * m], s[4 * m + 1], s[4 * m + 2], s[4 * m + 3]));
             } else if (tid == 0) {
                 flag_status(p.lv.status, WKV7_DEV_BAD_SLOT);
+            }
+            if constexpr (SBF16) {  // carry on from the state as the checkpoint holds it
+#pragma unroll
+                for (int e = 0; e < 16; ++e) s[e] = round_bf16(s[e]);
             }
         }
     }
 #pragma unroll
     for (int m = 0; m < 4; ++m)
-        *reinterpret_cast<float4 *>(S + i * kHeadSize + 16 * q + 4 * m) =
-            make_float4(s[4 * m], s[4 * m + 1], s[4 * m + 2], s[4 * m + 3]);
+        store_state4<SBF16>(p.lv.states, s_off + i * kHeadSize + 16 * q + 4 * m,
+                            make_float4(s[4 * m], s[4 * m + 1], s[4 * m + 2], s[4 * m + 3]));
 }
 
 }  // namespace
@@ -140,10 +147,13 @@ cudaError_t launch_prefill_sequential(const PrefillArgs &a, cudaStream_t s, int 
     if (a.n_seqs <= 0) return cudaSuccess;
     if (a.lv.n_heads > 65535) return cudaErrorInvalidValue;
     dim3 grid(static_cast<unsigned>(a.n_seqs), static_cast<unsigned>(a.lv.n_heads));
-    if (a.in.bf16)
-        prefill_seq_kernel<true><<<grid, 256, 0, s>>>(a);
-    else
-        prefill_seq_kernel<false><<<grid, 256, 0, s>>>(a);
+    if (a.in.bf16) {
+        if (a.state_bf16) prefill_seq_kernel<true, true><<<grid, 256, 0, s>>>(a);
+        else prefill_seq_kernel<true, false><<<grid, 256, 0, s>>>(a);
+    } else {
+        if (a.state_bf16) prefill_seq_kernel<false, true><<<grid, 256, 0, s>>>(a);
+        else prefill_seq_kernel<false, false><<<grid, 256, 0, s>>>(a);
+    }
     ++*launches;
     return cudaGetLastError();
 }

@@ -38,14 +38,15 @@ struct DecodeArgs {
 // step_snap_ids ([n][K]) non-null, the state after token k of row b also goes
 // to snapshot step_snap_ids[b*K + k] (this layer's slice).
 struct DecodeMultiArgs {
-    LayerView lv;
+    LayerView lv;  // for a bf16-state pool, states/slot_stride/layer_off count bf16 elements
     const int *slot_ids;
     int n;
     int n_tok;
     TokenInputs in;
-    float *snaps;
+    float *snaps;  // same element type and strides as the states
     int n_snaps;
     const int *step_snap_ids;
+    bool state_bf16;
 };
 
 // Optional states at every 64-token boundary of each sequence: sequence s
@@ -58,15 +59,20 @@ struct CheckpointArgs {
     const int *ckpt_ids;
 };
 
+// On a bf16-state pool the start state is read as bf16 and the states written
+// (the final one, checkpoints) are rounded to bf16; the carry inside a sequence
+// stays float32 except at checkpoint boundaries, where it continues from the
+// rounded checkpoint, so that resuming from a checkpoint reproduces the rest.
 struct PrefillArgs {
-    LayerView lv;
+    LayerView lv;  // for a bf16-state pool, states/slot_stride/layer_off count bf16 elements
     const int *slot_ids;
     const int *cu_seqlens;
     int n_seqs;
     int total_tokens;
     int max_seqlen;
     TokenInputs in;
-    CheckpointArgs ck;
+    CheckpointArgs ck;  // snaps: same element type and strides as the states
+    bool state_bf16;
 };
 
 // Whole-slot copies: dst[dst_ids[i]] <- src[src_ids[i]], slot_floats each; a

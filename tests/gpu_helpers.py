@@ -42,3 +42,25 @@ def sampled_head_inputs(seed: int, tag: str, n_tok: int, H: int, N: int, heads,
     for t, name in zip(dev, NAMES):
         t[:, hidx] = torch.from_numpy(host[name]).to(device).to(torch.bfloat16)
     return dev, host
+
+
+def bf16_spacing(x):
+    """Spacing of bf16 values at |x| (at least the subnormal spacing 2^-133)."""
+    ax = np.maximum(np.abs(x), 2.0**-126)
+    return np.exp2(np.floor(np.log2(ax)) - 7)
+
+
+def check_bf16_state_step(o_gpu, S_gpu, o_ref, S_ref):
+    """One step from a stored bf16 state: o within DECODE_TOL of the oracle's
+    float64 step; the stored new state within one bf16 spacing of the oracle's
+    float64 step rounded to bf16 (the float32 and float64 results round to
+    different neighbours only when they straddle a rounding boundary), plus the
+    float32 arithmetic error of the step (2^-18 of the head's largest entry,
+    which matters only where an entry nearly cancels); at least 99% of the
+    entries identical."""
+    assert rel(o_gpu, o_ref) < DECODE_TOL
+    diff = np.abs(S_gpu - S_ref)
+    head_max = np.abs(S_ref).max(axis=(-2, -1), keepdims=True)
+    allow = bf16_spacing(np.maximum(np.abs(S_gpu), np.abs(S_ref))) + head_max * 2.0**-18
+    assert bool((diff <= allow).all()), float((diff / allow).max())
+    assert float((diff == 0).mean()) >= 0.99

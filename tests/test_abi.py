@@ -203,7 +203,7 @@ def test_snapshot_verbs_need_a_snapshot_store(lib):
 
 def test_bf16_state_pool(lib):
     """A bf16-state pool: half the bytes per slot, state pointers step in bf16,
-    decode and the verbs are offered, the other recurrence calls are not."""
+    and every call is offered."""
     d16 = _desc(state_dtype=1)
     d32 = _desc()
     body32 = lib.wkv7_pool_required_bytes(ctypes.byref(d32)) - 256
@@ -221,10 +221,13 @@ def test_bf16_state_pool(lib):
         assert lib.wkv7_pool_state_ptr(h, 2, 1, ctypes.byref(p21)) == 0
         assert p00.value == FAKE_DEVICE_ADDR + 256
         assert p21.value - p00.value == 2 * sb + 3 * 64 * 64 * 2
-        assert lib.wkv7_prefill(h, 0, x, x, 1, 10, 10, 1, *ins, x, None) == 7
-        assert lib.wkv7_prefill_sequential(h, 0, x, x, 1, 10, 10, 1, *ins, x, None) == 7
-        assert lib.wkv7_decode_multi(h, 0, x, 1, 2, 1, *ins, x, None, None) == 7
-        assert lib.wkv7_decode_step(h, 0, x, 0, 1, *ins, x, None) == 0  # offered (empty: no-op)
+        # every recurrence call is offered (empty calls: no-ops) and host-checked as usual
+        assert lib.wkv7_prefill(h, 0, x, x, 0, 0, 0, 1, *ins, x, None) == 0
+        assert lib.wkv7_prefill_sequential(h, 0, x, x, 0, 0, 0, 1, *ins, x, None) == 0
+        assert lib.wkv7_decode_multi(h, 0, x, 0, 2, 1, *ins, x, None, None) == 0
+        assert lib.wkv7_decode_step(h, 0, x, 0, 1, *ins, x, None) == 0
+        assert lib.wkv7_prefill(h, 2, x, x, 1, 10, 10, 1, *ins, x, None) == 1
+        assert lib.wkv7_decode_multi(h, 0, x, 1, 0, 1, *ins, x, None, None) == 1
         desc = wkv7.PoolDesc()
         assert lib.wkv7_pool_get_desc(h, ctypes.byref(desc)) == 0 and desc.state_dtype == 1
     finally:
