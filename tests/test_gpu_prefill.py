@@ -4,6 +4,8 @@ wkv7_prefill (chunked, bf16 tensor-core operands, float32 carry): normwise-max
 relative error <= 2e-2 on outputs and final states.  wkv7_prefill_sequential
 (float32 token by token): <= 1e-4.
 """
+import functools
+
 import numpy as np
 import pytest
 import torch
@@ -228,3 +230,33 @@ def test_output_alignment_does_not_change_results():
     assert torch.equal(outs[0], outs[1]) and torch.equal(states[0], states[1])
     o_ref, _ = oracle.prefill(S0.astype(np.float64), cu, *host_inputs(ins))
     assert rel(outs[1].cpu().numpy(), o_ref) < PREFILL_TOL
+
+
+@functools.lru_cache(maxsize=2)
+def _many(n_seqs, max_len, H):
+    """Seeded inputs, start states and slot order of the many-sequence case."""
+    N = 64
+    rng = np.random.default_rng(n_seqs)
+    lengths = rng.integers(1, max_len + 1, n_seqs)
+    cu = wl.cu_seqlens(lengths)
+    ins = wl.token_inputs(44, f"many/{n_seqs}", int(cu[-1]), H, N, dtype="bf16")
+    S0 = (wl.slot_states(44, f"many/{n_seqs}/s0", range(n_seqs), 1, H, N)[:, 0] if n_seqs <= 5000
+          else np.zeros((n_seqs, H, N, N)))  # created slots
+    return cu, ins, S0, rng.permutation(n_seqs)
+
+
+@pytest.mark.parametrize("name,sequential,tol", PATHS)
+@pytest.mark.parametrize("n_seqs,max_len,H", [(5000, 40, 2), (70000, 1, 1)])
+def test_many_sequences(name, sequential, tol, n_seqs, max_len, H):
+    """More sequences than the chunked kernel orders longest-first (4096; then
+    index order) and than one grid dimension holds (65535; the ranks are split
+    over two): every sequence still gets its own result."""
+    cu, ins, S0, slots = _many(n_seqs, max_len, H)
+    with Pool(1, H, n_seqs) as pool:
+        pool.states[torch.as_tensor(slots), 0] = torch.from_numpy(S0).cuda().float()
+        o, code = _run(pool, slots, cu, ins, sequential)
+        assert code == 0
+        S_gpu = pool.states[torch.as_tensor(slots), 0].cpu().numpy()
+    o_ref, S_ref = oracle.prefill(S0.astype(np.float64), cu, *host_inputs(ins), n_threads=8)
+    assert rel(o, o_ref) < tol
+    assert rel(S_gpu, S_ref) < tol
