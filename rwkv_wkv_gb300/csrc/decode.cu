@@ -23,6 +23,7 @@ namespace {
 
 template <bool BF16>
 __global__ void __launch_bounds__(256) decode_kernel(DecodeArgs p) {
+    pdl_prologue();
     const int H = p.lv.n_heads;
     const int unit = blockIdx.x;
     const int bi = unit / H;
@@ -100,6 +101,7 @@ constexpr int kBf16RowStep = kHeadSize / kBf16Rows;
 
 template <bool BF16>
 __global__ void __launch_bounds__(kBf16Threads) decode_bf16state_kernel(DecodeArgs p) {
+    pdl_prologue();
     const int H = p.lv.n_heads;
     const int unit = blockIdx.x;
     const int bi = unit / H;
@@ -183,18 +185,14 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s, int *launches) {
     if (units <= 0) return cudaSuccess;
     if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
     dim3 grid(static_cast<unsigned>(units));
-    if (a.state_bf16) {
-        if (a.in.bf16)
-            decode_bf16state_kernel<true><<<grid, kBf16Threads, 0, s>>>(a);
-        else
-            decode_bf16state_kernel<false><<<grid, kBf16Threads, 0, s>>>(a);
-    } else if (a.in.bf16) {
-        decode_kernel<true><<<grid, 256, 0, s>>>(a);
-    } else {
-        decode_kernel<false><<<grid, 256, 0, s>>>(a);
-    }
+    cudaError_t e;
+    if (a.state_bf16)
+        e = launch_pdl(a.in.bf16 ? decode_bf16state_kernel<true> : decode_bf16state_kernel<false>, grid,
+                       dim3(kBf16Threads), 0, s, a);
+    else
+        e = launch_pdl(a.in.bf16 ? decode_kernel<true> : decode_kernel<false>, grid, dim3(256), 0, s, a);
     ++*launches;
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace wkv7

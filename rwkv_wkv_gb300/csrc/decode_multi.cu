@@ -30,6 +30,7 @@ enum { kR = 0, kW, kK, kV, kA, kB, kInputs };
 template <bool BF16, bool SNAPS, bool SBF16>
 __global__ void __launch_bounds__(256, (SNAPS && SBF16) ? 4 : 5) decode_multi_kernel(DecodeMultiArgs p) {
     __shared__ __align__(16) float xs[kGroup][kInputs][kHeadSize];
+    pdl_prologue();
     const int H = p.lv.n_heads;
     const int unit = blockIdx.x;
     const int bi = unit / H;
@@ -149,18 +150,14 @@ cudaError_t launch_decode_multi(const DecodeMultiArgs &a, cudaStream_t s, int *l
     dim3 grid(static_cast<unsigned>(units));
     const bool snaps = a.step_snap_ids != nullptr;
     const int variant = (a.in.bf16 ? 4 : 0) | (snaps ? 2 : 0) | (a.state_bf16 ? 1 : 0);
-    switch (variant) {
-        case 0: decode_multi_kernel<false, false, false><<<grid, 256, 0, s>>>(a); break;
-        case 1: decode_multi_kernel<false, false, true><<<grid, 256, 0, s>>>(a); break;
-        case 2: decode_multi_kernel<false, true, false><<<grid, 256, 0, s>>>(a); break;
-        case 3: decode_multi_kernel<false, true, true><<<grid, 256, 0, s>>>(a); break;
-        case 4: decode_multi_kernel<true, false, false><<<grid, 256, 0, s>>>(a); break;
-        case 5: decode_multi_kernel<true, false, true><<<grid, 256, 0, s>>>(a); break;
-        case 6: decode_multi_kernel<true, true, false><<<grid, 256, 0, s>>>(a); break;
-        default: decode_multi_kernel<true, true, true><<<grid, 256, 0, s>>>(a); break;
-    }
+    void (*const kernels[8])(DecodeMultiArgs) = {
+        decode_multi_kernel<false, false, false>, decode_multi_kernel<false, false, true>,
+        decode_multi_kernel<false, true, false>,  decode_multi_kernel<false, true, true>,
+        decode_multi_kernel<true, false, false>,  decode_multi_kernel<true, false, true>,
+        decode_multi_kernel<true, true, false>,   decode_multi_kernel<true, true, true>};
+    const cudaError_t e = launch_pdl(kernels[variant], grid, dim3(256), 0, s, a);
     ++*launches;
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace wkv7

@@ -340,6 +340,7 @@ template <bool SBF16>
 __global__ void __launch_bounds__(kThreads, 2)
     prefill_chunk_kernel(const PrefillArgs p, const __grid_constant__ InputMaps maps) {
     extern __shared__ uint8_t smem_raw[];
+    pdl_prologue();
     const int H = p.lv.n_heads;
     const int h = blockIdx.x;
     const int rank = static_cast<int>(blockIdx.z * kGridY + blockIdx.y);
@@ -1032,9 +1033,9 @@ cudaError_t launch_prefill_chunked(const PrefillArgs &a, cudaStream_t s, int *la
     if (e != cudaSuccess) return e;
     const unsigned ny = static_cast<unsigned>(a.n_seqs) < kGridY ? static_cast<unsigned>(a.n_seqs) : kGridY;
     const dim3 grid(static_cast<unsigned>(a.lv.n_heads), ny, (static_cast<unsigned>(a.n_seqs) + kGridY - 1) / kGridY);
-    kernel<<<grid, kThreads, kSmemBytes, s>>>(a, maps);
+    e = launch_pdl(kernel, grid, dim3(kThreads), kSmemBytes, s, a, maps);
     ++*launches;
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace wkv7

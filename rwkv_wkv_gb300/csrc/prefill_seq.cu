@@ -26,6 +26,7 @@ template <bool BF16, bool SBF16>
 __global__ void __launch_bounds__(256) prefill_seq_kernel(PrefillArgs p) {
     __shared__ __align__(16) float key_s[kTile][kKeyInputs][4][kQS];
     __shared__ __align__(16) float v_s[kTile][kHeadSize];
+    pdl_prologue();
 
     const int seq = blockIdx.x;
     const int h = blockIdx.y;
@@ -147,15 +148,12 @@ cudaError_t launch_prefill_sequential(const PrefillArgs &a, cudaStream_t s, int 
     if (a.n_seqs <= 0) return cudaSuccess;
     if (a.lv.n_heads > 65535) return cudaErrorInvalidValue;
     dim3 grid(static_cast<unsigned>(a.n_seqs), static_cast<unsigned>(a.lv.n_heads));
-    if (a.in.bf16) {
-        if (a.state_bf16) prefill_seq_kernel<true, true><<<grid, 256, 0, s>>>(a);
-        else prefill_seq_kernel<true, false><<<grid, 256, 0, s>>>(a);
-    } else {
-        if (a.state_bf16) prefill_seq_kernel<false, true><<<grid, 256, 0, s>>>(a);
-        else prefill_seq_kernel<false, false><<<grid, 256, 0, s>>>(a);
-    }
+    void (*const kernels[4])(PrefillArgs) = {prefill_seq_kernel<false, false>, prefill_seq_kernel<false, true>,
+                                             prefill_seq_kernel<true, false>, prefill_seq_kernel<true, true>};
+    const cudaError_t e =
+        launch_pdl(kernels[(a.in.bf16 ? 2 : 0) | (a.state_bf16 ? 1 : 0)], grid, dim3(256), 0, s, a);
     ++*launches;
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace wkv7

@@ -17,6 +17,7 @@ constexpr long long kVecPerCta = kThreads * kVecPerThread;
 constexpr int kMaxGridY = 65535;
 
 __global__ void __launch_bounds__(kThreads) slot_copy_kernel(CopyArgs a, int pair0) {
+    pdl_prologue();
     const int pair = pair0 + blockIdx.y;
     const int d = a.dst_ids ? __ldg(a.dst_ids + pair) : pair;  // no id array: the i-th slot of a packed buffer
     const int s = a.src_ids ? __ldg(a.src_ids + pair) : pair;
@@ -57,6 +58,7 @@ __global__ void __launch_bounds__(kThreads) slot_zero_dev_kernel(float *states, 
                                                                  long long slot_floats,
                                                                  const int *ids, int pair0,
                                                                  int *status) {
+    pdl_prologue();
     const int slot = __ldg(ids + pair0 + blockIdx.y);
     if (slot < 0 || slot >= n_slots) {
         if (blockIdx.x == 0 && threadIdx.x == 0) flag_status(status, WKV7_DEV_BAD_SLOT);
@@ -68,6 +70,7 @@ __global__ void __launch_bounds__(kThreads) slot_zero_dev_kernel(float *states, 
 __global__ void __launch_bounds__(kThreads) slot_zero_val_kernel(float *states, int n_slots,
                                                                  long long slot_floats, ZeroIds ids,
                                                                  int *status) {
+    pdl_prologue();
     const int slot = ids.ids[blockIdx.y];
     if (slot < 0 || slot >= n_slots) {
         if (blockIdx.x == 0 && threadIdx.x == 0) flag_status(status, WKV7_DEV_BAD_SLOT);
@@ -87,9 +90,10 @@ cudaError_t launch_slot_copy(const CopyArgs &a, cudaStream_t s, int *launches) {
     const unsigned gx = blocks_per_slot(a.slot_floats);
     for (int p0 = 0; p0 < a.n; p0 += kMaxGridY) {
         const int cnt = a.n - p0 < kMaxGridY ? a.n - p0 : kMaxGridY;
-        slot_copy_kernel<<<dim3(gx, static_cast<unsigned>(cnt)), kThreads, 0, s>>>(a, p0);
+        cudaError_t e = launch_pdl(slot_copy_kernel, dim3(gx, static_cast<unsigned>(cnt)), dim3(kThreads), 0, s,
+                                   a, p0);
         ++*launches;
-        cudaError_t e = cudaGetLastError();
+        if (e == cudaSuccess) e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -101,10 +105,10 @@ cudaError_t launch_slot_zero_dev(float *states, int n_slots, long long slot_floa
     const unsigned gx = blocks_per_slot(slot_floats);
     for (int p0 = 0; p0 < n; p0 += kMaxGridY) {
         const int cnt = n - p0 < kMaxGridY ? n - p0 : kMaxGridY;
-        slot_zero_dev_kernel<<<dim3(gx, static_cast<unsigned>(cnt)), kThreads, 0, s>>>(
-            states, n_slots, slot_floats, ids_dev, p0, status);
+        cudaError_t e = launch_pdl(slot_zero_dev_kernel, dim3(gx, static_cast<unsigned>(cnt)), dim3(kThreads), 0,
+                                   s, states, n_slots, slot_floats, ids_dev, p0, status);
         ++*launches;
-        cudaError_t e = cudaGetLastError();
+        if (e == cudaSuccess) e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -118,10 +122,10 @@ cudaError_t launch_slot_zero_host(float *states, int n_slots, long long slot_flo
         const int cnt = n - p0 < kZeroIdsPerLaunch ? n - p0 : kZeroIdsPerLaunch;
         ZeroIds ids;
         for (int i = 0; i < cnt; ++i) ids.ids[i] = ids_host[p0 + i];
-        slot_zero_val_kernel<<<dim3(gx, static_cast<unsigned>(cnt)), kThreads, 0, s>>>(
-            states, n_slots, slot_floats, ids, status);
+        cudaError_t e = launch_pdl(slot_zero_val_kernel, dim3(gx, static_cast<unsigned>(cnt)), dim3(kThreads), 0,
+                                   s, states, n_slots, slot_floats, ids, status);
         ++*launches;
-        cudaError_t e = cudaGetLastError();
+        if (e == cudaSuccess) e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
