@@ -161,3 +161,49 @@ def test_decode_sweep_32_layers_64_heads_sampled(B):
         pool.close()
         del pool
         torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
+def test_dependent_calls_without_host_sync(state_dtype):
+    """Eight decode steps on the same slots, each launched right after the
+    previous one with no host synchronisation (each kernel may begin launching
+    while the previous one drains and must still read the state it wrote), then
+    a snapshot, a fork and a prefill that read those states; compared with the
+    oracle's chained steps."""
+    H, N, B, T = 8, 64, 64, 8
+    ins = wl.token_inputs(45, "chain", T * B, H, N, dtype="bf16")
+    ins = {k: v.reshape(T, B, H, N) for k, v in ins.items()}
+    dev = [[torch.from_numpy(ins[n][t]).cuda().to(torch.bfloat16) for n in wl.INPUT_NAMES]
+           for t in range(T)]
+    S0 = wl.slot_states(45, "chain/s0", range(B), 1, H, N)[:, 0]
+    if state_dtype == "bf16":
+        S0 = oracle.round_bf16(S0)
+    pre = wl.token_inputs(46, "chain/pre", 100, H, N, dtype="bf16")
+    tdt = torch.bfloat16 if state_dtype == "bf16" else torch.float32
+    with Pool(1, H, 2 * B, n_snapshots=B, state_dtype=state_dtype) as pool:
+        pool.states[:B, 0] = torch.from_numpy(S0).cuda().to(tdt)
+        ids, fork_dst, pre_slot, pre_cu = i32(range(B)), i32(range(B, 2 * B)), i32([B]), i32([0, 100])
+        pre_dev = dev_inputs(pre, "bf16")
+        torch.cuda.synchronize()
+        outs = [pool.decode_step(0, ids, *dev[t]) for t in range(T)]
+        pool.snapshot(ids, ids)
+        pool.fork(ids, fork_dst)
+        o_pre = pool.prefill(0, pre_slot, pre_cu, *pre_dev, max_seqlen=100)
+        torch.cuda.synchronize()
+        assert pool.device_status() == 0
+        o_gpu = torch.stack(outs).cpu().numpy()
+        S_gpu = pool.states[:B, 0].double().cpu().numpy()
+        assert torch.equal(pool.snapshots[:, 0], pool.states[:B, 0])
+        assert torch.equal(pool.states[B + 1:2 * B, 0], pool.states[1:B, 0])
+        S_pre = pool.states[B, 0].double().cpu().numpy()
+    S = S0.astype(np.float64)
+    step = oracle.decode_step_bf16_state if state_dtype == "bf16" else oracle.decode_step
+    for t in range(T):
+        o, S = step(S, *[x[t] for x in host_inputs(ins)], n_threads=8)
+        assert rel(o_gpu[t], o) < (DECODE_TOL if state_dtype == "f32" else 1e-2), t
+    assert rel(S_gpu, S) < (DECODE_TOL if state_dtype == "f32" else 1e-2)
+    o_ref, S_ref = oracle.prefill(S_gpu[:1], np.array([0, 100]), *host_inputs(pre))
+    assert rel(o_pre.cpu().numpy(), o_ref) < 2e-2
+    if state_dtype == "bf16":
+        S_ref = oracle.round_bf16(S_ref)
+    assert rel(S_pre, S_ref[0]) < 2e-2
