@@ -46,6 +46,10 @@
  *     result is undefined (not detected on the fast path).
  *   - Only head_size == 64 is implemented; other sizes return
  *     WKV7_ERR_UNSUPPORTED.
+ *   - Kernels are launched with programmatic dependent launch: a kernel may
+ *     begin launching while the previous one in its stream drains, but waits
+ *     for all earlier work in the stream before it touches memory, so stream
+ *     order is kept exactly as with ordinary launches.
  */
 #ifndef WKV7_H
 #define WKV7_H
@@ -71,7 +75,8 @@ typedef enum {
     WKV7_ERR_POOL_FULL = 4,     /* fewer free slots/snapshots than requested */
     WKV7_ERR_BAD_SEQLENS = 5,   /* host-checkable sequence sizes are inconsistent */
     WKV7_ERR_CUDA = 6,          /* a CUDA runtime call failed; see wkv7_last_error */
-    WKV7_ERR_UNSUPPORTED = 7,   /* head_size != 64, or dtype not offered by this call */
+    WKV7_ERR_UNSUPPORTED = 7,   /* head_size != 64, an input dtype the call does not
+                                   take, or a misaligned input/output base */
     WKV7_ERR_DEVICE_STATUS = 8, /* a kernel recorded a fault; code in *code_out */
     WKV7_ERR_TIMEOUT = 9,       /* the stream did not finish within the limit */
     WKV7_ERR_NO_MEMORY = 10     /* host or device allocation failed */
