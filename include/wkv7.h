@@ -344,6 +344,15 @@ const char *wkv7_last_error(void);
 uint64_t wkv7_launch_count(void);
 int32_t wkv7_version(void);
 
+/* Test hook for the bounded waits of the chunked prefill (process-wide, off by
+ * default; for tests only).  While on != 0, every wkv7_prefill on the chunked
+ * path skips its first input load, so the wait for it is never satisfied; each
+ * wait then gives up after about 50 ms instead of about 2 s, the CTA releases
+ * its tensor memory and exits, and the call reports WKV7_DEV_WAIT_TIMEOUT
+ * through wkv7_get_device_status (its outputs and the slot's state are not
+ * meaningful).  The context stays usable.  Returns WKV7_OK. */
+wkv7_status wkv7_test_force_wait_timeout(int32_t on);
+
 #ifdef __cplusplus
 }
 #endif

@@ -19,6 +19,7 @@ constexpr size_t kHeaderBytes = 256;  // device status word lives here
 
 std::atomic<uint64_t> g_launches{0};
 thread_local char g_last_error[512] = "";
+std::atomic<int> g_test_wait_timeout{0};  // wkv7_test_force_wait_timeout
 
 void set_error(const char *what, cudaError_t e) {
     std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%d)", what,
@@ -472,6 +473,9 @@ static wkv7_status prefill_common(wkv7_pool *pool, int32_t layer, const int32_t 
     pa.in = {r, w, k, v, a, b, in_dtype == WKV7_BF16, o};
     pa.ck = {pool->snaps, pool->desc.n_snapshots, cu_ckpt_dev, ckpt_snap_ids_dev};
     pa.state_bf16 = pool->state_bf16;
+    const bool force_timeout = g_test_wait_timeout.load(std::memory_order_relaxed) != 0;
+    pa.wait_cycles = force_timeout ? wkv7::kTestWaitCycles : wkv7::kWaitCycles;
+    pa.test_skip_first_load = force_timeout;
     int launches = 0;
     cudaError_t e = chunked ? wkv7::launch_prefill_chunked(pa, stream, &launches)
                             : wkv7::launch_prefill_sequential(pa, stream, &launches);
@@ -577,6 +581,11 @@ const char *wkv7_status_string(wkv7_status s) {
 const char *wkv7_last_error(void) { return g_last_error; }
 
 uint64_t wkv7_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+wkv7_status wkv7_test_force_wait_timeout(int32_t on) {
+    g_test_wait_timeout.store(on != 0, std::memory_order_relaxed);
+    return WKV7_OK;
+}
 
 int32_t wkv7_version(void) { return WKV7_VERSION; }
 

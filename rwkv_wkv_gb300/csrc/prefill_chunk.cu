@@ -67,7 +67,6 @@ using namespace sm100;
 
 constexpr int kL = 64;
 constexpr int kThreads = 256;  // 8 warps; two CTAs per SM
-constexpr long long kWaitCycles = 4000000000LL;  // about 2 s at 2 GHz
 constexpr float kMaxLog2Range = 120.0f;           // |G - Gm| limit (float exponent range)
 constexpr float kMinDecayRel = 0x1p-120f, kMaxDecayRel = 0x1p120f;  // the same limit on 2^(G - Gm)
 
@@ -331,8 +330,8 @@ __device__ __noinline__ int seq_of_rank(const int *cu, int n, int rank, int *wor
 // the CTA's abort flag; the flag is read (uniformly) after the phase's closing
 // barrier, so a timed-out phase runs to that barrier on garbage and then the
 // CTA leaves.
-__device__ __forceinline__ void mma_wait(uint32_t bar, uint32_t parity, volatile int *flag) {
-    if (!mbar_wait_bounded(bar, parity, kWaitCycles)) *flag = 1;
+__device__ __forceinline__ void mma_wait(uint32_t bar, uint32_t parity, volatile int *flag, long long limit) {
+    if (!mbar_wait_bounded(bar, parity, limit)) *flag = 1;
 }
 
 // SBF16: the pool stores its states in bf16 (see the store paths of the readback).
@@ -405,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int x = x0; x <= x1; ++x)
             tma_load_3d(smem_addr(base + stage_off(x)), &maps.m[x], 0, h, tcn, bar_in);
     };
-    if (tid == 0) stage_inputs(0, 5, t0, true);
+    if (tid == 0 && !p.test_skip_first_load) stage_inputs(0, 5, t0, true);
 
     // element offset of this (slot, layer, head) state; elements are bf16 on a
     // bf16-state pool (read exactly here; stored states are rounded to bf16)
@@ -589,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         uint32_t in_r[8], in_w[8], in_k[8], in_v[8], in_a[8], in_b[8];
         float e0s, e1s, eGm0, eGm1, EL0, EL1;  // 2^(G_{tb-1} - Gm), 2^Gm, 2^(G_L - Gm) per channel
         {
-            mma_wait(bar_in, ph_in, flag);  // the staged inputs have landed
+            mma_wait(bar_in, ph_in, flag, p.wait_cycles);  // the staged inputs have landed
             ph_in ^= 1;
             {
                 auto st = [&](int x, int t) -> uint32_t {
@@ -707,7 +706,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             tc_fence_after();
             readback_state_product(prev_c, prev_tc0, prev_Lc, false);
         }
-        mma_wait(bar_mma, ph_mma, flag);
+        mma_wait(bar_mma, ph_mma, flag, p.wait_cycles);
         ph_mma ^= 1;
         tc_fence_after();
         {
@@ -897,7 +896,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             umma_128xNx64(tmem + kColG2, smem_addr(base + OFF_G2A), smem_addr(base + OFF_G2B), 64, false);
             umma_commit(bar_mma);
         }
-        mma_wait(bar_mma, ph_mma, flag);
+        mma_wait(bar_mma, ph_mma, flag, p.wait_cycles);
         ph_mma ^= 1;
         if (tid == 0 && !last) stage_inputs(0, 5, tc0 + kL, true);  // G2A and R1 are dead
         tc_fence_after();
@@ -922,7 +921,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             umma_ta_128xNx64(tmem + 0, tmem + kColZA, smem_addr(base + OFF_G34B), 128, true, true);
             umma_commit(bar_mma);
         }
-        mma_wait(bar_mma, ph_mma, flag);
+        mma_wait(bar_mma, ph_mma, flag, p.wait_cycles);
         ph_mma ^= 1;
         tc_fence_after();
         {  // [Phi^T; R'^T] and [Y_B^T; Y_Q^T] rows -> the bf16 A operands of G5 in tensor memory
@@ -952,7 +951,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             umma_ta_128xNx64(tmem + 0, tmem + kColYA, smem_addr(base + OFF_V), 64, true, false);
             umma_commit(bar_mma);
         }
-        mma_wait(bar_mma, ph_mma, flag);
+        mma_wait(bar_mma, ph_mma, flag, p.wait_cycles);
         ph_mma ^= 1;
         tc_fence_after();
         prev_c = c;
@@ -969,10 +968,10 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     if (*flag) {  // a wait gave up: give in-flight MMAs a last chance, then leave
         if (tid == 0) flag_status(p.lv.status, WKV7_DEV_WAIT_TIMEOUT);
-        mbar_wait_bounded(bar_mma, ph_mma, kWaitCycles);
-        mbar_wait_bounded(bar_in, ph_in, kWaitCycles);
+        mbar_wait_bounded(bar_mma, ph_mma, p.wait_cycles);
+        mbar_wait_bounded(bar_in, ph_in, p.wait_cycles);
     }
-    if (range_bad) flag_status(p.lv.status, WKV7_DEV_DECAY_RANGE);
+    if (range_bad && !*flag) flag_status(p.lv.status, WKV7_DEV_DECAY_RANGE);  // a timeout is reported instead
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {

@@ -73,7 +73,12 @@ struct PrefillArgs {
     TokenInputs in;
     CheckpointArgs ck;  // snaps: same element type and strides as the states
     bool state_bf16;
+    long long wait_cycles;      // bound of every wait in the chunked kernel (clock cycles)
+    bool test_skip_first_load;  // test hook: the first input load is never issued
 };
+
+constexpr long long kWaitCycles = 4000000000LL;     // about 2 s at 2 GHz
+constexpr long long kTestWaitCycles = 100000000LL;  // about 50 ms: the test hook's bound
 
 // Whole-slot copies: dst[dst_ids[i]] <- src[src_ids[i]], slot_floats each; a
 // null id array stands for the identity (the i-th slot of a packed buffer).

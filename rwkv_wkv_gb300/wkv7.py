@@ -83,6 +83,7 @@ _SIGS = {
     "wkv7_last_error": (ctypes.c_char_p, []),
     "wkv7_launch_count": (ctypes.c_uint64, []),
     "wkv7_version": (ctypes.c_int32, []),
+    "wkv7_test_force_wait_timeout": (ctypes.c_int, [_I32]),
 }
 
 _lib = None

@@ -14,7 +14,7 @@ import oracle
 import workloads as wl
 from gpu_helpers import (PREFILL_TOL, SEQ_PREFILL_TOL, dev_inputs, host_inputs, i32, rel,
                          sampled_head_inputs)
-from rwkv_wkv_gb300 import DEV_BAD_SEQLENS, DEV_BAD_SLOT, Pool
+from rwkv_wkv_gb300 import DEV_BAD_SEQLENS, DEV_BAD_SLOT, DEV_WAIT_TIMEOUT, Pool, load_library
 
 pytestmark = pytest.mark.gpu
 
@@ -260,3 +260,33 @@ def test_many_sequences(name, sequential, tol, n_seqs, max_len, H):
     o_ref, S_ref = oracle.prefill(S0.astype(np.float64), cu, *host_inputs(ins), n_threads=8)
     assert rel(o, o_ref) < tol
     assert rel(S_gpu, S_ref) < tol
+
+
+def test_bounded_wait_gives_up_and_the_context_stays_usable():
+    """With the test hook on, the chunked prefill's first input load is never
+    issued: every wait for it gives up (about 50 ms), the CTAs release their
+    tensor memory and exit, the call reports WKV7_DEV_WAIT_TIMEOUT and leaves
+    the slots' states alone.  The same call then runs normally."""
+    lib = load_library()
+    H, N = 2, 64
+    lengths = [100, 7]
+    cu = wl.cu_seqlens(lengths)
+    ins = wl.token_inputs(47, "timeout", int(cu[-1]), H, N, dtype="bf16")
+    S0 = wl.slot_states(47, "timeout/s0", range(2), 1, H, N)[:, 0]
+    dev = dev_inputs(ins, "bf16")
+    with Pool(1, H, 2) as pool:
+        pool.states[:, 0] = torch.from_numpy(S0).cuda()
+        before = pool.states.clone()
+        assert lib.wkv7_test_force_wait_timeout(1) == 0
+        try:
+            pool.prefill(0, i32([0, 1]), i32(cu), *dev, max_seqlen=max(lengths))
+            assert pool.device_status() == DEV_WAIT_TIMEOUT
+        finally:
+            lib.wkv7_test_force_wait_timeout(0)
+        assert torch.equal(pool.states, before)
+        o = pool.prefill(0, i32([0, 1]), i32(cu), *dev, max_seqlen=max(lengths))
+        assert pool.device_status() == 0
+        S_gpu = pool.states[:, 0].cpu().numpy()
+    o_ref, S_ref = oracle.prefill(S0.astype(np.float64), cu, *host_inputs(ins))
+    assert rel(o.cpu().numpy(), o_ref) < PREFILL_TOL
+    assert rel(S_gpu, S_ref) < PREFILL_TOL
