@@ -165,19 +165,21 @@ def test_resume_from_bf16_checkpoint_is_bit_identical(name, sequential, tol):
             assert torch.equal(pool.snapshots[3:6 - m], ck_full[m:]), m
 
 
-def _token_inputs(seed, B, K):
-    ins = wl.token_inputs(seed, "bf16paths/multi", B * K, H, N, dtype="bf16")
+def _token_inputs(seed, B, K, dtype="bf16"):
+    ins = wl.token_inputs(seed, "bf16paths/multi", B * K, H, N, dtype=dtype)
     host = {n: ins[n].reshape(B, K, H, N) for n in NAMES}
-    dev = [torch.from_numpy(np.ascontiguousarray(host[n])).cuda().to(torch.bfloat16) for n in NAMES]
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    dev = [torch.from_numpy(np.ascontiguousarray(host[n])).cuda().to(tdt) for n in NAMES]
     return host, dev
 
 
-def test_decode_multi_is_k_rounded_steps():
+@pytest.mark.parametrize("in_dtype", ["bf16", "f32"])
+def test_decode_multi_is_k_rounded_steps(in_dtype):
     """Each token meets the one-step bf16 contract from the state stored after
     the previous token (its rollback snapshot); the call equals K one-token calls
     bit for bit; rolling back to token k and continuing reproduces the rest."""
     B, K, pool_n = 10, 4, 24
-    host, dev = _token_inputs(64, B, K)
+    host, dev = _token_inputs(64, B, K, in_dtype)
     ids = wl.distinct_slots(64, "bf16paths/ids", B, pool_n)
     S0 = oracle.round_bf16(wl.slot_states(64, "bf16paths/multi/s0", range(pool_n), 1, H, N)[:, 0])
     sel = torch.as_tensor(ids, dtype=torch.long)

@@ -290,3 +290,31 @@ def test_bounded_wait_gives_up_and_the_context_stays_usable():
     o_ref, S_ref = oracle.prefill(S0.astype(np.float64), cu, *host_inputs(ins))
     assert rel(o.cpu().numpy(), o_ref) < PREFILL_TOL
     assert rel(S_gpu, S_ref) < PREFILL_TOL
+
+
+@pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
+def test_sequential_prefill_float32_inputs(state_dtype):
+    """wkv7_prefill_sequential also takes float32 inputs: against the oracle at the
+    float32 tolerance, and on a bf16-state pool equal to the float32-pool run with
+    the final state rounded."""
+    H, N = 3, 64
+    lengths = [70, 64, 1, 9]
+    cu = wl.cu_seqlens(lengths)
+    ins = wl.token_inputs(49, "seq/f32", int(cu[-1]), H, N, dtype="f32")
+    dev = dev_inputs(ins, "f32")
+    assert dev[0].dtype == torch.float32
+    S0 = oracle.round_bf16(wl.slot_states(49, "seq/f32/s0", range(len(lengths)), 1, H, N)[:, 0])
+    runs = {}
+    for sd, tdt in (("f32", torch.float32), (state_dtype, torch.bfloat16 if state_dtype == "bf16" else torch.float32)):
+        with Pool(1, H, len(lengths), state_dtype=sd) as pool:
+            pool.states[:, 0] = torch.from_numpy(S0).cuda().to(tdt)
+            o = pool.prefill(0, i32(range(len(lengths))), i32(cu), *dev, max_seqlen=max(lengths),
+                             sequential=True)
+            assert pool.device_status() == 0
+            runs[sd] = (o.clone(), pool.states[:, 0].clone())
+    o_ref, S_ref = oracle.prefill(S0.astype(np.float64), cu, *host_inputs(ins))
+    assert rel(runs["f32"][0].cpu().numpy(), o_ref) < SEQ_PREFILL_TOL
+    assert rel(runs["f32"][1].cpu().numpy(), S_ref) < SEQ_PREFILL_TOL
+    if state_dtype == "bf16":
+        assert torch.equal(runs["bf16"][0], runs["f32"][0])
+        assert torch.equal(runs["bf16"][1], runs["f32"][1].to(torch.bfloat16))
