@@ -28,7 +28,7 @@ def _inputs(seed, B, K, H, N, dtype):
     return host, dev
 
 
-@pytest.mark.parametrize("K", [1, 3, 8])
+@pytest.mark.parametrize("K", [1, 3, 8, 13])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("snaps", [False, True])
 def test_decode_multi_matches_oracle(K, dtype, snaps):
