@@ -126,3 +126,32 @@ def test_snapshot_and_resume_is_bit_identical(sequential):
     ob, sb = run(True)
     assert torch.equal(oa, ob)
     assert torch.equal(sa, sb)
+
+
+def test_verbs_past_one_launch():
+    """More ids than one launch covers: create zeroes from host ids 512 at a time,
+    fork and reset take device ids 65535 per launch."""
+    n, half = 140000, 70000
+    with Pool(1, 1, n) as pool:
+        _fill_random(pool, 7)
+        before = pool.states.clone()
+        created = pool.create(600)
+        assert pool.device_status() == 0
+        c = torch.as_tensor(created, dtype=torch.long, device="cuda")
+        assert bool((pool.states[c] == 0).all())
+        others = torch.ones(n, dtype=torch.bool, device="cuda")
+        others[c] = False
+        assert torch.equal(pool.states[others], before[others])
+
+        perm = torch.as_tensor(np.random.default_rng(3).permutation(n).astype(np.int32), device="cuda")
+        src, dst = perm[:half], perm[half:]
+        mid = pool.states.clone()
+        pool.fork(src, dst)
+        assert pool.device_status() == 0
+        assert torch.equal(pool.states[dst.long()], mid[src.long()])
+        assert torch.equal(pool.states[src.long()], mid[src.long()])
+
+        pool.reset(dst)
+        assert pool.device_status() == 0
+        assert bool((pool.states[dst.long()] == 0).all())
+        assert torch.equal(pool.states[src.long()], mid[src.long()])
