@@ -48,7 +48,9 @@
  *     WKV7_ERR_UNSUPPORTED.
  *   - Kernels are launched with programmatic dependent launch: a kernel may
  *     begin launching while the previous one in its stream drains, but waits
- *     for all earlier work in the stream before it touches memory, so stream
+ *     for all earlier work in the stream before it reads or writes anything
+ *     that work may produce (before that, decode only reads its slot ids, which
+ *     no library kernel writes, and prefetches state lines into L2), so stream
  *     order is kept exactly as with ordinary launches.
  */
 #ifndef WKV7_H

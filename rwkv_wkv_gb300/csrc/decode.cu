@@ -21,23 +21,37 @@
 namespace wkv7 {
 namespace {
 
+// CTAs that can be resident when a kernel starts launching before its
+// predecessor ends (152 SMs, up to 8 of these CTAs each); only they prefetch.
+constexpr int kFirstWaveCtas = 152 * 8;
+
 template <bool BF16>
 __global__ void __launch_bounds__(256) decode_kernel(DecodeArgs p) {
-    pdl_prologue();
+    pdl_launch_dependents();
     const int H = p.lv.n_heads;
     const int unit = blockIdx.x;
     const int bi = unit / H;
     const int h = unit - bi * H;
-    const int slot = __ldg(p.slot_ids + bi);
-    if (slot < 0 || slot >= p.lv.n_slots) {
-        if (threadIdx.x == 0) flag_status(p.lv.status, WKV7_DEV_BAD_SLOT);
-        return;
-    }
-    float *S = p.lv.states + static_cast<size_t>(slot) * p.lv.slot_stride + p.lv.layer_off +
-               static_cast<size_t>(h) * kHeadFloats;
     const int tid = threadIdx.x;
     const int c = (tid & 15) * 4;  // first key column held by this thread
     const int row0 = tid >> 4;     // value rows row0 + 16*m
+    // Before waiting for the previous kernel: the slot id (no kernel of the library
+    // writes an id array) and, in the CTAs that can be resident while the previous
+    // kernel drains, an L2 prefetch of the unit's state rows (it only warms L2), so
+    // that the first wave's loads after the wait hit L2.
+    const int slot = __ldg(p.slot_ids + bi);
+    const bool ok = slot >= 0 && slot < p.lv.n_slots;
+    float *S = p.lv.states + static_cast<size_t>(ok ? slot : 0) * p.lv.slot_stride + p.lv.layer_off +
+               static_cast<size_t>(h) * kHeadFloats;
+    if (ok && unit < kFirstWaveCtas && (tid & 7) == 0) {  // one prefetch per 128-byte line
+#pragma unroll
+        for (int m = 0; m < 4; ++m) prefetch_l2(S + (row0 + 16 * m) * kHeadSize + c);
+    }
+    pdl_wait();
+    if (!ok) {
+        if (tid == 0) flag_status(p.lv.status, WKV7_DEV_BAD_SLOT);
+        return;
+    }
 
     float4 s[4];
 #pragma unroll
@@ -101,21 +115,29 @@ constexpr int kBf16RowStep = kHeadSize / kBf16Rows;
 
 template <bool BF16>
 __global__ void __launch_bounds__(kBf16Threads) decode_bf16state_kernel(DecodeArgs p) {
-    pdl_prologue();
+    pdl_launch_dependents();
     const int H = p.lv.n_heads;
     const int unit = blockIdx.x;
     const int bi = unit / H;
     const int h = unit - bi * H;
-    const int slot = __ldg(p.slot_ids + bi);
-    if (slot < 0 || slot >= p.lv.n_slots) {
-        if (threadIdx.x == 0) flag_status(p.lv.status, WKV7_DEV_BAD_SLOT);
-        return;
-    }
-    uint16_t *S = reinterpret_cast<uint16_t *>(p.lv.states) + static_cast<size_t>(slot) * p.lv.slot_stride +
-                  p.lv.layer_off + static_cast<size_t>(h) * kHeadFloats;
     const int tid = threadIdx.x;
     const int c = (tid & 7) * 8;  // first key column held by this thread
     const int row0 = tid >> 3;    // value rows row0 + kBf16RowStep*m
+    // the slot id and an L2 prefetch of the state rows before the wait, as in decode_kernel
+    const int slot = __ldg(p.slot_ids + bi);
+    const bool ok = slot >= 0 && slot < p.lv.n_slots;
+    uint16_t *S = reinterpret_cast<uint16_t *>(p.lv.states) +
+                  static_cast<size_t>(ok ? slot : 0) * p.lv.slot_stride + p.lv.layer_off +
+                  static_cast<size_t>(h) * kHeadFloats;
+    if (ok && unit < kFirstWaveCtas && (tid & 7) == 0) {  // one 128-byte row per prefetch
+#pragma unroll
+        for (int m = 0; m < kBf16Rows; ++m) prefetch_l2(S + (row0 + kBf16RowStep * m) * kHeadSize);
+    }
+    pdl_wait();
+    if (!ok) {
+        if (tid == 0) flag_status(p.lv.status, WKV7_DEV_BAD_SLOT);
+        return;
+    }
 
     uint4 raw[kBf16Rows];
 #pragma unroll

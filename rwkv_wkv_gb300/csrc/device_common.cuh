@@ -101,11 +101,22 @@ __device__ __forceinline__ void st_global_v8(float *p, const float *v) {
 // Programmatic dependent launch.  A kernel launched with launch_pdl lets the next
 // kernel in its stream start launching once all of its CTAs have begun
 // (launch_dependents), and itself waits for everything before it in the stream
-// to complete and become visible (wait) before touching global memory, so only
-// the launch latency and CTA dispatch overlap the previous kernel's tail.
-__device__ __forceinline__ void pdl_prologue() {
+// to complete and become visible (wait) before it reads or writes anything that
+// earlier work may produce, so only the launch latency, CTA dispatch and (in the
+// decode kernels) a slot-id read and an L2 prefetch overlap the previous kernel's
+// tail.
+__device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_prologue() {
+    pdl_launch_dependents();
+    pdl_wait();
+}
+
+// Warm L2 with the 128-byte line at p (no visible effect: safe before pdl_wait).
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 template <typename... Params, typename... Args>
