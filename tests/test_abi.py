@@ -38,6 +38,12 @@ def test_header_declarations_are_all_exported(lib):
     assert set(declared) == set(wkv7.exported_symbols())
 
 
+def test_wait_timeout_test_hook_is_host_only(lib):
+    """The bounded-wait test hook only sets a process-wide flag (no CUDA call)."""
+    assert lib.wkv7_test_force_wait_timeout(1) == 0
+    assert lib.wkv7_test_force_wait_timeout(0) == 0
+
+
 def test_version_and_strings(lib):
     assert lib.wkv7_version() == 1
     assert lib.wkv7_status_string(0) == b"ok"
