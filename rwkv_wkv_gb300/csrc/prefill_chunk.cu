@@ -51,9 +51,12 @@
 // into tensor memory as bf16; they never touch shared memory.
 // Accumulators live in tensor memory (256 columns); the float32 state leaves
 // the accumulator each chunk, is written back as the next chunk's bf16 hi/lo
-// operand pair and, after the last chunk, to the slot in float32.
-// All waits are bounded; a timeout flags WKV7_DEV_WAIT_TIMEOUT and the CTA
-// releases its tensor memory and exits.
+// operand pair and, after the last chunk, to the slot (float32, or rounded to
+// bf16 on a bf16-state pool; checkpoints likewise).  Each thread's 128-byte
+// output row leaves in 32-byte stores when o allows them.
+// All waits are bounded (by an argument: about 2 s, or about 50 ms under the
+// test hook); a timeout flags WKV7_DEV_WAIT_TIMEOUT and the CTA releases its
+// tensor memory and exits.
 #include <cuda_bf16.h>
 
 #include "device_common.cuh"
