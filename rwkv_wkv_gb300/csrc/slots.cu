@@ -1,10 +1,12 @@
 // Slot verbs as device copies ("wkvm: state-slot inference for RWKV, GDN and
 // Mamba hybrids", "The allocation unit wkvm changes": create, snapshot, fork,
 // hibernate, resume; hibernate and resume move slots to and from a pinned host
-// buffer that the kernel reaches through its mapped device address).  A slot is one contiguous range of float32 states (every layer and
-// head), so every verb is a whole-range copy or fill.  Each CTA moves 32 KiB
-// of one slot with 128-bit streaming loads/stores; grid.y walks the slot
-// pairs.  HBM-bound: 2 x slot_bytes per copied slot, 1 x per zeroed slot.
+// buffer that the kernel reaches through its mapped device address).  A slot is
+// one contiguous range of states (every layer and head; float32 or bf16, moved
+// here as 16-byte words, so the verbs are bit-exact for either), so every verb
+// is a whole-range copy or fill.  Each CTA moves 32 KiB of one slot with
+// 128-bit streaming loads/stores; grid.y walks the slot pairs.  HBM-bound:
+// 2 x slot_bytes per copied slot, 1 x per zeroed slot.
 #include "device_common.cuh"
 #include "wkv7_internal.h"
 
