@@ -6,6 +6,8 @@
 // decode's: 256 threads per (row, head), thread t holding the float4 at byte
 // offset 16*t + 4096*m of the 16 KiB state, row reductions as xor shuffles
 // inside a half-warp.
+#include <type_traits>
+
 #include "device_common.cuh"
 #include "wkv7_internal.h"
 
@@ -15,9 +17,10 @@ namespace {
 // K consecutive tokens per (row, head) with the state held in registers
 // throughout: the state is read and written once per call instead of once per
 // token, and only the inputs and readouts scale with K.  The inputs of up to
-// kGroup tokens are staged in shared memory (float32) by the whole CTA at once,
-// so their loads overlap each other and the state load instead of sitting on
-// the token chain.  With per-token snapshots the state after every token is also
+// kGroup tokens are staged in shared memory (as they come, bf16 or float32) by
+// the whole CTA at once, so their loads overlap each other and the state load
+// instead of sitting on the token chain.  With per-token snapshots the state
+// after every token is also
 // streamed to its snapshot (the rollback points of a speculative verify: the
 // rvLLM README, "Speculative decoding", verifies K+1 tokens in one pass; wkvm's
 // fork/restore verbs then keep or drop them).  On a bf16-state pool (SBF16) the
@@ -27,9 +30,40 @@ namespace {
 constexpr int kGroup = 8;  // tokens staged per pass
 enum { kR = 0, kW, kK, kV, kA, kB, kInputs };
 
+// Staged inputs of one group of tokens: bf16 inputs stay bf16 in shared memory
+// (half the bytes each token's broadcast reads move), float32 ones float32.
+template <bool BF16>
+struct Staged {
+    using Elem = typename std::conditional<BF16, uint16_t, float>::type;
+    Elem x[kGroup][kInputs][kHeadSize];
+    __device__ __forceinline__ float4 vec4(int t, int i, int c) const {  // elements c..c+3
+        if constexpr (BF16) {
+            const uint2 u = *reinterpret_cast<const uint2 *>(&x[t][i][c]);
+            return make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
+        } else {
+            return *reinterpret_cast<const float4 *>(&x[t][i][c]);
+        }
+    }
+    __device__ __forceinline__ float one(int t, int i, int e) const {
+        if constexpr (BF16)
+            return __uint_as_float(static_cast<uint32_t>(x[t][i][e]) << 16);
+        else
+            return x[t][i][e];
+    }
+    // four consecutive input elements from global memory, as they are stored here
+    __device__ __forceinline__ void stage4(int t, int i, int c, const void *src, size_t off) {
+        if constexpr (BF16)
+            *reinterpret_cast<uint2 *>(&x[t][i][c]) =
+                __ldg(reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(src) + off));
+        else
+            *reinterpret_cast<float4 *>(&x[t][i][c]) =
+                __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(src) + off));
+    }
+};
+
 template <bool BF16, bool SNAPS, bool SBF16>
 __global__ void __launch_bounds__(256, (SNAPS && SBF16) ? 4 : 5) decode_multi_kernel(DecodeMultiArgs p) {
-    __shared__ __align__(16) float xs[kGroup][kInputs][kHeadSize];
+    __shared__ __align__(16) Staged<BF16> xs;
     pdl_prologue();
     const int H = p.lv.n_heads;
     const int unit = blockIdx.x;
@@ -71,14 +105,13 @@ __global__ void __launch_bounds__(256, (SNAPS && SBF16) ? 4 : 5) decode_multi_ke
             const int x = rem >> 4, q = rem & 15;
             const void *src = x == kR ? p.in.r : x == kW ? p.in.w : x == kK ? p.in.k
                             : x == kV ? p.in.v : x == kA ? p.in.a : p.in.b;
-            const float4 val = load4<BF16>(src, io_of(g0 + t) + 4 * q);
-            reinterpret_cast<float4 *>(&xs[t][x][0])[q] = val;
+            xs.stage4(t, x, 4 * q, src, io_of(g0 + t) + 4 * q);
         }
         __syncthreads();
 #pragma unroll 1
         for (int t = 0; t < ng; ++t) {
             const int k = g0 + t;
-            const float4 a4 = *reinterpret_cast<const float4 *>(&xs[t][kA][c]);
+            const float4 a4 = xs.vec4(t, kA, c);
             float hs[4];
 #pragma unroll
             for (int m = 0; m < 4; ++m) hs[m] = dot4(s[m], a4);
@@ -86,14 +119,14 @@ __global__ void __launch_bounds__(256, (SNAPS && SBF16) ? 4 : 5) decode_multi_ke
             for (int off = 8; off >= 1; off >>= 1)
 #pragma unroll
                 for (int m = 0; m < 4; ++m) hs[m] += __shfl_xor_sync(0xffffffffu, hs[m], off);
-            const float4 w4 = *reinterpret_cast<const float4 *>(&xs[t][kW][c]);
-            const float4 b4 = *reinterpret_cast<const float4 *>(&xs[t][kB][c]);
-            const float4 k4 = *reinterpret_cast<const float4 *>(&xs[t][kK][c]);
-            const float4 r4 = *reinterpret_cast<const float4 *>(&xs[t][kR][c]);
+            const float4 w4 = xs.vec4(t, kW, c);
+            const float4 b4 = xs.vec4(t, kB, c);
+            const float4 k4 = xs.vec4(t, kK, c);
+            const float4 r4 = xs.vec4(t, kR, c);
             float os[4];
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
-                const float vm = xs[t][kV][row0 + 16 * m];
+                const float vm = xs.one(t, kV, row0 + 16 * m);
                 s[m].x = fmaf(s[m].x, w4.x, fmaf(hs[m], b4.x, vm * k4.x));
                 s[m].y = fmaf(s[m].y, w4.y, fmaf(hs[m], b4.y, vm * k4.y));
                 s[m].z = fmaf(s[m].z, w4.z, fmaf(hs[m], b4.z, vm * k4.z));
