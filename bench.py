@@ -93,7 +93,7 @@ KERNEL_SOURCES = {
     "prefill": ("prefill_chunk_kernel.mixed_prefill_64seq.md",
                 ["prefill_chunk.cu", "sm100_ptx.cuh", "device_common.cuh", "wkv7_internal.h"]),
     "decode": ("decode_kernel.decode_12L_12H_256of1024.md",
-               ["decode.cu", "device_common.cuh", "wkv7_internal.h"]),
+               ["decode.cu", "device_common.cuh", "wkv7_internal.h", "row_sums.cuh"]),
 }
 
 

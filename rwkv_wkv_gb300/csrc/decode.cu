@@ -11,11 +11,12 @@
 // 16*t + 4096*m (m = 0..3) of the state, i.e. key columns 4*(t%16)..+3 of
 // value rows t/16 + 16*m.  Each load/store instruction of the CTA covers 4 KiB
 // of contiguous memory.  A row's 64 columns sit in one half-warp, so both
-// row reductions (S a before the update, S' r after it) are 4-level xor
-// shuffles inside the half-warp, and the state never touches shared memory.
+// row reductions (S a before the update, S' r after it) stay inside the
+// half-warp (row_sums.cuh), and the state never touches shared memory.
 #include <cuda_bf16.h>
 
 #include "device_common.cuh"
+#include "row_sums.cuh"
 #include "wkv7_internal.h"
 
 namespace wkv7 {
@@ -72,10 +73,7 @@ __global__ void __launch_bounds__(256) decode_kernel(DecodeArgs p) {
     float hs[4];
 #pragma unroll
     for (int m = 0; m < 4; ++m) hs[m] = dot4(s[m], a4);
-#pragma unroll
-    for (int off = 8; off >= 1; off >>= 1)
-#pragma unroll
-        for (int m = 0; m < 4; ++m) hs[m] += __shfl_xor_sync(0xffffffffu, hs[m], off);
+    row_sums4(hs, tid & 31);
 
     // decay, delta write, kv write; then the readout on the new state
     float os[4];
@@ -90,14 +88,8 @@ __global__ void __launch_bounds__(256) decode_kernel(DecodeArgs p) {
 #pragma unroll
     for (int m = 0; m < 4; ++m)
         __stcs(reinterpret_cast<float4 *>(S + (row0 + 16 * m) * kHeadSize + c), s[m]);
-#pragma unroll
-    for (int off = 8; off >= 1; off >>= 1)
-#pragma unroll
-        for (int m = 0; m < 4; ++m) os[m] += __shfl_xor_sync(0xffffffffu, os[m], off);
-    if ((tid & 15) == 0) {
-#pragma unroll
-        for (int m = 0; m < 4; ++m) p.in.o[io + row0 + 16 * m] = os[m];
-    }
+    const float ou = reduce_scatter4(os, tid & 15);  // row ((tid >> 2) & 3)'s readout
+    if ((tid & 3) == 0) p.in.o[io + row0 + 16 * ((tid >> 2) & 3)] = ou;
 }
 
 // Decode over a pool whose states are stored in bf16 (half the bytes of the

@@ -9,6 +9,7 @@
 #include <type_traits>
 
 #include "device_common.cuh"
+#include "row_sums.cuh"
 #include "wkv7_internal.h"
 
 namespace wkv7 {
@@ -60,21 +61,6 @@ struct Staged {
                 __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(src) + off));
     }
 };
-
-// Four row sums over the 16 lanes of a half-warp (v[m]: this lane's partial of
-// row m), as a reduce-scatter: lane l ends with the sum of row (l >> 2) & 3.  The
-// pairwise additions (partners at xor 8, 4, 2, 1, in that order) are those of a
-// butterfly over each row, so the sums equal the butterfly's bit for bit, in 5
-// shuffles instead of 16.
-__device__ __forceinline__ float reduce_scatter4(const float (&v)[4], int hl) {
-    const bool b3 = (hl & 8) != 0, b2 = (hl & 4) != 0;
-    const float t0 = (b3 ? v[2] : v[0]) + __shfl_xor_sync(0xffffffffu, b3 ? v[0] : v[2], 8);
-    const float t1 = (b3 ? v[3] : v[1]) + __shfl_xor_sync(0xffffffffu, b3 ? v[1] : v[3], 8);
-    float u = (b2 ? t1 : t0) + __shfl_xor_sync(0xffffffffu, b2 ? t0 : t1, 4);
-    u += __shfl_xor_sync(0xffffffffu, u, 2);
-    u += __shfl_xor_sync(0xffffffffu, u, 1);
-    return u;
-}
 
 template <bool BF16, bool SNAPS, bool SBF16>
 __global__ void __launch_bounds__(256, (SNAPS && SBF16) ? 4 : 5) decode_multi_kernel(DecodeMultiArgs p) {
@@ -130,11 +116,7 @@ __global__ void __launch_bounds__(256, (SNAPS && SBF16) ? 4 : 5) decode_multi_ke
             float hs[4];
 #pragma unroll
             for (int m = 0; m < 4; ++m) hs[m] = dot4(s[m], a4);
-            {  // every lane needs all four sums: reduce-scatter, then broadcast
-                const float u = reduce_scatter4(hs, tid & 15);
-#pragma unroll
-                for (int m = 0; m < 4; ++m) hs[m] = __shfl_sync(0xffffffffu, u, (tid & 16) | (4 * m));
-            }
+            row_sums4(hs, tid & 31);  // every lane needs all four sums
             const float4 w4 = xs.vec4(t, kW, c);
             const float4 b4 = xs.vec4(t, kB, c);
             const float4 k4 = xs.vec4(t, kK, c);
