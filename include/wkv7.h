@@ -192,11 +192,15 @@ wkv7_status wkv7_slot_reset(wkv7_pool *pool, const int32_t *slot_ids_dev, int32_
                             cudaStream_t stream);
 
 /* snapshot: copy slot slot_ids_dev[i] -> snapshot snap_ids_dev[i], i < n, bit
- * for bit.  restore (the verb "resume"): snapshot -> slot.  fork: slot
- * src_ids_dev[i] -> slot dst_ids_dev[i].  ("The allocation unit wkvm
- * changes": a fixed-size slot can be copied, parked and restored cheaply.)
- * Whole-slot copies of every layer and head.  Out-of-range ids are skipped and
- * flagged WKV7_DEV_BAD_SLOT.  n == 0 is a no-op. */
+ * for bit.  restore: snapshot -> slot (rolls the slot back to the snapshot).
+ * fork: slot src_ids_dev[i] -> slot dst_ids_dev[i].  ("The allocation unit
+ * wkvm changes": a fixed-size slot can be copied, parked and restored
+ * cheaply; parking in host memory is wkv7_slot_hibernate / wkv7_slot_resume.)
+ * Whole-slot copies of every layer and head; the id arrays are caller-owned
+ * device int32 arrays of n entries.  Errors: INVALID_ARG (NULL pool or id
+ * array with n > 0, n < 0, n larger than the destination table, snapshot or
+ * restore on a pool without a snapshot store), CUDA.  Device: out-of-range ids
+ * are skipped and flagged WKV7_DEV_BAD_SLOT.  n == 0 is a no-op. */
 wkv7_status wkv7_slot_snapshot(wkv7_pool *pool, const int32_t *slot_ids_dev,
                                const int32_t *snap_ids_dev, int32_t n, cudaStream_t stream);
 wkv7_status wkv7_slot_restore(wkv7_pool *pool, const int32_t *snap_ids_dev,
