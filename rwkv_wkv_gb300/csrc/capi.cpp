@@ -321,6 +321,7 @@ static wkv7_status copy_verb(wkv7_pool *pool, float *dst, int n_dst, const int32
     if (!pool || n < 0) return WKV7_ERR_INVALID_ARG;  // null ids: checked by the callers
     if (n == 0) return WKV7_OK;
     if (n_dst == 0 || n_src == 0) return WKV7_ERR_INVALID_ARG;  // no snapshot store
+    if (n > n_dst) return WKV7_ERR_INVALID_ARG;  // destinations must be distinct
     wkv7::CopyArgs a;
     a.dst = dst;
     a.src = src;

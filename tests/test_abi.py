@@ -177,6 +177,8 @@ def test_host_checks_return_before_launch(lib):
         assert lib.wkv7_slot_fork(h, None, x, 1, None) == 1
         assert lib.wkv7_slot_snapshot(h, x, x, -1, None) == 1
         assert lib.wkv7_slot_restore(h, x, x, 0, None) == 0
+        assert lib.wkv7_slot_snapshot(h, x, x, 5, None) == 1  # more than the 4 snapshots
+        assert lib.wkv7_slot_fork(h, x, x, 9, None) == 1       # more than the 8 slots
         # hibernate / resume: NULL ids or host buffer, n < 0, a host buffer too small
         sb = lib.wkv7_slot_bytes(h)
         assert lib.wkv7_slot_hibernate(h, None, 1, x, sb, None) == 1
