@@ -54,7 +54,8 @@ def _load():
             lib = ctypes.CDLL(build())
             dp = ctypes.POINTER(ctypes.c_double)
             ll = ctypes.c_longlong
-            for name in ("wkv7_oracle_sequential", "wkv7_oracle_matprod"):
+            for name in ("wkv7_oracle_sequential", "wkv7_oracle_matprod",
+                         "wkv7_oracle_sequential_decay_first"):
                 f = getattr(lib, name)
                 f.restype = ctypes.c_int
                 f.argtypes = [ctypes.c_int, ctypes.c_int, dp, ll, ll] + [dp] * 7
@@ -96,9 +97,19 @@ def _one_head(fn_name, S0, r, w, k, v, a, b, extra=()):
     return o, S
 
 
-def sequential(S0, r, w, k, v, a, b):
-    """Sequential recurrence on one head. Returns (o [T,N], S_T [N,N])."""
-    return _one_head("wkv7_oracle_sequential", S0, r, w, k, v, a, b)
+def sequential(S0, r, w, k, v, a, b, reading: str = "A"):
+    """Sequential recurrence on one head. Returns (o [T,N], S_T [N,N]).
+
+    reading "A" (the default, the one the build follows): h = S a is read on the
+    state before the decay.  reading "B": the order of the RWKV-X pseudo-code
+    ("WKV-7 Kernel (Generalized Delta Rule)"), which decays the state first and
+    then reads h = (S diag(w)) a.  "B" exists only to measure how far the two
+    readings lie apart; nothing else uses it."""
+    if reading == "A":
+        return _one_head("wkv7_oracle_sequential", S0, r, w, k, v, a, b)
+    if reading == "B":
+        return _one_head("wkv7_oracle_sequential_decay_first", S0, r, w, k, v, a, b)
+    raise ValueError(f"reading must be 'A' or 'B', not {reading!r}")
 
 
 def matprod(S0, r, w, k, v, a, b):
@@ -265,11 +276,51 @@ def decode_multi(states, r, w, k, v, a, b, n_threads: int = 1):
 
 
 def rel_err(x, ref) -> float:
-    """Normwise-max relative error: max|x - ref| / max|ref| (0 when both are 0)."""
+    """Normwise-max relative error of one tensor: max|x - ref| / max|ref|, taken
+    over all entries (the plain absolute max when ref is all zero).  The shapes
+    must match exactly: no broadcasting."""
     x = np.asarray(x, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
+    if x.shape != ref.shape:
+        raise ValueError(f"rel_err: shape {x.shape} against reference shape {ref.shape}")
     den = float(np.max(np.abs(ref))) if ref.size else 0.0
     num = float(np.max(np.abs(x - ref))) if ref.size else 0.0
     if den == 0.0:
         return num
     return num / den
+
+
+def rel_err_slices(x, ref, lead: int) -> np.ndarray:
+    """rel_err of every slice over the first `lead` axes: for x, ref of shape
+    [d0, .., d_{lead-1}, ...] the array [d0, .., d_{lead-1}] of normwise-max
+    errors of x[i0, .., i_{lead-1}] against ref[i0, .., i_{lead-1}], so that a
+    slice whose values are small is judged against its own scale."""
+    x = np.asarray(x, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    if x.shape != ref.shape:
+        raise ValueError(f"rel_err_slices: shape {x.shape} against reference shape {ref.shape}")
+    if lead < 0 or lead > ref.ndim:
+        raise ValueError(f"rel_err_slices: lead {lead} for {ref.ndim} axes")
+    out_shape = ref.shape[:lead]
+    xf = x.reshape(int(np.prod(out_shape, dtype=np.int64)), -1)
+    rf = ref.reshape(xf.shape)
+    if rf.shape[1] == 0:
+        return np.zeros(out_shape)
+    num = np.max(np.abs(xf - rf), axis=1)
+    den = np.max(np.abs(rf), axis=1)
+    res = np.where(den > 0, num / np.where(den > 0, den, 1.0), num)
+    return res.reshape(out_shape)
+
+
+def elementwise_rel(x, ref, floor: float = 1e-6) -> np.ndarray:
+    """Elementwise relative error |x - ref| / (|ref| + floor * max|ref|): the
+    per-entry companion of rel_err.  The floor (relative to the tensor's largest
+    entry) keeps entries that are zero, or nearly, from dividing by zero."""
+    x = np.asarray(x, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    if x.shape != ref.shape:
+        raise ValueError(f"elementwise_rel: shape {x.shape} against reference shape {ref.shape}")
+    scale = float(np.max(np.abs(ref))) if ref.size else 0.0
+    den = np.abs(ref) + floor * scale
+    diff = np.abs(x - ref)
+    return np.where(den > 0, diff / np.where(den > 0, den, 1.0), diff)

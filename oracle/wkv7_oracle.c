@@ -87,6 +87,50 @@ ORACLE_API int wkv7_oracle_sequential(int N, int T, double *S, long long base,
     return 0;
 }
 
+/* The other order the pages leave open (RWKV-X Architecture, "WKV-7 Kernel
+ * (Generalized Delta Rule)", whose pseudo-code decays the state first and then
+ * reads a @ state): S' = S diag(w);  h = S' a;  S'' = S' + h b^T + v k^T;
+ * o = S'' r.  Not the reading the build follows (that one reads h on the state
+ * before the decay, above); kept only so that the difference between the two
+ * readings can be measured.  One token on one head; h is caller scratch. */
+static void seq_token_decay_first(int N, double *S, const double *r, const double *w,
+                                  const double *k, const double *v, const double *a,
+                                  const double *b, double *o, double *h)
+{
+    for (int i = 0; i < N; ++i)                   /* S = S diag(w) */
+        for (int j = 0; j < N; ++j) S[i * N + j] *= w[j];
+    for (int i = 0; i < N; ++i) {                 /* h = S a (decayed state) */
+        double acc = 0.0;
+        for (int j = 0; j < N; ++j) acc += S[i * N + j] * a[j];
+        h[i] = acc;
+    }
+    for (int i = 0; i < N; ++i)                   /* S += h b^T + v k^T */
+        for (int j = 0; j < N; ++j) S[i * N + j] += h[i] * b[j] + v[i] * k[j];
+    for (int i = 0; i < N; ++i) {                 /* o = S r */
+        double acc = 0.0;
+        for (int j = 0; j < N; ++j) acc += S[i * N + j] * r[j];
+        o[i] = acc;
+    }
+}
+
+ORACLE_API int wkv7_oracle_sequential_decay_first(int N, int T, double *S, long long base,
+                                                  long long tok_stride, const double *r,
+                                                  const double *w, const double *k,
+                                                  const double *v, const double *a,
+                                                  const double *b, double *o)
+{
+    if (N <= 0 || T < 0) return 1;
+    double *h = (double *)malloc(sizeof(double) * (size_t)N);
+    if (!h) return 2;
+    for (int t = 0; t < T; ++t) {
+        long long off = base + (long long)t * tok_stride;
+        seq_token_decay_first(N, S, r + off, w + off, k + off, v + off, a + off, b + off,
+                              o + off, h);
+    }
+    free(h);
+    return 0;
+}
+
 /* Many independent units (heads x sequences, or heads x batch rows), split over
  * n_threads POSIX threads.  Unit u owns S + u*N*N, starts at base[u] and runs
  * T[u] tokens.  Used for batched parity references and for CPU timing. */

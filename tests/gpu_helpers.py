@@ -31,6 +31,44 @@ def rel(x, ref):
     return oracle.rel_err(np.asarray(x, dtype=np.float64), ref)
 
 
+# Elementwise companion of the normwise bound: its median must stay under the
+# path's tolerance and its 99.9th percentile under 100 times it.  Entries near
+# zero are judged against a floor of 1e-6 of the tensor's largest magnitude, so
+# the upper percentiles are those entries' rounding, not a wrong element.
+ELEM_P999_FACTOR = 100.0
+
+
+def check_parity(x, ref, tol, lead=0, cu=None, elementwise=False, what=""):
+    """Assert x against the oracle's ref: the normwise-max error of the whole
+    tensor and of every slice (each over the first `lead` axes, or, with cu,
+    each (sequence, head) of a packed [tokens][heads][...] tensor) below tol;
+    with `elementwise`, the median elementwise error below tol and its 99.9th
+    percentile below ELEM_P999_FACTOR * tol.  Returns the figures."""
+    import oracle
+    x = np.asarray(x, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    out = {"normwise": oracle.rel_err(x, ref)}
+    assert out["normwise"] < tol, (what, out)
+    if cu is not None:
+        worst = 0.0
+        for s in range(len(cu) - 1):
+            a, b = int(cu[s]), int(cu[s + 1])
+            if b > a:
+                per = oracle.rel_err_slices(np.swapaxes(x[a:b], 0, 1), np.swapaxes(ref[a:b], 0, 1), 1)
+                worst = max(worst, float(per.max()))
+        out["worst_slice"] = worst
+    elif lead:
+        out["worst_slice"] = float(oracle.rel_err_slices(x, ref, lead).max())
+    if "worst_slice" in out:
+        assert out["worst_slice"] < tol, (what, out)
+    if elementwise:
+        e = oracle.elementwise_rel(x, ref)
+        out["elem_median"] = float(np.median(e))
+        out["elem_p999"] = float(np.quantile(e, 0.999))
+        assert out["elem_median"] < tol and out["elem_p999"] < ELEM_P999_FACTOR * tol, (what, out)
+    return out
+
+
 def sampled_head_inputs(seed: int, tag: str, n_tok: int, H: int, N: int, heads,
                         device="cuda"):
     """Full-size bf16 device inputs whose `heads` carry seeded host values (also

@@ -1,5 +1,6 @@
 """The seeded input generator: determinism, counter addressing, rounding."""
 import numpy as np
+import pytest
 
 import workloads as wl
 
@@ -31,6 +32,25 @@ def test_bf16_round_to_nearest_even():
     for val, bits in cases.items():
         assert int(wl.bf16_bits(np.array([val]))[0]) == bits, val
     assert wl.bf16_to_f32(np.array([0x3F80], dtype=np.uint16))[0] == one
+
+
+def test_bf16_rounding_is_one_step_from_float64():
+    """A float64 value just above a bf16 tie rounds up; a detour through float32
+    would first round it onto the tie and then to even (down)."""
+    x = 1.0 + 2.0 ** -8 + 2.0 ** -40        # 1 + half a bf16 spacing + a little
+    assert np.float32(x) == np.float32(1.0 + 2.0 ** -8)  # float32 lands on the tie
+    assert int(wl.bf16_bits(np.array([x]))[0]) == 0x3F81
+    # subnormal spacing 2^-133, overflow to inf, signs, zero
+    assert int(wl.bf16_bits(np.array([2.0 ** -133]))[0]) == 0x0001
+    assert int(wl.bf16_bits(np.array([1.5 * 2.0 ** -133]))[0]) == 0x0002   # tie -> even
+    assert int(wl.bf16_bits(np.array([-2.0 ** -134]))[0]) == 0x8000        # tie -> even (zero)
+    assert int(wl.bf16_bits(np.array([3.4e38]))[0]) == 0x7F80              # inf
+    assert int(wl.bf16_bits(np.array([-0.0]))[0]) == 0x8000
+    # agrees with torch's float32 -> bf16 conversion (nearest even) on float32 inputs
+    torch = pytest.importorskip("torch")
+    f = np.random.default_rng(3).standard_normal(100_000).astype(np.float32) * 3.0
+    want = torch.from_numpy(f).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(wl.bf16_bits(f), want)
 
 
 def test_token_inputs_recipe():

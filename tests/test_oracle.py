@@ -394,3 +394,49 @@ def test_bf16_state_decode_is_the_float64_step_then_rounding():
     o2, S2 = oracle.decode_step(S0, r, w, k, v, a, b)
     assert np.array_equal(o1, o2)
     assert np.array_equal(S1, oracle.round_bf16(S2)) and not np.array_equal(S1, S2)
+
+
+# ------------------------------------------------- the other order (reading B)
+
+def test_decay_first_reading_hand_worked(golden_dir):
+    """The oracle's switch for the decay-first order of the RWKV-X pseudo-code
+    reproduces its own hand-worked example, and the shared example tells the two
+    readings apart at the first token (the default stays reading A)."""
+    g = _golden(golden_dir)
+    gb = {}
+    with open(os.path.join(golden_dir, "wkv7_two_tokens_n2_decay_first.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                key, *nums = line.split()
+                gb[key] = np.array([float(x) for x in nums])
+    S0 = np.stack([g["S0_0"], g["S0_1"]])
+    ins = [np.stack([g[f"{n}_t1"], g[f"{n}_t2"]]) for n in ("r", "w", "k", "v", "a", "b")]
+    o1, S1 = oracle.sequential(S0, *[x[:1] for x in ins], reading="B")
+    np.testing.assert_array_equal(o1[0], gb["o_t1"])
+    np.testing.assert_array_equal(S1, np.stack([gb["S1_0"], gb["S1_1"]]))
+    o, S2 = oracle.sequential(S0, *ins, reading="B")
+    np.testing.assert_array_equal(o, np.stack([gb["o_t1"], gb["o_t2"]]))
+    np.testing.assert_array_equal(S2, np.stack([gb["S2_0"], gb["S2_1"]]))
+    oa, _ = oracle.sequential(S0, *ins)
+    np.testing.assert_array_equal(oa, np.stack([g["o_t1"], g["o_t2"]]))
+    assert not np.array_equal(oa[0], o[0])
+    with pytest.raises(ValueError):
+        oracle.sequential(S0, *ins, reading="C")
+
+
+def test_decay_first_reading_agrees_where_the_orders_coincide():
+    """With w = 1 (no decay) the two orders are the same map, so the closed forms
+    that cannot tell them apart hold for both; with a generic decay they differ."""
+    rng = np.random.default_rng(7)
+    N, T = 6, 9
+    r, w, k, v, a, b = _rand_inputs(T, N, rng)
+    S0 = rng.standard_normal((N, N))
+    ones = np.ones_like(w)
+    oa, Sa = oracle.sequential(S0, r, ones, k, v, a, b)
+    ob, Sb = oracle.sequential(S0, r, ones, k, v, a, b, reading="B")
+    np.testing.assert_allclose(ob, oa, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(Sb, Sa, rtol=1e-13, atol=1e-13)
+    oa, _ = oracle.sequential(S0, r, w, k, v, a, b)
+    ob, _ = oracle.sequential(S0, r, w, k, v, a, b, reading="B")
+    assert np.max(np.abs(oa - ob)) > 1e-3

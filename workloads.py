@@ -111,11 +111,26 @@ def normals_at(seed: int, tag: str, idx: np.ndarray, mean: float = 0.0,
 # --------------------------------------------------------------------------
 
 def bf16_bits(x: np.ndarray) -> np.ndarray:
-    """Round float64/float32 values to bf16 (nearest, ties to even); uint16 bits."""
-    f = np.ascontiguousarray(x, dtype=np.float32)
-    u = f.view(np.uint32).astype(np.uint64)
-    rounded = (u + np.uint64(0x7FFF) + ((u >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16)
-    return rounded.astype(np.uint16)
+    """Round values to bf16 in one step (nearest, ties to even) and return the
+    uint16 bit patterns.  The input is taken as float64 (float32 values widen
+    exactly), so a float64 draw is rounded once, with no float32 stop on the way.
+
+    A finite x = m 2^e (frexp: 0.5 <= |m| < 1) is a multiple of 2^(e-8) once it
+    is rounded to bf16's 8 significant bits; below 2^-126 the bf16 spacing stays
+    2^-133.  Scaling by a power of two and np.rint (ties to even) are exact, and
+    the rounded value is exactly a float32 whose upper 16 bits are the bf16
+    pattern.  Magnitudes that round past the largest finite bf16 become inf."""
+    v = np.ascontiguousarray(x, dtype=np.float64)
+    out = v.copy()
+    fin = np.isfinite(v) & (v != 0.0)
+    xf = v[fin]
+    _, e = np.frexp(xf)
+    spacing = np.ldexp(1.0, np.maximum(e - 8, -133))
+    y = np.rint(xf / spacing) * spacing
+    y = np.where(np.abs(y) > 3.3895313892515355e38, np.copysign(np.inf, y), y)
+    out[fin] = y
+    f = out.astype(np.float32)  # exact: every bf16 value is a float32 value
+    return (f.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
 
 
 def bf16_to_f32(bits: np.ndarray) -> np.ndarray:
