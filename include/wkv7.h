@@ -22,7 +22,10 @@
  *     slot layout  [layer][head][i][j]  float32 (or bf16, see state_dtype),
  *                  row-major, contiguous
  *     slot bytes   n_layers * n_heads * head_size^2 * 4 (2 for bf16 states)
- *     pool layout  [slot][layer][head][i][j]; snapshots use the same layout
+ *     pool layout  a 256-byte header (the device status word), the slots
+ *                  [slot][layer][head][i][j], the snapshots in the same
+ *                  layout, then the id-validation bitmap (one bit per id of
+ *                  the larger table, rounded up to 256 bytes)
  *
  * Token inputs are packed [rows][n_heads][head_size] (row = batch entry for
  * decode, token for prefill), contiguous, float32 or bf16; outputs o are
@@ -43,7 +46,8 @@
  *     read with wkv7_get_device_status.  Kernels never trap or assert.
  *   - Slot ids within one call must be distinct, and a call's source and
  *     destination sets must not overlap; violating this is a data race whose
- *     result is undefined (not detected on the fast path).
+ *     result is undefined.  The fast paths do not check it;
+ *     wkv7_validate_ids is the debug pass that does.
  *   - Only head_size == 64 is implemented; other sizes return
  *     WKV7_ERR_UNSUPPORTED.
  *   - Kernels are launched with programmatic dependent launch: a kernel may
@@ -92,6 +96,11 @@ typedef enum { WKV7_F32 = 0, WKV7_BF16 = 1 } wkv7_dtype;
 #define WKV7_DEV_BAD_SEQLENS 2  /* cu_seqlens not monotone, out of range or longer than max_seqlen */
 #define WKV7_DEV_WAIT_TIMEOUT 3 /* a bounded in-kernel wait gave up; outputs of that unit are invalid */
 #define WKV7_DEV_DECAY_RANGE 4  /* chunked prefill: decay over half a chunk beyond the float range */
+#define WKV7_DEV_DUP_SLOT 5     /* wkv7_validate_ids: an id listed twice (in one list or in both) */
+
+/* Id tables for wkv7_validate_ids. */
+#define WKV7_TABLE_SLOTS 0
+#define WKV7_TABLE_SNAPSHOTS 1
 
 typedef struct {
     int32_t n_layers;    /* >= 1 */
@@ -123,11 +132,18 @@ typedef struct {
 /* ---------------------------------------------------------------- pool ---- */
 
 /* Bytes of device memory a pool with this description needs: a 256-byte
- * header (the device status word) followed by the slot and snapshot states.
- * Returns 0 for an invalid description. */
+ * header (the device status word), the slot and snapshot states, and the
+ * bitmap that wkv7_validate_ids uses (max(n_slots, n_snapshots) bits rounded
+ * up to 256 bytes).  Returns 0 for an invalid description. */
 size_t wkv7_pool_required_bytes(const wkv7_pool_desc *desc);
 
-/* Create a pool.  With a caller buffer no CUDA call is made (slot contents are
+/* Create a pool: the fixed-capacity store of state slots of "wkvm: state-slot
+ * inference for RWKV, GDN and Mamba hybrids", section "The allocation unit wkvm
+ * changes" (a request owns a fixed-size slot), with the capacity reserved up
+ * front as "Virtual Memory for KV Cache and Model Weights" reserves hybrid
+ * recurrent-state slots separately at admission; each slot holds the
+ * per-layer, per-head [head_size, head_size] states of RWKV-X Architecture,
+ * "WKV-7 Kernel (Generalized Delta Rule)".  With a caller buffer no CUDA call is made (slot contents are
  * whatever the buffer holds until wkv7_slot_create zeroes them) except that
  * the caller must have zeroed the first 256 bytes (the status word).  With
  * device_buffer == NULL the library allocates on the current device and zeroes
@@ -135,7 +151,9 @@ size_t wkv7_pool_required_bytes(const wkv7_pool_desc *desc);
  * Errors: INVALID_ARG, UNSUPPORTED (head_size), NO_MEMORY, CUDA. */
 wkv7_status wkv7_pool_create(const wkv7_pool_desc *desc, wkv7_pool **out);
 
-/* Destroy a pool; frees the device buffer only if the library allocated it.
+/* Destroy a pool (the opaque state's free of RWKV-X Architecture, "Adapter
+ * API": new/free/reset of an opaque state); frees the device buffer only if
+ * the library allocated it.
  * The caller must make sure no work using the pool is still in flight. */
 wkv7_status wkv7_pool_destroy(wkv7_pool *pool);
 
@@ -147,7 +165,8 @@ wkv7_status wkv7_pool_get_desc(const wkv7_pool *pool, wkv7_pool_desc *out);
 size_t wkv7_slot_bytes(const wkv7_pool *pool);
 
 /* Device address of the float32 [n_heads][head_size][head_size] state of
- * (slot, layer), or of a snapshot (for a bf16-state pool the address of the
+ * (slot, layer) -- the per-head, per-layer state matrices of RWKV-X
+ * Architecture, "WKV-7 Kernel (Generalized Delta Rule)" -- or of a snapshot (for a bf16-state pool the address of the
  * bf16 states, returned through the same float pointer type).  For tests and
  * for initialising states.
  * Errors: INVALID_ARG, BAD_SLOT (index out of range; allocation state is not
@@ -236,7 +255,11 @@ wkv7_status wkv7_slot_resume(wkv7_pool *pool, const void *host_src, size_t host_
  * and stores, so the six input bases and o must be 16-byte aligned; a base
  * that is not is reported as UNSUPPORTED before any launch. */
 
-/* decode: one token for each of n slots at one layer.  For b < n and every
+/* decode: one token for each of n slots at one layer -- the per-token
+ * recurrence of RWKV-X Architecture, "WKV-7 Kernel (Generalized Delta Rule)"
+ * (decay, delta-rule term, key-value write, readout after the update), run as
+ * one batched step over the state slots of "wkvm: state-slot inference for
+ * RWKV, GDN and Mamba hybrids" ("The allocation unit wkvm changes").  For b < n and every
  * head h, the state at (slot_ids_dev[b], layer, h) takes one step of the
  * recurrence with inputs x[b][h][:] (x = r, w, k, v, a, b; [n][n_heads][64],
  * dtype in_dtype) and o[b][h][:] (float32) receives the readout.  The state is
@@ -332,11 +355,38 @@ wkv7_status wkv7_prefill_checkpointed(wkv7_pool *pool, int32_t layer, const int3
                                       const int32_t *ckpt_snap_ids_dev, int32_t sequential,
                                       cudaStream_t stream);
 
+/* --------------------------------------------------------- validation ---- */
+
+/* validate_ids: the debug pass over device id arrays that the fast paths skip.
+ * Checks that every id of ids_a_dev[0..n_a) and ids_b_dev[0..n_b) lies in the
+ * table (WKV7_TABLE_SLOTS: [0, n_slots); WKV7_TABLE_SNAPSHOTS: [0,
+ * n_snapshots)) and that no id occurs twice, within either list or in both --
+ * so it covers the repeated ids of one call (a = the call's ids, n_b = 0) and
+ * the overlap of a mixed step's decode and prefill slot sets (a = decode ids,
+ * b = prefill ids).  The state-slot engine's hard-error discipline (the rvLLM
+ * README: no silent fallback; a request that breaks the contract is an
+ * error, never repaired) applied to ids only the device holds.
+ * Asynchronous on `stream` like every call: two kernels (clear the pool's
+ * bitmap, then mark each id with an atomic OR).  A repeat records
+ * WKV7_DEV_DUP_SLOT and an out-of-range id WKV7_DEV_BAD_SLOT in the device
+ * status word (first fault wins); wkv7_get_device_status then returns
+ * WKV7_ERR_DUP_SLOT (or WKV7_ERR_DEVICE_STATUS).  Reads only the id arrays;
+ * writes only the pool's bitmap and status word, never a state.  Two
+ * validate calls on one pool must not overlap in time (they share the
+ * bitmap).  Id arrays are caller-owned device int32 arrays.  Errors:
+ * INVALID_ARG (NULL pool, unknown table, n_a or n_b negative, a NULL array
+ * with a positive count), CUDA.  n_a == n_b == 0 is a no-op. */
+wkv7_status wkv7_validate_ids(wkv7_pool *pool, int32_t table, const int32_t *ids_a_dev, int32_t n_a,
+                              const int32_t *ids_b_dev, int32_t n_b, cudaStream_t stream);
+
 /* ------------------------------------------------------------- status ---- */
 
 /* Wait (at most timeout_ms, polling; <= 0 means 10000) for the work queued on
  * `stream`, then read and clear the pool's device status word into *code_out
- * (WKV7_DEV_*).  Returns WKV7_ERR_DEVICE_STATUS when the code is non-zero,
+ * (WKV7_DEV_*).  This is how the hard errors of the rvLLM README ("no
+ * fallbacks": a fault is reported, never silently repaired) reach the host for
+ * the faults that only a kernel sees.  Returns WKV7_ERR_DUP_SLOT when the code
+ * is WKV7_DEV_DUP_SLOT, WKV7_ERR_DEVICE_STATUS for any other non-zero code,
  * WKV7_ERR_TIMEOUT when the stream did not finish in time (the word is left
  * as it is), WKV7_ERR_CUDA on a CUDA error. */
 wkv7_status wkv7_get_device_status(wkv7_pool *pool, cudaStream_t stream, int32_t timeout_ms,

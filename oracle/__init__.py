@@ -290,11 +290,16 @@ def rel_err(x, ref) -> float:
     return num / den
 
 
-def rel_err_slices(x, ref, lead: int) -> np.ndarray:
+def rel_err_slices(x, ref, lead: int, floor_frac: float = 0.0) -> np.ndarray:
     """rel_err of every slice over the first `lead` axes: for x, ref of shape
     [d0, .., d_{lead-1}, ...] the array [d0, .., d_{lead-1}] of normwise-max
     errors of x[i0, .., i_{lead-1}] against ref[i0, .., i_{lead-1}], so that a
-    slice whose values are small is judged against its own scale."""
+    slice whose values are small is judged against its own scale.
+
+    With floor_frac > 0 a slice's denominator is at least floor_frac times the
+    median over slices of max|ref slice|: a slice whose result nearly cancels
+    (an output o = v (k . r) with k . r close to 0, say) carries the rounding of
+    its summands, which are of the typical size, not of its own tiny size."""
     x = np.asarray(x, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     if x.shape != ref.shape:
@@ -308,8 +313,36 @@ def rel_err_slices(x, ref, lead: int) -> np.ndarray:
         return np.zeros(out_shape)
     num = np.max(np.abs(xf - rf), axis=1)
     den = np.max(np.abs(rf), axis=1)
+    if floor_frac > 0.0:
+        den = np.maximum(den, floor_frac * float(np.median(den)))
     res = np.where(den > 0, num / np.where(den > 0, den, 1.0), num)
     return res.reshape(out_shape)
+
+
+def rel_err_segments(x, ref, cu, floor_frac: float = 0.0) -> np.ndarray:
+    """rel_err of every (sequence, head) of packed [tokens][heads][...] arrays:
+    sequence q covers tokens cu[q] .. cu[q+1]-1.  Returns [n_seqs, heads]
+    (0 for an empty sequence); floor_frac as in rel_err_slices, the median
+    taken over the non-empty (sequence, head) slices."""
+    x = np.asarray(x, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    if x.shape != ref.shape:
+        raise ValueError(f"rel_err_segments: shape {x.shape} against reference shape {ref.shape}")
+    cu = np.asarray(cu, dtype=np.int64)
+    n, H = len(cu) - 1, ref.shape[1]
+    if n < 0 or (n > 0 and (cu[0] != 0 or cu[-1] != ref.shape[0] or np.any(np.diff(cu) < 0))):
+        raise ValueError("rel_err_segments: cu must run from 0 to the token count, non-decreasing")
+    num = np.zeros((n, H))
+    den = np.zeros((n, H))
+    filled = np.diff(cu) > 0
+    axes = tuple(i for i in range(ref.ndim) if i != 1)
+    for q in np.nonzero(filled)[0]:
+        a, b = int(cu[q]), int(cu[q + 1])
+        num[q] = np.max(np.abs(x[a:b] - ref[a:b]), axis=axes)
+        den[q] = np.max(np.abs(ref[a:b]), axis=axes)
+    if floor_frac > 0.0 and filled.any():
+        den = np.maximum(den, floor_frac * float(np.median(den[filled])))
+    return np.where(den > 0, num / np.where(den > 0, den, 1.0), num)
 
 
 def elementwise_rel(x, ref, floor: float = 1e-6) -> np.ndarray:

@@ -21,7 +21,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libwkv7.so")
 
-SOURCES = ["capi.cpp", "decode.cu", "decode_multi.cu", "slots.cu", "prefill_seq.cu", "prefill_chunk.cu"]
+SOURCES = ["capi.cpp", "decode.cu", "decode_multi.cu", "slots.cu", "prefill_seq.cu", "prefill_chunk.cu",
+           "validate.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-I", INCLUDE, "-I", CSRC]
 

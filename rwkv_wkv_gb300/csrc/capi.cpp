@@ -89,6 +89,14 @@ size_t slot_bytes_of(const wkv7_pool_desc *d) {
            static_cast<size_t>(d->head_size) * static_cast<size_t>(d->head_size) * state_elem_bytes(d);
 }
 
+// The id-validation bitmap after the snapshot store: one bit per id of the
+// larger table, rounded up to 256 bytes.
+size_t marks_bytes_of(const wkv7_pool_desc *d) {
+    const size_t ids = static_cast<size_t>(d->n_slots > d->n_snapshots ? d->n_slots : d->n_snapshots);
+    const size_t words = (ids + 31) / 32;
+    return (words * 4 + 255) / 256 * 256;
+}
+
 }  // namespace
 
 struct wkv7_pool {
@@ -98,6 +106,7 @@ struct wkv7_pool {
     int32_t *status = nullptr;
     float *states = nullptr;
     float *snaps = nullptr;
+    uint32_t *marks = nullptr;  // id-validation bitmap (scratch of wkv7_validate_ids)
     long long slot_floats = 0;  // slot bytes / 4: the unit of the byte-copy verbs
     bool state_bf16 = false;
     std::mutex mu;
@@ -144,7 +153,8 @@ size_t wkv7_pool_required_bytes(const wkv7_pool_desc *desc) {
     if (!desc_valid(desc)) return 0;
     size_t sb = slot_bytes_of(desc);
     return kHeaderBytes + sb * (static_cast<size_t>(desc->n_slots) +
-                                static_cast<size_t>(desc->n_snapshots));
+                                static_cast<size_t>(desc->n_snapshots)) +
+           marks_bytes_of(desc);
 }
 
 wkv7_status wkv7_pool_create(const wkv7_pool_desc *desc, wkv7_pool **out) {
@@ -188,6 +198,9 @@ wkv7_status wkv7_pool_create(const wkv7_pool_desc *desc, wkv7_pool **out) {
     p->slot_floats = static_cast<long long>(slot_bytes_of(desc) / sizeof(float));
     p->state_bf16 = desc->state_dtype == WKV7_BF16;
     p->snaps = p->states + static_cast<size_t>(p->slot_floats) * static_cast<size_t>(desc->n_slots);
+    p->marks = reinterpret_cast<uint32_t *>(
+        p->base + kHeaderBytes +
+        slot_bytes_of(desc) * (static_cast<size_t>(desc->n_slots) + static_cast<size_t>(desc->n_snapshots)));
     try {
         p->slots.init(desc->n_slots);
         p->snapshots.init(desc->n_snapshots);
@@ -518,6 +531,27 @@ wkv7_status wkv7_prefill_checkpointed(wkv7_pool *pool, int32_t layer, const int3
                           cu_ckpt_dev, ckpt_snap_ids_dev);
 }
 
+// ------------------------------------------------------------- validation --
+
+wkv7_status wkv7_validate_ids(wkv7_pool *pool, int32_t table, const int32_t *ids_a_dev, int32_t n_a,
+                              const int32_t *ids_b_dev, int32_t n_b, cudaStream_t stream) {
+    if (!pool || n_a < 0 || n_b < 0) return WKV7_ERR_INVALID_ARG;
+    if (table != WKV7_TABLE_SLOTS && table != WKV7_TABLE_SNAPSHOTS) return WKV7_ERR_INVALID_ARG;
+    if ((n_a > 0 && !ids_a_dev) || (n_b > 0 && !ids_b_dev)) return WKV7_ERR_INVALID_ARG;
+    if (n_a == 0 && n_b == 0) return WKV7_OK;
+    wkv7::ValidateArgs va;
+    va.marks = pool->marks;
+    va.n_table = table == WKV7_TABLE_SLOTS ? pool->desc.n_slots : pool->desc.n_snapshots;
+    va.ids_a = ids_a_dev;
+    va.n_a = n_a;
+    va.ids_b = ids_b_dev;
+    va.n_b = n_b;
+    va.status = pool->status;
+    int launches = 0;
+    cudaError_t e = wkv7::launch_validate_ids(va, stream, &launches);
+    return cuda_status("validate_ids", e, launches);
+}
+
 // ----------------------------------------------------------------- status --
 
 wkv7_status wkv7_get_device_status(wkv7_pool *pool, cudaStream_t stream, int32_t timeout_ms,
@@ -559,6 +593,7 @@ wkv7_status wkv7_get_device_status(wkv7_pool *pool, cudaStream_t stream, int32_t
         if (e != cudaSuccess) return cuda_status("status:clear", e, 0);
     }
     *code_out = code;
+    if (code == WKV7_DEV_DUP_SLOT) return WKV7_ERR_DUP_SLOT;
     return code != 0 ? WKV7_ERR_DEVICE_STATUS : WKV7_OK;
 }
 

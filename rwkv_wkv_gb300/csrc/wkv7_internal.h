@@ -99,7 +99,20 @@ struct ZeroIds {
     int ids[kZeroIdsPerLaunch];
 };
 
+// Debug validation of two device id lists against a table of n_table ids
+// (marks: a bitmap of (n_table + 31) / 32 words of scratch).
+struct ValidateArgs {
+    uint32_t *marks;
+    int n_table;
+    const int *ids_a;
+    int n_a;
+    const int *ids_b;
+    int n_b;
+    int *status;
+};
+
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s, int *launches);
+cudaError_t launch_validate_ids(const ValidateArgs &a, cudaStream_t s, int *launches);
 cudaError_t launch_decode_multi(const DecodeMultiArgs &a, cudaStream_t s, int *launches);
 cudaError_t launch_prefill_sequential(const PrefillArgs &a, cudaStream_t s, int *launches);
 cudaError_t launch_prefill_chunked(const PrefillArgs &a, cudaStream_t s, int *launches);

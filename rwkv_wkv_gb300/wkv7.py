@@ -16,7 +16,8 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libwkv7.so")
 
 F32, BF16 = 0, 1
-DEV_OK, DEV_BAD_SLOT, DEV_BAD_SEQLENS, DEV_WAIT_TIMEOUT, DEV_DECAY_RANGE = 0, 1, 2, 3, 4
+DEV_OK, DEV_BAD_SLOT, DEV_BAD_SEQLENS, DEV_WAIT_TIMEOUT, DEV_DECAY_RANGE, DEV_DUP_SLOT = 0, 1, 2, 3, 4, 5
+TABLE_SLOTS, TABLE_SNAPSHOTS = 0, 1
 HEAD_SIZE = 64
 _HEADER_BYTES = 256
 
@@ -78,6 +79,7 @@ _SIGS = {
                           + [_VP, _VP]),
     "wkv7_prefill_checkpointed": (ctypes.c_int, [_P, _I32, _VP, _VP, _I32, _I32, _I32, ctypes.c_int]
                                   + [_VP] * 7 + [_VP, _VP, _I32, _VP]),
+    "wkv7_validate_ids": (ctypes.c_int, [_P, _I32, _VP, _I32, _VP, _I32, _VP]),
     "wkv7_get_device_status": (ctypes.c_int, [_P, _VP, _I32, _I32P]),
     "wkv7_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "wkv7_last_error": (ctypes.c_char_p, []),
@@ -378,11 +380,28 @@ class Pool:
                "prefill_sequential" if sequential else "prefill")
         return o
 
+    # ------------------------------------------------------------ validation
+    def validate_ids(self, ids_a: torch.Tensor, ids_b: torch.Tensor | None = None,
+                     table: str = "slots", stream=None) -> None:
+        """Debug pass (wkv7_validate_ids): every id of ids_a and ids_b (device int32)
+        in the table and none twice; the verdict lands in the device status word
+        (DEV_DUP_SLOT, DEV_BAD_SLOT), read with device_status()."""
+        if table not in ("slots", "snapshots"):
+            raise ValueError("table must be 'slots' or 'snapshots'")
+        nb = 0 if ids_b is None else ids_b.numel()
+        pb = _dev_i32(ids_b, "ids_b", self.device) if nb else None
+        na = ids_a.numel()
+        pa = _dev_i32(ids_a, "ids_a", self.device) if na else None
+        _check(self._lib.wkv7_validate_ids(self._h, TABLE_SLOTS if table == "slots" else TABLE_SNAPSHOTS,
+                                           pa, na, pb, nb, _stream_handle(stream, self.device)),
+               "validate_ids")
+
     # ---------------------------------------------------------------- status
     def device_status(self, stream=None, timeout_ms: int = 10000) -> int:
+        """Read and clear the device status word (a DEV_* code; 0 when clean)."""
         code = ctypes.c_int32()
         st = self._lib.wkv7_get_device_status(self._h, _stream_handle(stream, self.device),
                                               timeout_ms, ctypes.byref(code))
-        if st not in (0, 8):
+        if st not in (0, 3, 8):  # OK, ERR_DUP_SLOT and ERR_DEVICE_STATUS carry the code
             _check(st, "get_device_status")
         return int(code.value)

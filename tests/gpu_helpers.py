@@ -31,6 +31,12 @@ def rel(x, ref):
     return oracle.rel_err(np.asarray(x, dtype=np.float64), ref)
 
 
+# Per-slice checks floor each slice's denominator at 1% of the median slice
+# scale: a slice whose result cancels (k . r near 0 for a one-token sequence
+# from a zero state, say) keeps the float32 rounding of summands of typical
+# size, far above the tolerance times its own tiny magnitude.
+SLICE_FLOOR = 1e-2
+
 # Elementwise companion of the normwise bound: its median must stay under the
 # path's tolerance and its 99.9th percentile under 100 times it.  Entries near
 # zero are judged against a floor of 1e-6 of the tensor's largest magnitude, so
@@ -50,15 +56,9 @@ def check_parity(x, ref, tol, lead=0, cu=None, elementwise=False, what=""):
     out = {"normwise": oracle.rel_err(x, ref)}
     assert out["normwise"] < tol, (what, out)
     if cu is not None:
-        worst = 0.0
-        for s in range(len(cu) - 1):
-            a, b = int(cu[s]), int(cu[s + 1])
-            if b > a:
-                per = oracle.rel_err_slices(np.swapaxes(x[a:b], 0, 1), np.swapaxes(ref[a:b], 0, 1), 1)
-                worst = max(worst, float(per.max()))
-        out["worst_slice"] = worst
+        out["worst_slice"] = float(oracle.rel_err_segments(x, ref, cu, floor_frac=SLICE_FLOOR).max())
     elif lead:
-        out["worst_slice"] = float(oracle.rel_err_slices(x, ref, lead).max())
+        out["worst_slice"] = float(oracle.rel_err_slices(x, ref, lead, floor_frac=SLICE_FLOOR).max())
     if "worst_slice" in out:
         assert out["worst_slice"] < tol, (what, out)
     if elementwise:

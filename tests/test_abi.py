@@ -69,7 +69,11 @@ def _fake_pool(lib, **kw):
 
 def test_required_bytes(lib):
     d = _desc()
-    assert lib.wkv7_pool_required_bytes(ctypes.byref(d)) == 256 + (8 + 4) * 2 * 3 * 64 * 64 * 4
+    # header + slots + snapshots + the validation bitmap (max(8, 4) bits -> 256 bytes)
+    assert lib.wkv7_pool_required_bytes(ctypes.byref(d)) == 256 + (8 + 4) * 2 * 3 * 64 * 64 * 4 + 256
+    big = _desc(n_slots=70000, n_snapshots=3)   # 70000 bits = 8750 bytes -> 8960
+    assert (lib.wkv7_pool_required_bytes(ctypes.byref(big))
+            == 256 + 70003 * 2 * 3 * 64 * 64 * 4 + 8960)
     bad = _desc(n_slots=0)
     assert lib.wkv7_pool_required_bytes(ctypes.byref(bad)) == 0
 
@@ -194,6 +198,14 @@ def test_host_checks_return_before_launch(lib):
         assert lib.wkv7_slot_create(h, 9, ids, None) == 4     # POOL_FULL, nothing allocated
         assert lib.wkv7_slot_count_free(h) == 8
         assert lib.wkv7_get_device_status(h, None, 10, None) == 1
+        # id validation: unknown table, negative counts, NULL arrays with ids; empty is a no-op
+        assert lib.wkv7_validate_ids(h, 2, x, 1, None, 0, None) == 1
+        assert lib.wkv7_validate_ids(h, 0, x, -1, None, 0, None) == 1
+        assert lib.wkv7_validate_ids(h, 0, x, 1, x, -2, None) == 1
+        assert lib.wkv7_validate_ids(h, 0, None, 1, None, 0, None) == 1
+        assert lib.wkv7_validate_ids(h, 1, x, 0, None, 3, None) == 1
+        assert lib.wkv7_validate_ids(None, 0, x, 1, None, 0, None) == 1
+        assert lib.wkv7_validate_ids(h, 0, None, 0, None, 0, None) == 0
     finally:
         lib.wkv7_pool_destroy(h)
 
@@ -214,8 +226,8 @@ def test_bf16_state_pool(lib):
     and every call is offered."""
     d16 = _desc(state_dtype=1)
     d32 = _desc()
-    body32 = lib.wkv7_pool_required_bytes(ctypes.byref(d32)) - 256
-    assert lib.wkv7_pool_required_bytes(ctypes.byref(d16)) - 256 == body32 // 2
+    body32 = lib.wkv7_pool_required_bytes(ctypes.byref(d32)) - 512   # header, bitmap
+    assert lib.wkv7_pool_required_bytes(ctypes.byref(d16)) - 512 == body32 // 2
     assert lib.wkv7_pool_required_bytes(ctypes.byref(_desc(state_dtype=2))) == 0
     st, h = _fake_pool(lib, state_dtype=1)
     assert st == 0

@@ -26,6 +26,11 @@ def test_reference_arm_prints_one_json_line():
     assert d["value"] > 0 and d["unit"] == "tokens/s" and d["higher_is_better"] is True
     assert d["steps"] == 1 and d["warmup"] == 1
     assert "workload" in d["config"]
+    # the same config keys as the GPU arm prints for this workload (the driver compares them)
+    for key in ("pool_slots", "layers", "heads", "head_size", "decode_slots", "state_dtype",
+                "input_dtype", "output_dtype", "parallelism", "l2", "graph"):
+        assert key in d["config"], key
+    assert d["config"]["parallelism"] == "1 gpu" and d["config"]["graph"] is False
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,

@@ -59,6 +59,42 @@ def test_rel_err_slices_hand_values():
         oracle.rel_err_slices(x, ref[:1], 1)
 
 
+def test_rel_err_slices_floor_hand_values():
+    """The optional floor: denominators of at least floor_frac x the median slice scale."""
+    ref = np.array([[4.0, 0.0], [2.0, -8.0], [0.01, 0.0], [1.0, 1.0]])  # slice maxima 4, 8, 0.01, 1
+    x = ref + np.array([[0.0, 0.04], [0.0, 0.0], [0.0005, 0.0], [0.0, 0.0]])
+    plain = oracle.rel_err_slices(x, ref, 1)
+    assert plain == pytest.approx([0.01, 0.0, 0.05, 0.0])
+    # median of (4, 8, 0.01, 1) is 2.5; a floor of 0.1 x 2.5 = 0.25 lifts only the third slice
+    floored = oracle.rel_err_slices(x, ref, 1, floor_frac=0.1)
+    assert floored == pytest.approx([0.01, 0.0, 0.0005 / 0.25, 0.0])
+
+
+def test_rel_err_segments_hand_values():
+    """Packed [tokens][heads][channels]: sequences of 2, 0 and 1 tokens, 2 heads."""
+    ref = np.zeros((3, 2, 2))
+    ref[0, 0] = [1.0, -2.0]; ref[1, 0] = [0.5, 0.0]      # seq 0, head 0: max |ref| 2
+    ref[0, 1] = [10.0, 0.0]; ref[1, 1] = [0.0, 4.0]      # seq 0, head 1: max 10
+    ref[2, 0] = [0.0, 0.0]                               # seq 2, head 0: all zero
+    ref[2, 1] = [3.0, -1.0]                              # seq 2, head 1: max 3
+    x = ref.copy()
+    x[1, 0, 1] = 0.1      # seq 0 head 0: 0.1 / 2
+    x[0, 1, 1] = -1.0     # seq 0 head 1: 1 / 10
+    x[2, 0, 0] = 0.25     # seq 2 head 0: zero reference -> absolute 0.25
+    e = oracle.rel_err_segments(x, ref, [0, 2, 2, 3])
+    assert e.shape == (3, 2)
+    assert e[0] == pytest.approx([0.05, 0.1])
+    assert e[1] == pytest.approx([0.0, 0.0])
+    assert e[2] == pytest.approx([0.25, 0.0])
+    # floor: median of the non-empty slice scales (2, 10, 0, 3) is 2.5 -> denominators >= 0.25
+    f = oracle.rel_err_segments(x, ref, [0, 2, 2, 3], floor_frac=0.1)
+    assert f[2, 0] == pytest.approx(1.0) and f[0, 0] == pytest.approx(0.05)
+    with pytest.raises(ValueError):
+        oracle.rel_err_segments(x, ref, [0, 2, 4])
+    with pytest.raises(ValueError):
+        oracle.rel_err_segments(x, ref[:2], [0, 2])
+
+
 def test_elementwise_rel_hand_values():
     ref = np.array([4.0, -2.0, 0.0, 1000.0])
     x = np.array([5.0, -2.0, 0.001, 1000.0])
