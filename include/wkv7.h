@@ -379,6 +379,33 @@ wkv7_status wkv7_prefill_checkpointed(wkv7_pool *pool, int32_t layer, const int3
 wkv7_status wkv7_validate_ids(wkv7_pool *pool, int32_t table, const int32_t *ids_a_dev, int32_t n_a,
                               const int32_t *ids_b_dev, int32_t n_b, cudaStream_t stream);
 
+/* validate_ids_noalloc: the same check as wkv7_validate_ids for callers that
+ * cannot allocate device memory -- a process whose device memory is already
+ * handed out in full to another allocator (a framework's caching allocator
+ * that reserved the device, say), or a serving loop that forbids allocation
+ * after start-up because cudaMalloc synchronises the device at an unbounded
+ * cost -- and that hold no pool to lend its scratch.  It takes no pool and
+ * allocates nothing: its bitmap is a static device array built into the
+ * library (1,048,576 bits = 128 KiB, held on every GPU that loads the library
+ * until the process exits), and the verdict goes to the caller's word.  No
+ * counterpart in the pages; it exists for such callers only.
+ * n_table: the ids are valid in [0, n_table), at most 1,048,576 (larger is
+ * WKV7_ERR_UNSUPPORTED).  ids_a_dev[n_a], ids_b_dev[n_b]: caller-owned device
+ * int32 lists, as in wkv7_validate_ids.  result_dev: a caller-owned device
+ * int32 that the call first sets to WKV7_DEV_OK and then, on a fault, to
+ * WKV7_DEV_DUP_SLOT (an id twice, within a list or in both) or
+ * WKV7_DEV_BAD_SLOT (an id out of range), the first fault winning; read it
+ * once `stream` has passed the call.  The first call on a device (with that
+ * device current) looks up the array's device address and keeps it; make that
+ * first call before any stream capture.  Every call on a device uses the same
+ * array, cleared by the call itself: calls whose work overlaps on the GPU (on
+ * different streams, or from different threads) race on it and may report
+ * wrong results.  Errors: INVALID_ARG (negative sizes, NULL result_dev, a
+ * NULL list with a positive count), UNSUPPORTED (n_table too large), CUDA. */
+wkv7_status wkv7_validate_ids_noalloc(int32_t n_table, const int32_t *ids_a_dev, int32_t n_a,
+                                      const int32_t *ids_b_dev, int32_t n_b, int32_t *result_dev,
+                                      cudaStream_t stream);
+
 /* ------------------------------------------------------------- status ---- */
 
 /* Wait (at most timeout_ms, polling; <= 0 means 10000) for the work queued on

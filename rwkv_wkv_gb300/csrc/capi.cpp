@@ -99,6 +99,15 @@ size_t marks_bytes_of(const wkv7_pool_desc *d) {
 
 }  // namespace
 
+namespace wkv7 {
+// For entry points defined outside this file: count their launches and record
+// their CUDA errors like every other call does.
+void note_launches(int launches) {
+    g_launches.fetch_add(static_cast<uint64_t>(launches), std::memory_order_relaxed);
+}
+void note_cuda_error(const char *what, cudaError_t e) { set_error(what, e); }
+}  // namespace wkv7
+
 struct wkv7_pool {
     wkv7_pool_desc desc{};
     char *base = nullptr;

@@ -111,6 +111,11 @@ struct ValidateArgs {
     int *status;
 };
 
+// Launch counter and last-error text of the C-ABI layer, for entry points that
+// live beside their kernels.
+void note_launches(int launches);
+void note_cuda_error(const char *what, cudaError_t e);
+
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s, int *launches);
 cudaError_t launch_validate_ids(const ValidateArgs &a, cudaStream_t s, int *launches);
 cudaError_t launch_decode_multi(const DecodeMultiArgs &a, cudaStream_t s, int *launches);

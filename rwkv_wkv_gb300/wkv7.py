@@ -80,6 +80,7 @@ _SIGS = {
     "wkv7_prefill_checkpointed": (ctypes.c_int, [_P, _I32, _VP, _VP, _I32, _I32, _I32, ctypes.c_int]
                                   + [_VP] * 7 + [_VP, _VP, _I32, _VP]),
     "wkv7_validate_ids": (ctypes.c_int, [_P, _I32, _VP, _I32, _VP, _I32, _VP]),
+    "wkv7_validate_ids_noalloc": (ctypes.c_int, [_I32, _VP, _I32, _VP, _I32, _VP, _VP]),
     "wkv7_get_device_status": (ctypes.c_int, [_P, _VP, _I32, _I32P]),
     "wkv7_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "wkv7_last_error": (ctypes.c_char_p, []),
