@@ -53,7 +53,7 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", choices=["mixed", "decode12", "prefill", "sweep", "verify",
-                                          "hibernate"],
+                                          "hibernate", "decode_mixed"],
                    default="mixed")
     p.add_argument("--batch", type=int, default=4096, help="sweep batch size")
     p.add_argument("--graph", action="store_true", help="replay each step as a CUDA graph")
@@ -282,6 +282,33 @@ class Mixed(Workload):
         pool.restore(self.snap_ids, self.snap_src)
         rec("restore")
         pool.free(created[::-1])
+
+    def verb_ceiling(self):
+        """GB/s of the device's own contiguous copy (torch copy_, a cudaMemcpyAsync)
+        and fill (zero_, a cudaMemsetAsync) of the same bytes as one verb call (64
+        slots), timed with CUDA events in this run: at 32-64 MB per call, the
+        ramp-up and tail of any transfer are a visible share of its time, so this,
+        not the large-copy peak, is what a verb of this size can reach."""
+        torch = self.torch
+        nbytes = wl.MIXED_VERB_N * self.pool.slot_bytes
+        a = torch.empty(nbytes, dtype=torch.uint8, device=self.pool.device)
+        b = torch.empty(nbytes, dtype=torch.uint8, device=self.pool.device)
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=self.pool.device)
+        out = {}
+        for name, fn, moved in (("copy", lambda: b.copy_(a), 2 * nbytes), ("fill", lambda: b.zero_(), nbytes)):
+            ts = []
+            for r in range(23):
+                flush.fill_(r & 0xFF)
+                s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                s0.record()
+                fn()
+                s1.record()
+                torch.cuda.synchronize()
+                if r >= 3:
+                    ts.append(s0.elapsed_time(s1))
+            out[name] = moved / (statistics.median(ts) / 1e3) / 1e9
+        del a, b, flush
+        return out
 
     def host_io(self):
         """(inputs to upload each step, outputs to read back each step)."""
@@ -607,9 +634,54 @@ class Hibernate(Workload):
         return None
 
 
+class DecodeMixed(Workload):
+    """The mixed serving step's decode call alone: 1024 slots at permuted ids of its
+    4096-slot, 32-head pool (the same launch, about 2.2 GB on the device)."""
+    name = "decode_1024_of_4096_32H"
+
+    def __init__(self, torch, device):
+        from rwkv_wkv_gb300 import Pool
+        W = wl.MIXED
+        self.torch, self.H, self.N = torch, W.H, W.N
+        self.pool = Pool(1, W.H, W.n_slots, device=device)
+        g = torch.Generator(device=device).manual_seed(W.seed)
+        self.pool.states.normal_(0.0, 0.1, generator=g)
+        plan = wl.mixed_plan(W.seed)
+        self.ids = torch.as_tensor(plan["decode"].astype(np.int32), device=device)
+        B = wl.MIXED_DECODE_B
+        self.ins = wl.token_inputs_device(W.seed, B, W.H, W.N, device, generator_offset=1)
+        self.o = torch.empty(B, W.H, W.N, dtype=torch.float32, device=device)
+        self.phases = ["decode"]
+        self.phase_bytes = {"decode": B * W.H * (2 * HEAD_BYTES_STATE + W.N * 2 * 6 + W.N * 4)}
+        self.tokens_per_step = B
+        self.dominant = "decode"
+        self.launches_per_step = 1
+
+    def step(self, ev=None):
+        if ev:
+            ev["start"].record()
+        self.pool.decode_step(0, self.ids, *self.ins, o=self.o)
+        if ev:
+            ev["decode"].record()
+
+    def host_io(self):
+        return [self.ids] + list(self.ins), [self.o]
+
+    def config(self):
+        return {"workload": "the mixed step's decode call: 1024 of 4096 slots, 32 heads x 64, 1 layer",
+                "pool_slots": wl.MIXED.n_slots, "layers": 1, "heads": self.H, "head_size": self.N,
+                "decode_slots": wl.MIXED_DECODE_B, "state_dtype": "f32", "input_dtype": "bf16",
+                "output_dtype": "f32"}
+
+    def oracle_sample(self, frac_target):
+        return _head_sample(self.H, frac_target, wl.MIXED_DECODE_B, None, self.tokens_per_step)
+
+
 def make_workload(args, torch, device):
     if args.workload == "mixed":
         return Mixed(torch, device, state_dtype=args.state_dtype)
+    if args.workload == "decode_mixed":
+        return DecodeMixed(torch, device)
     if args.workload == "decode12":
         return Decode12(torch, device)
     if args.workload == "prefill":
@@ -842,6 +914,13 @@ def run_ours(args):
                                    "of the same bytes (cudaMemcpyAsync through torch)",
                     "bytes_per_launch": wk.phase_bytes["hibernate"],
                     "ms_per_launch": phases["hibernate"]["ms"], "traffic": None}
+    if hasattr(wk, "verb_ceiling"):  # small copies: also against a same-size device copy
+        ceil = wk.verb_ceiling()
+        for n in ("create", "snapshot", "fork", "restore"):
+            if n in phases:
+                ref = ceil["fill"] if n == "create" else ceil["copy"]
+                phases[n]["same_size_device_copy_GB_per_s"] = round(ref, 1)
+                phases[n]["frac_of_same_size_device_copy"] = round(phases[n]["GB_per_s"] / ref, 4)
     extra = {}
     if "decode" in phase_ms:
         rows = wk.phase_bytes["decode"]
@@ -1157,6 +1236,10 @@ def _shapes_only(args):
         s.checkpoints = args.checkpoints
         s.tokens_per_step = s.total
         cls = Prefill
+    elif args.workload == "decode_mixed":
+        s.H, s.N = wl.MIXED.H, wl.MIXED.N
+        s.tokens_per_step = wl.MIXED_DECODE_B
+        cls = DecodeMixed
     elif args.workload == "verify":
         W = wl.MIXED
         s.H, s.N, s.K, s.B, s.W = W.H, W.N, args.verify_k, wl.MIXED_DECODE_B, W

@@ -95,7 +95,7 @@ typedef enum { WKV7_F32 = 0, WKV7_BF16 = 1 } wkv7_dtype;
 #define WKV7_DEV_BAD_SLOT 1     /* a device slot/snapshot id was out of range */
 #define WKV7_DEV_BAD_SEQLENS 2  /* cu_seqlens not monotone, out of range or longer than max_seqlen */
 #define WKV7_DEV_WAIT_TIMEOUT 3 /* a bounded in-kernel wait gave up; outputs of that unit are invalid */
-#define WKV7_DEV_DECAY_RANGE 4  /* chunked prefill: decay over half a chunk beyond the float range */
+#define WKV7_DEV_DECAY_RANGE 4  /* reserved: not recorded (the chunked prefill runs such units token by token) */
 #define WKV7_DEV_DUP_SLOT 5     /* wkv7_validate_ids: an id listed twice (in one list or in both) */
 
 /* Id tables for wkv7_validate_ids. */
@@ -303,13 +303,14 @@ wkv7_status wkv7_decode_multi(wkv7_pool *pool, int32_t layer, const int32_t *slo
  * and o[t][h][:] (float32) the readout of every token.  The result equals
  * the token-by-token recurrence up to rounding; it is computed in chunks of
  * 64 tokens anchored at each sequence's first token, with bf16 tensor-core
- * operands and a float32 state carried between chunks.  max_seqlen bounds
- * every sequence length.  Errors: INVALID_ARG, UNSUPPORTED (in_dtype must be
- * WKV7_BF16; a misaligned base), CUDA.  Device:
- * WKV7_DEV_BAD_SLOT, WKV7_DEV_BAD_SEQLENS (that sequence is skipped),
- * WKV7_DEV_DECAY_RANGE (the decay over half a chunk, 32 tokens, exceeds
- * 2^120 in some channel: that sequence's results are not reliable),
- * WKV7_DEV_WAIT_TIMEOUT. */
+ * operands and a float32 state carried between chunks.  A (sequence, head)
+ * whose decay over half a chunk (32 tokens) exceeds 2^120 in some channel --
+ * beyond the float range of the chunk factorisation, e.g. w = 2^-8 for 32
+ * tokens, or w = 0 -- is run token by token in float32 by the same call
+ * instead (its results then equal wkv7_prefill_sequential's).  max_seqlen
+ * bounds every sequence length.  Errors: INVALID_ARG, UNSUPPORTED (in_dtype
+ * must be WKV7_BF16; a misaligned base), CUDA.  Device: WKV7_DEV_BAD_SLOT,
+ * WKV7_DEV_BAD_SEQLENS (that sequence is skipped), WKV7_DEV_WAIT_TIMEOUT. */
 wkv7_status wkv7_prefill(wkv7_pool *pool, int32_t layer, const int32_t *slot_ids_dev,
                          const int32_t *cu_seqlens_dev, int32_t n_seqs, int32_t total_tokens,
                          int32_t max_seqlen, wkv7_dtype in_dtype, const void *r,

@@ -28,7 +28,10 @@
 //       bf16 pairs, stored to 128-byte swizzled tiles.  Decays inside the Gram
 //       products are taken relative to the chunk midpoint (token 31), so no
 //       factor exceeds 2^(half-chunk decay); factors that meet S0 are relative
-//       to the start.
+//       to the start.  A (sequence, head) with a chunk whose half-chunk decay
+//       exceeds 2^120 in some channel (beyond the float range of these factors)
+//       keeps its start state: after the chunk loop the same CTA runs it token
+//       by token in float32 (prefill_seq_unit.cuh) and rewrites its outputs.
 // Tensor-memory readbacks give warps w and w+4 the same 32 lanes (rows) and
 // split the columns between them.
 //   G1  [Bbar;Kbar] x Am^T -> Mab rows s              (M=128, N=64, K=64)
@@ -60,6 +63,7 @@
 #include <cuda_bf16.h>
 
 #include "device_common.cuh"
+#include "prefill_seq_unit.cuh"
 #include "sm100_ptx.cuh"
 #include "wkv7_internal.h"
 
@@ -129,6 +133,7 @@ __device__ __forceinline__ void store_state_column32_bf16(float *states, size_t 
 __device__ __forceinline__ int up_idx(int i, int j) { return i * (7 - i) / 2 + (j - i - 1); }
 constexpr uint32_t kSmemBytes = kSmallBytes + 1024 + kTileBytes;  // + worst-case alignment
 static_assert(2 * (kSmemBytes + 1024) <= 228 * 1024, "two CTAs per SM");
+static_assert(sizeof(SeqStage) <= kTileBytes, "the token-by-token path stages in the tiles");
 constexpr uint32_t kTmemCols = 256;
 // Tensor-memory columns: G1 64-127 and G1' 128-255 (Q_k^T at 192-255 until it
 // is moved into G34's accumulator); G34's accumulator 0-127, loaded with its
@@ -333,8 +338,19 @@ __device__ __noinline__ int seq_of_rank(const int *cu, int n, int rank, int *wor
 // the CTA's abort flag; the flag is read (uniformly) after the phase's closing
 // barrier, so a timed-out phase runs to that barrier on garbage and then the
 // CTA leaves.
-__device__ __forceinline__ void mma_wait(uint32_t bar, uint32_t parity, volatile int *flag, long long limit) {
-    if (!mbar_wait_bounded(bar, parity, limit)) *flag = 1;
+__device__ __forceinline__ bool mma_wait(uint32_t bar, uint32_t parity, volatile int *flag, long long limit) {
+    if (mbar_wait_bounded(bar, parity, limit)) return true;
+    *flag = 1;
+    return false;
+}
+
+// The token-by-token route of a unit whose decay leaves the chunk
+// factorisation's range; kept out of line so that the chunked path's register
+// allocation and instruction stream do not carry it.
+template <bool SBF16>
+__device__ __noinline__ void prefill_unit_token_by_token(const PrefillArgs &p, int h, int t0, int t1, int ck0,
+                                                         size_t s_off, SeqStage *st) {
+    prefill_seq_unit<true, SBF16>(p, h, t0, t1, ck0, s_off, st);
 }
 
 // SBF16: the pool stores its states in bf16 (see the store paths of the readback).
@@ -407,7 +423,16 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int x = x0; x <= x1; ++x)
             tma_load_3d(smem_addr(base + stage_off(x)), &maps.m[x], 0, h, tcn, bar_in);
     };
-    if (tid == 0 && !p.test_skip_first_load) stage_inputs(0, 5, t0, true);
+    // A load thread 0 has issued and not yet seen land (on the input barrier's
+    // phase in_parity), for the drain after a wait that gave up.  (The MMA
+    // barrier needs no such record: every commit is followed by its wait before
+    // the loop can stop, so the last commit's phase is the one before ph_mma.)
+    bool in_flight = false;
+    uint32_t in_parity = 0;
+    if (tid == 0 && !p.test_skip_first_load) {
+        stage_inputs(0, 5, t0, true);
+        in_flight = true;
+    }
 
     // element offset of this (slot, layer, head) state; elements are bf16 on a
     // bf16-state pool (read exactly here; stored states are rounded to bf16)
@@ -449,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     // checks is 16-byte aligned), so o's own alignment decides the store width.
     const bool o_v8 = (reinterpret_cast<uintptr_t>(p.in.o) & 31u) == 0;
     uint32_t ph_mma = 0, ph_in = 0;
-    bool range_bad = false;
+    bool range_bad = false;  // a chunk's decay left the factorisation's range (this thread saw it)
     int prev_c = 0, prev_tc0 = 0, prev_Lc = 0;  // chunk whose state product awaits its readback
 
     // Readback of the state product [S_L^T; O^T] (tensor-memory columns 0-63): O rows to the output, S_L^T rows to the bf16 hi/lo
@@ -591,7 +616,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         uint32_t in_r[8], in_w[8], in_k[8], in_v[8], in_a[8], in_b[8];
         float e0s, e1s, eGm0, eGm1, EL0, EL1;  // 2^(G_{tb-1} - Gm), 2^Gm, 2^(G_L - Gm) per channel
         {
-            mma_wait(bar_in, ph_in, flag, p.wait_cycles);  // the staged inputs have landed
+            if (mma_wait(bar_in, ph_in, flag, p.wait_cycles) && tid == 0) in_flight = false;  // inputs landed
             ph_in ^= 1;
             {
                 auto st = [&](int x, int t) -> uint32_t {
@@ -901,7 +926,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         mma_wait(bar_mma, ph_mma, flag, p.wait_cycles);
         ph_mma ^= 1;
-        if (tid == 0 && !last) stage_inputs(0, 5, tc0 + kL, true);  // G2A and R1 are dead
+        if (tid == 0 && !last && !*flag) {  // G2A and R1 are dead
+            in_parity = ph_in;
+            stage_inputs(0, 5, tc0 + kL, true);
+            in_flight = true;
+        }
         tc_fence_after();
         {  // Z^T row (this thread's 32 columns) -> bf16 A operand of G34 in tensor memory
             float v[32];
@@ -963,23 +992,32 @@ __global__ void __launch_bounds__(kThreads, 2)
         // The readback of this product waits for the next chunk's first MMA (or the loop end);
         // R1 and the operand tiles are free for the next chunk's elementwise phase now.
     }
-    __syncthreads();  // every thread sees the same abort flag
-    if (!*flag) {
+    // every thread sees the same abort flag; a unit with a chunk out of range is
+    // run token by token below instead, so its chunked final state is not stored
+    const bool fallback = __syncthreads_or(range_bad) != 0;
+    if (!*flag && !fallback) {
         tc_fence_after();
         readback_state_product(prev_c, prev_tc0, prev_Lc, true);
     }
 
-    if (*flag) {  // a wait gave up: give in-flight MMAs a last chance, then leave
-        if (tid == 0) flag_status(p.lv.status, WKV7_DEV_WAIT_TIMEOUT);
-        mbar_wait_bounded(bar_mma, ph_mma, p.wait_cycles);
-        mbar_wait_bounded(bar_in, ph_in, p.wait_cycles);
+    if (*flag && tid == 0) {  // a wait gave up: let what thread 0 issued land (bounded), then leave
+        flag_status(p.lv.status, WKV7_DEV_WAIT_TIMEOUT);
+        mbar_wait_bounded(bar_mma, ph_mma ^ 1u, p.wait_cycles);  // the last commit
+        if (in_flight) mbar_wait_bounded(bar_in, in_parity, p.wait_cycles);
     }
-    if (range_bad && !*flag) flag_status(p.lv.status, WKV7_DEV_DECAY_RANGE);  // a timeout is reported instead
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
+    }
+    if (fallback && !*flag) {
+        // Token by token in float32 from the slot's start state, which the chunked
+        // pass has left untouched (its final state is stored only after the last
+        // chunk); outputs and checkpoints are rewritten.  The tiles are free: no
+        // copy or MMA is in flight.
+        __syncthreads();
+        prefill_unit_token_by_token<SBF16>(p, h, t0, t1, ck0, s_off, reinterpret_cast<SeqStage *>(base));
     }
 }
 

@@ -151,27 +151,61 @@ def test_chunked_and_sequential_agree():
     assert rel(outs[0][1], outs[1][1]) < PREFILL_TOL
 
 
-def test_decay_beyond_the_chunk_factorisation_is_flagged():
+@pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
+def test_decay_beyond_the_chunk_factorisation(state_dtype):
     """A channel whose decay over half a chunk exceeds 2^120 (w = 2^-8 for 40
-    tokens) makes the chunked path flag WKV7_DEV_DECAY_RANGE; the float32
-    token-by-token path takes the same inputs and still matches the oracle."""
-    from rwkv_wkv_gb300 import DEV_DECAY_RANGE
-    H, N, T = 2, 64, 40
-    ins = wl.token_inputs(31, "decay", T, H, N, dtype="bf16")
+    tokens, or an exact w = 0) cannot be factorised in chunks; wkv7_prefill then
+    runs that (sequence, head) token by token in float32 in the same call, and
+    every unit -- those and their neighbours on the chunked path -- matches the
+    oracle.  Nothing is flagged."""
+    H, N = 3, 64
+    lengths = [40, 150, 64, 200]
+    cu = wl.cu_seqlens(lengths)
+    ins = wl.token_inputs(31, "decay", int(cu[-1]), H, N, dtype="bf16")
     ins["w"] = ins["w"].copy()
-    ins["w"][:, 1, 5] = 2.0 ** -8
-    cu = wl.cu_seqlens([T])
-    with Pool(1, H, 2) as pool:
-        pool.create(1)
-        pool.prefill(0, i32([0]), i32(cu), *dev_inputs(ins, "bf16"), max_seqlen=T)
-        assert pool.device_status() == DEV_DECAY_RANGE
-        pool.states.zero_()
-        o_seq, code = _run(pool, [0], cu, ins, sequential=True)
+    ins["w"][0:40, 1, 5] = 2.0 ** -8                      # sequence 0, head 1
+    ins["w"][cu[1] + 70:cu[1] + 110, 2, 60] = 2.0 ** -9   # sequence 1, head 2, its second chunk
+    ins["w"][cu[3] + 130, 0, 7] = 0.0                     # sequence 3, head 0: w = 0 once
+    S0 = oracle.round_bf16(wl.slot_states(31, "decay/s0", range(len(lengths)), 1, H, N)[:, 0])
+    tdt = torch.bfloat16 if state_dtype == "bf16" else torch.float32
+    with Pool(1, H, len(lengths), state_dtype=state_dtype) as pool:
+        pool.states[:, 0] = torch.from_numpy(S0).cuda().to(tdt)
+        o, code = _run(pool, list(range(len(lengths))), cu, ins, sequential=False)
         assert code == 0
-        S_seq = pool.states[0, 0].cpu().numpy()
-    o_ref, S_ref = oracle.prefill(np.zeros((1, H, N, N)), cu, *host_inputs(ins))
-    assert rel(o_seq, o_ref) < SEQ_PREFILL_TOL
-    assert rel(S_seq, S_ref[0]) < SEQ_PREFILL_TOL
+        S_gpu = pool.states[:, 0].float().cpu().numpy()
+    o_ref, S_ref = oracle.prefill(S0.astype(np.float64), cu, *host_inputs(ins))
+    if state_dtype == "bf16":
+        S_ref = oracle.round_bf16(S_ref)
+    check_parity(o, o_ref, PREFILL_TOL, cu=cu, what="o")
+    check_parity(S_gpu, S_ref, PREFILL_TOL, lead=2, what="S")
+    # the units that left the chunked path are exact to float32 (bf16 storage aside)
+    per = oracle.rel_err_segments(o, o_ref, cu)
+    assert per[0, 1] < 1e-4 and per[1, 2] < 1e-4 and per[3, 0] < 1e-4, per
+
+
+def test_decay_beyond_the_chunk_factorisation_with_checkpoints():
+    """The token-by-token route also writes every 64-token checkpoint of the unit."""
+    H, N = 2, 64
+    lengths = [130, 64]
+    cu = wl.cu_seqlens(lengths)
+    ins = wl.token_inputs(32, "decay/ck", int(cu[-1]), H, N, dtype="bf16")
+    ins["w"] = ins["w"].copy()
+    ins["w"][80:120, 0, 11] = 2.0 ** -8                   # sequence 0, head 0, second chunk
+    n_ck = [x // 64 for x in lengths]
+    cu_ck = np.concatenate([[0], np.cumsum(n_ck)]).astype(np.int32)
+    with Pool(1, H, len(lengths), n_snapshots=int(cu_ck[-1])) as pool:
+        slots = pool.create(len(lengths))
+        o = pool.prefill(0, i32(slots), i32(cu), *dev_inputs(ins, "bf16"), max_seqlen=max(lengths),
+                         cu_ckpt=i32(cu_ck), ckpt_ids=i32(np.arange(cu_ck[-1])))
+        assert pool.device_status() == 0
+        ck = pool.snapshots[:, 0].cpu().numpy()
+        S_gpu = pool.states[torch.as_tensor(slots), 0].cpu().numpy()
+    o_ref, S_ref, ck_ref = oracle.prefill_checkpoints(np.zeros((2, H, N, N)), cu, *host_inputs(ins))
+    check_parity(o.cpu().numpy(), o_ref, PREFILL_TOL, cu=cu, what="o")
+    check_parity(S_gpu, S_ref, PREFILL_TOL, lead=2, what="S")
+    ck_ref = np.stack([c for seq in ck_ref for c in seq])
+    check_parity(ck, ck_ref, PREFILL_TOL, lead=2, what="checkpoints")
+    assert oracle.rel_err(ck[:2, 0], ck_ref[:2, 0]) < 1e-4  # the token-by-token unit's checkpoints
 
 
 @pytest.mark.parametrize("sequential", [False, True])
