@@ -50,6 +50,14 @@
 //   G5  [Phi^T; R'^T] x (S0_hi + S0_lo)^T + [Y_B^T; Y_Q^T] x V -> [S_L^T; O^T],
 //       both A operands in tensor memory, S0 split into bf16 hi + lo (B read
 //       MN-major)                                    (M=128, N=64)
+//       It runs while the warps build the next chunk's elementwise operands; its
+//       completion is awaited just before the next G1 is issued (G1' writes the
+//       columns of its A operands).
+// One thread (lane 0 of warp 7) issues every copy and MMA.  A thread that issues
+// tcgen05.mma is held for about the time the tensor core takes to accept them
+// (some 60 cycles per K=16 instruction here), so the issuer is a warp whose work
+// right after each issue has slack: not warps 0 and 1, which run the diagonal
+// inverse after G1.
 // The A operands of G34 and G5 go from the readback registers straight back
 // into tensor memory as bf16; they never touch shared memory.
 // Accumulators live in tensor memory (256 columns); the float32 state leaves
@@ -74,6 +82,7 @@ using namespace sm100;
 
 constexpr int kL = 64;
 constexpr int kThreads = 256;  // 8 warps; two CTAs per SM
+constexpr int kIssuer = 224;   // lane 0 of warp 7 issues the copies and MMAs
 constexpr float kMaxLog2Range = 120.0f;           // |G - Gm| limit (float exponent range)
 constexpr float kMinDecayRel = 0x1p-120f, kMaxDecayRel = 0x1p120f;  // the same limit on 2^(G - Gm)
 
@@ -86,7 +95,7 @@ constexpr uint32_t kTile128 = 16384;  // 128 rows
 constexpr uint32_t SOFF_TOT = 0;                    // per-warp log2-decay totals [8][64] fp32
 constexpr uint32_t SOFF_GAM = SOFF_TOT + 8 * 64 * 4;  // D(0,L] per channel [64]
 constexpr uint32_t SOFF_BAR = SOFF_GAM + 64 * 4;    // mbarrier: MMA completion
-constexpr uint32_t SOFF_HOLD = SOFF_BAR + 16;       // tensor-memory base
+constexpr uint32_t SOFF_HOLD = SOFF_BAR + 24;       // tensor-memory base (after 3 mbarriers)
 constexpr uint32_t SOFF_FLAG = SOFF_HOLD + 4;       // abort flag
 constexpr uint32_t kSmallBytes = SOFF_FLAG + 4;
 constexpr uint32_t OFF_R1 = 0;                      // tile offsets from the aligned base
@@ -403,9 +412,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     auto blk = [base](int b) { return reinterpret_cast<float *>(base + OFF_R1 + b * kSlotBytes); };
 
     if (warp == 0) tmem_alloc(smem_addr(holder), kTmemCols);
-    if (tid == 0) {
+    if (tid == kIssuer) {
         mbar_init(bar_mma, 1);
         mbar_init(bar_mma + 8, 1);  // the input barrier
+        mbar_init(bar_mma + 16, 1);  // the state product G5
         fence_mbar_init();
         *flag = 0;
 #pragma unroll
@@ -416,20 +426,21 @@ __global__ void __launch_bounds__(kThreads, 2)
     // tcn into their staging tiles, completing on the input barrier (whose
     // expected byte count, one chunk's six boxes, is set by the first call of
     // each phase).  Boxes past the last token are zero-filled; the elementwise
-    // phase turns those rows into identity tokens.  Issued by thread 0.
+    // phase turns those rows into identity tokens.  Issued by the issuer thread.
     const uint32_t bar_in = bar_mma + 8;
+    const uint32_t bar_g5 = bar_mma + 16;
     auto stage_inputs = [&](int x0, int x1, int tcn, bool first) {
         if (first) mbar_arrive_expect_tx(bar_in, 6 * kTile64);
         for (int x = x0; x <= x1; ++x)
             tma_load_3d(smem_addr(base + stage_off(x)), &maps.m[x], 0, h, tcn, bar_in);
     };
-    // A load thread 0 has issued and not yet seen land (on the input barrier's
+    // A load the issuer has issued and not yet seen land (on the input barrier's
     // phase in_parity), for the drain after a wait that gave up.  (The MMA
     // barrier needs no such record: every commit is followed by its wait before
     // the loop can stop, so the last commit's phase is the one before ph_mma.)
     bool in_flight = false;
     uint32_t in_parity = 0;
-    if (tid == 0 && !p.test_skip_first_load) {
+    if (tid == kIssuer && !p.test_skip_first_load) {
         stage_inputs(0, 5, t0, true);
         in_flight = true;
     }
@@ -473,7 +484,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     // Every output row starts a multiple of 128 bytes past o (which the host
     // checks is 16-byte aligned), so o's own alignment decides the store width.
     const bool o_v8 = (reinterpret_cast<uintptr_t>(p.in.o) & 31u) == 0;
-    uint32_t ph_mma = 0, ph_in = 0;
+    uint32_t ph_mma = 0, ph_in = 0, ph_g5 = 0;
+    bool g5_pending = false;
     bool range_bad = false;  // a chunk's decay left the factorisation's range (this thread saw it)
     int prev_c = 0, prev_tc0 = 0, prev_Lc = 0;  // chunk whose state product awaits its readback
 
@@ -616,7 +628,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         uint32_t in_r[8], in_w[8], in_k[8], in_v[8], in_a[8], in_b[8];
         float e0s, e1s, eGm0, eGm1, EL0, EL1;  // 2^(G_{tb-1} - Gm), 2^Gm, 2^(G_L - Gm) per channel
         {
-            if (mma_wait(bar_in, ph_in, flag, p.wait_cycles) && tid == 0) in_flight = false;  // inputs landed
+            if (mma_wait(bar_in, ph_in, flag, p.wait_cycles) && tid == kIssuer) in_flight = false;  // inputs landed
             ph_in ^= 1;
             {
                 auto st = [&](int x, int t) -> uint32_t {
@@ -689,7 +701,14 @@ __global__ void __launch_bounds__(kThreads, 2)
         __syncthreads();
 
         // --------------------------------------------------- G1 and G1'
-        if (tid == 0) {
+        if (g5_pending) {  // the previous chunk's state product ran during the elementwise phase;
+                           // G1' writes the tensor-memory columns of its A operands
+            mma_wait(bar_g5, ph_g5, flag, p.wait_cycles);
+            ph_g5 ^= 1;
+            g5_pending = false;
+            tc_fence_after();
+        }
+        if (tid == kIssuer) {
             tc_fence_after();
             umma_128xNx64(tmem + kColG1, smem_addr(base + OFF_G1A), smem_addr(base + OFF_G1B), 64, false);
             umma_128xNx64(tmem + kColG1p, smem_addr(base + OFF_G1B), smem_addr(base + OFF_G1A), 128, false);
@@ -919,14 +938,14 @@ __global__ void __launch_bounds__(kThreads, 2)
         __syncthreads();
 
         // ------------------------------------------------------------- G2
-        if (tid == 0) {
+        if (tid == kIssuer) {
             tc_fence_after();
             umma_128xNx64(tmem + kColG2, smem_addr(base + OFF_G2A), smem_addr(base + OFF_G2B), 64, false);
             umma_commit(bar_mma);
         }
         mma_wait(bar_mma, ph_mma, flag, p.wait_cycles);
         ph_mma ^= 1;
-        if (tid == 0 && !last && !*flag) {  // G2A and R1 are dead
+        if (tid == kIssuer && !last && !*flag) {  // G2A and R1 are dead
             in_parity = ph_in;
             stage_inputs(0, 5, tc0 + kL, true);
             in_flight = true;
@@ -947,7 +966,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (*flag) break;
 
         // ------------------------------------------------------------ G34
-        if (tid == 0) {
+        if (tid == kIssuer) {
             tc_fence_after();
             // accumulates onto the additive terms loaded during the inverse
             umma_ta_128xNx64(tmem + 0, tmem + kColZA, smem_addr(base + OFF_G34B), 128, true, true);
@@ -976,16 +995,14 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (*flag) break;
 
         // ------------------- G5: [S_L^T; O^T] = [Phi^T; R'^T] [S0_hi | S0_lo]^T + Y^T V^T
-        if (tid == 0) {
+        if (tid == kIssuer) {
             tc_fence_after();
             umma_ta_128xNx64(tmem + 0, tmem + kColA2, smem_addr(base + OFF_SHI), 64, false, true);
             umma_ta_128xNx64(tmem + 0, tmem + kColA2, smem_addr(base + OFF_SLO), 64, true, true);
             umma_ta_128xNx64(tmem + 0, tmem + kColYA, smem_addr(base + OFF_V), 64, true, false);
-            umma_commit(bar_mma);
+            umma_commit(bar_g5);
         }
-        mma_wait(bar_mma, ph_mma, flag, p.wait_cycles);
-        ph_mma ^= 1;
-        tc_fence_after();
+        g5_pending = true;  // awaited once the next chunk's elementwise phase is done (or after the loop)
         prev_c = c;
         prev_tc0 = tc0;
         prev_Lc = Lc;
@@ -994,15 +1011,23 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     // every thread sees the same abort flag; a unit with a chunk out of range is
     // run token by token below instead, so its chunked final state is not stored
+    if (g5_pending && !*flag) {
+        mma_wait(bar_g5, ph_g5, flag, p.wait_cycles);
+        ph_g5 ^= 1;
+        g5_pending = false;
+    }
     const bool fallback = __syncthreads_or(range_bad) != 0;
     if (!*flag && !fallback) {
         tc_fence_after();
         readback_state_product(prev_c, prev_tc0, prev_Lc, true);
     }
 
-    if (*flag && tid == 0) {  // a wait gave up: let what thread 0 issued land (bounded), then leave
+    if (*flag && tid == kIssuer) {  // a wait gave up: let what the issuer issued land (bounded), then leave
         flag_status(p.lv.status, WKV7_DEV_WAIT_TIMEOUT);
         mbar_wait_bounded(bar_mma, ph_mma ^ 1u, p.wait_cycles);  // the last commit
+        // the last state product: not yet waited for, or its wait gave up (a phase
+        // before any commit counts as complete, so this returns at once then)
+        mbar_wait_bounded(bar_g5, g5_pending ? ph_g5 : ph_g5 ^ 1u, p.wait_cycles);
         if (in_flight) mbar_wait_bounded(bar_in, in_parity, p.wait_cycles);
     }
     tc_fence_before();
