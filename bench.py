@@ -93,10 +93,13 @@ def load_peaks():
         return dict(FALLBACK_PEAKS)
 
 
+# kernel -> (committed ncu summary, the workloads whose launch of that kernel it
+# profiles, the sources it was taken on)
 KERNEL_SOURCES = {
-    "prefill": ("prefill_chunk_kernel.mixed_prefill_64seq.md",
-                ["prefill_chunk.cu", "sm100_ptx.cuh", "device_common.cuh", "wkv7_internal.h"]),
-    "decode": ("decode_kernel.decode_12L_12H_256of1024.md",
+    "prefill": ("prefill_chunk_kernel.mixed_prefill_64seq.md", ("mixed",),
+                ["prefill_chunk.cu", "sm100_ptx.cuh", "device_common.cuh", "wkv7_internal.h",
+                 "prefill_seq_unit.cuh"]),
+    "decode": ("decode_kernel.mixed_decode_1024of4096.md", ("mixed", "decode_mixed"),
                ["decode.cu", "device_common.cuh", "wkv7_internal.h", "row_sums.cuh"]),
 }
 
@@ -106,9 +109,9 @@ def profiled_traffic(kernel: str, workload: str):
     was taken on this workload's launch shape and the kernel's sources are
     unchanged since; else None."""
     import hashlib
-    if kernel not in KERNEL_SOURCES or workload != "mixed" or kernel != "prefill":
+    if kernel not in KERNEL_SOURCES or workload not in KERNEL_SOURCES[kernel][1]:
         return None
-    fname, sources = KERNEL_SOURCES[kernel]
+    fname, _, sources = KERNEL_SOURCES[kernel]
     try:
         text = open(os.path.join(ROOT, "profiles", fname)).read()
         m = hashlib.sha256()
@@ -928,7 +931,9 @@ def run_ours(args):
         n_slot_steps = rows // per_row
         extra["decode"] = {"slot_steps_per_s": round(n_slot_steps / (phase_ms["decode"] / 1e3), 1),
                            "GB_per_s": phases["decode"]["GB_per_s"],
-                           "hbm_frac": phases["decode"]["hbm_frac"]}
+                           "hbm_frac": phases["decode"]["hbm_frac"],
+                           "traffic": profiled_traffic("decode", args.workload)
+                           if getattr(wk, "state_dtype", "f32") == "f32" else None}
     if "verify" in phase_ms:
         extra["verify"] = {"slot_token_steps_per_s": round(wk.tokens_per_step
                                                            / (phase_ms["verify"] / 1e3), 1),
