@@ -307,7 +307,11 @@ wkv7_status wkv7_decode_multi(wkv7_pool *pool, int32_t layer, const int32_t *slo
  * whose decay over half a chunk (32 tokens) exceeds 2^120 in some channel --
  * beyond the float range of the chunk factorisation, e.g. w = 2^-8 for 32
  * tokens, or w = 0 -- is run token by token in float32 by the same call
- * instead (its results then equal wkv7_prefill_sequential's).  max_seqlen
+ * instead (its results then equal wkv7_prefill_sequential's).  The test
+ * takes every w in (0, 1], the range of the method's decay: it looks at the
+ * factors at the ends of each 8-token run, between which they only fall (a
+ * w above 1 may take a factor out of range unseen, losing precision there;
+ * NaN, inf and 0 are always caught).  max_seqlen
  * bounds every sequence length.  Errors: INVALID_ARG, UNSUPPORTED (in_dtype
  * must be WKV7_BF16; a misaligned base), CUDA.  Device: WKV7_DEV_BAD_SLOT,
  * WKV7_DEV_BAD_SEQLENS (that sequence is skipped), WKV7_DEV_WAIT_TIMEOUT. */

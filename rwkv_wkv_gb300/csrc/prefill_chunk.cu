@@ -217,16 +217,15 @@ __device__ __forceinline__ void load_row16(const uint8_t *tile, int row, int col
 
 // ------------------------------------------- 16x16 fp32 block products (TF32)
 // Warp-level D (+)= A B for 16x16 fp32 blocks in shared memory (row pitch
-// kSlotRow floats), on the tensor cores with TF32 operands (rounded to nearest)
+// kSlotRow floats), on the tensor cores with TF32 operands (truncated)
 // and fp32 accumulation: two K=8 steps x two 8-column halves of
 // mma.sync.m16n8k8.  Fragment layout of m16n8k8 (g = lane / 4, q = lane % 4):
 // A a0 (g, q), a1 (g+8, q), a2 (g, q+4), a3 (g+8, q+4); B b0 (q, g), b1 (q+4, g);
 // C/D c0 (g, 2q), c1 (g, 2q+1), c2 (g+8, 2q), c3 (g+8, 2q+1) -- per 8-column half.
-__device__ __forceinline__ uint32_t tf32_rn(float x) {
-    uint32_t y;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(y) : "f"(x));
-    return y;
-}
+// A TF32 operand: the float's own bits; the tensor core reads their upper 19 bits
+// (truncation).  T leaves the inverse rounded to bf16 (8 bits) anyway, and a
+// conversion instruction per operand element cost 3% of the kernel's time.
+__device__ __forceinline__ uint32_t tf32_rn(float x) { return __float_as_uint(x); }
 
 __device__ __forceinline__ void mma_tf32_m16n8k8(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                                  uint32_t b1) {
@@ -646,12 +645,13 @@ __global__ void __launch_bounds__(kThreads, 2)
                     in_b[i] = valid ? st(5, t) : 0u;
                 }
             }
-            float s0 = 0.f, s1 = 0.f;  // this warp's log2-decay totals
+            float p0 = 1.f, p1 = 1.f;  // this warp's decay products
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                s0 += lg2_approx(bf16_lo(in_w[i]));
-                s1 += lg2_approx(bf16_hi(in_w[i]));
+                p0 *= bf16_lo(in_w[i]);
+                p1 *= bf16_hi(in_w[i]);
             }
+            const float s0 = lg2_approx(p0), s1 = lg2_approx(p1);  // this warp's log2-decay totals
             *reinterpret_cast<float2 *>(tot + warp * 64 + ch) = make_float2(s0, s1);
             __syncthreads();
             float G0 = 0.f, G1 = 0.f, Gm0 = 0.f, Gm1 = 0.f, G630 = 0.f, G631 = 0.f;
@@ -679,13 +679,10 @@ __global__ void __launch_bounds__(kThreads, 2)
             float e0 = e0s, e1 = e1s;
             uint32_t ep2 = pack_bf16(e0, e1);  // 2^(G_{t-1} - Gm)
             uint8_t *g1a = base + OFF_G1A, *g1b = base + OFF_G1B;
-            bool in_range = true;  // every 2^(G_t - Gm) of this warp's tokens within 2^+-120
 #pragma unroll
             for (int ii = 0; ii < 8; ++ii) {
                 e0 *= bf16_lo(in_w[ii]);  // padding tokens have w = 1
                 e1 *= bf16_hi(in_w[ii]);
-                in_range = in_range && e0 >= kMinDecayRel && e0 <= kMaxDecayRel &&
-                           e1 >= kMinDecayRel && e1 <= kMaxDecayRel;  // false for NaN too
                 const uint32_t ec2 = pack_bf16(e0, e1);                              // 2^(G_t - Gm)
                 const uint32_t iv2 = pack_bf16(rcp_approx(e0), rcp_approx(e1));    // 2^(Gm - G_t)
                 const uint32_t off = rowbase + ii * 128 + ((xl ^ ii) << 4);
@@ -695,7 +692,11 @@ __global__ void __launch_bounds__(kThreads, 2)
                 *reinterpret_cast<uint32_t *>(g1b + 8192 + off) = bmul2(in_r[ii], ec2);
                 ep2 = ec2;
             }
-            if (!in_range) range_bad = true;
+            // With every w in (0, 1] the factors fall from 2^(G_{tb-1} - Gm) (checked above)
+            // to the last token's: that one decides whether all lie within 2^+-120 (a NaN or
+            // an overflow anywhere reaches it too).
+            if (!(e0 >= kMinDecayRel && e0 <= kMaxDecayRel && e1 >= kMinDecayRel && e1 <= kMaxDecayRel))
+                range_bad = true;
         }
         fence_proxy_async_smem();
         __syncthreads();
