@@ -719,8 +719,12 @@ __global__ void __launch_bounds__(kThreads, 2)
             float e0 = e0s, e1 = e1s;
             uint32_t dp2 = pack_bf16(e0 * eGm0, e1 * eGm1);  // D(0, t-1]
             uint8_t *r0t = base + OFF_R0;
-            uint32_t cb[3][2][4];  // channel-major operands [Bhat, Khat, V][channel][token pair]
+            uint32_t cb[3][2][4];  // channel-major operands [Bhat, Khat, V][channel ch + (e ^ sw)][token pair]
             uint32_t prv[3];
+            // lanes 4-7 of each group of 8 take channel ch + 1 first, so that the eight
+            // 16-byte stores of a quarter-warp fall in eight different bank groups
+            const uint32_t sw = (static_cast<uint32_t>(lane) >> 2) & 1u;
+            const uint32_t sel0 = sw ? 0x7632u : 0x5410u, sel1 = sel0 ^ 0x2222u;
 #pragma unroll
             for (int ii = 0; ii < 8; ++ii) {
                 e0 *= bf16_lo(in_w[ii]);
@@ -736,8 +740,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                     if ((ii & 1) == 0) {
                         prv[o] = cur[o];
                     } else {  // tokens (ii-1, ii) of channel ch, then of channel ch+1
-                        cb[o][0][ii >> 1] = __byte_perm(prv[o], cur[o], 0x5410);
-                        cb[o][1][ii >> 1] = __byte_perm(prv[o], cur[o], 0x7632);
+                        cb[o][0][ii >> 1] = __byte_perm(prv[o], cur[o], sel0);
+                        cb[o][1][ii >> 1] = __byte_perm(prv[o], cur[o], sel1);
                     }
                 }
                 dp2 = dc2;
@@ -746,8 +750,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
             for (int o = 0; o < 3; ++o)
 #pragma unroll
-                for (int e = 0; e < 2; ++e)  // 8 tokens of channel-major row ch + e
-                    *reinterpret_cast<uint4 *>(dst[o] + sw128_off(ch + e, tb)) =
+                for (int e = 0; e < 2; ++e)  // 8 tokens of channel-major row ch + (e ^ sw)
+                    *reinterpret_cast<uint4 *>(dst[o] + sw128_off(ch + (e ^ sw), tb)) =
                         make_uint4(cb[o][e][0], cb[o][e][1], cb[o][e][2], cb[o][e][3]);
         }
         if (c > 0) {  // the previous chunk's state product, read back while G1 and G1' run
