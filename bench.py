@@ -67,6 +67,9 @@ def parse_args(argv=None):
                    help="verify workload: no per-token rollback states")
     p.add_argument("--state-dtype", choices=["f32", "bf16"], default="f32",
                    help="mixed and sweep workloads: state storage (bf16 halves the state bytes)")
+    p.add_argument("--out-dtype", choices=["f32", "bf16"], default="f32",
+                   help="mixed workload: output dtype (bf16: each readout rounded to bf16, half the "
+                        "output bytes)")
     p.add_argument("--no-targets", action="store_true",
                    help="mixed workload: skip the 8 x 4096 prefill and the 32-layer sweep lines")
     p.add_argument("--min-timed-s", type=float, default=0.6,
@@ -213,10 +216,11 @@ class Workload:
 class Mixed(Workload):
     name = wl.MIXED.name
 
-    def __init__(self, torch, device, seed=wl.MIXED.seed, state_dtype="f32"):
+    def __init__(self, torch, device, seed=wl.MIXED.seed, state_dtype="f32", out_dtype="f32"):
         from rwkv_wkv_gb300 import Pool
         W = wl.MIXED
-        self.state_dtype = state_dtype
+        self.state_dtype, self.out_dtype = state_dtype, out_dtype
+        self.out_elem_bytes = 2 if out_dtype == "bf16" else 4
         self.state_head_bytes = HEAD_BYTES_STATE // (2 if state_dtype == "bf16" else 1)
         self.torch, self.device = torch, device
         self.H, self.N = W.H, W.N
@@ -225,7 +229,7 @@ class Mixed(Workload):
         self.lengths = plan["lengths"].astype(np.int64)
         self.total = int(self.lengths.sum())
         self.pool = Pool(1, W.H, W.n_slots, n_snapshots=wl.MIXED_VERB_N, device=device,
-                         state_dtype=state_dtype)
+                         state_dtype=state_dtype, out_dtype=out_dtype)
         g = torch.Generator(device=device).manual_seed(seed)
         self.pool.states.normal_(0.0, 0.1, generator=g)
         # slot table: every id in use except the prefill targets, which each
@@ -243,12 +247,13 @@ class Mixed(Workload):
         self.dec_in = wl.token_inputs_device(seed, B, W.H, W.N, device, generator_offset=1)
         self.pre_in = wl.token_inputs_device(seed, self.total, W.H, W.N, device,
                                              generator_offset=2)
-        self.o_dec = torch.empty(B, W.H, W.N, dtype=torch.float32, device=device)
-        self.o_pre = torch.empty(self.total, W.H, W.N, dtype=torch.float32, device=device)
+        odt = self.pool.o_torch_dtype
+        self.o_dec = torch.empty(B, W.H, W.N, dtype=odt, device=device)
+        self.o_pre = torch.empty(self.total, W.H, W.N, dtype=odt, device=device)
         slot_bytes = self.pool.slot_bytes
         nv = wl.MIXED_VERB_N
         in_row = W.H * W.N * 2 * 6
-        out_row = W.H * W.N * 4
+        out_row = W.H * W.N * self.out_elem_bytes
         self.phases = ["create", "snapshot", "decode", "prefill", "fork", "restore"]
         self.phase_bytes = {
             "create": wl.MIXED_PREFILL_SEQS * slot_bytes,
@@ -321,12 +326,13 @@ class Mixed(Workload):
 
     def config(self):
         return {"workload": wl.MIXED.description
-                + ("; bf16 state storage" if self.state_dtype == "bf16" else ""),
+                + ("; bf16 state storage" if self.state_dtype == "bf16" else "")
+                + ("; bf16 outputs" if self.out_dtype == "bf16" else ""),
                 "pool_slots": wl.MIXED.n_slots,
                 "layers": 1, "heads": self.H, "head_size": self.N,
                 "decode_slots": wl.MIXED_DECODE_B, "prefill_seqs": wl.MIXED_PREFILL_SEQS,
                 "prefill_tokens": self.total, "verb_slots": wl.MIXED_VERB_N,
-                "state_dtype": self.state_dtype, "input_dtype": "bf16", "output_dtype": "f32"}
+                "state_dtype": self.state_dtype, "input_dtype": "bf16", "output_dtype": self.out_dtype}
 
     def oracle_sample(self, frac_target: float):
         """Sample of the step for the CPU oracle: every decode row and prefill
@@ -682,7 +688,7 @@ class DecodeMixed(Workload):
 
 def make_workload(args, torch, device):
     if args.workload == "mixed":
-        return Mixed(torch, device, state_dtype=args.state_dtype)
+        return Mixed(torch, device, state_dtype=args.state_dtype, out_dtype=args.out_dtype)
     if args.workload == "decode_mixed":
         return DecodeMixed(torch, device)
     if args.workload == "decode12":
@@ -734,12 +740,18 @@ def time_oracle_sample(work, keep=None):
     return t_total, n_threads
 
 
-def gpu_parity(work, refs):
+def _default_dtypes(wk) -> bool:
+    """Float32 states and outputs: the launch shapes the committed profiles cover."""
+    return getattr(wk, "state_dtype", "f32") == "f32" and getattr(wk, "out_dtype", "f32") == "f32"
+
+
+def gpu_parity(work, refs, out_dtype="f32"):
     """The library on the oracle sample's own inputs (a pool of the sample's heads),
     against the oracle's results: the normwise-max relative error of o and of the
     states, its worst (row or sequence, head) slice (denominators floored at 1% of
     the median slice scale), and the elementwise median |x - y| / (|y| + 1e-6
-    max|y|).  Part of the CPU-baseline leg."""
+    max|y|).  Part of the CPU-baseline leg.  With bf16 outputs the tolerance grows by
+    half a bf16 unit (2^-8)."""
     import oracle
     import torch
     from rwkv_wkv_gb300 import Pool
@@ -751,26 +763,28 @@ def gpu_parity(work, refs):
         if item[0] == "decode":
             st = item[1]
             n, nh = st.shape[0], st.shape[1]
-            with Pool(1, nh, n, device=dev) as pool:
+            with Pool(1, nh, n, device=dev, out_dtype=out_dtype) as pool:
                 pool.states[:, 0] = torch.from_numpy(np.ascontiguousarray(st, dtype=np.float32)).to(dev)
                 o = pool.decode_step(0, torch.arange(n, dtype=torch.int32, device=dev), *ins)
                 status = pool.device_status()
-                o, S = o.cpu().numpy(), pool.states[:, 0].cpu().numpy()
+                o, S = o.float().cpu().numpy(), pool.states[:, 0].cpu().numpy()
             slices_o = oracle.rel_err_slices(o, o_ref, 2, floor_frac=1e-2)
             tol = 1e-4
         else:
             cu = item[1]
             st = item[3]
             n, nh = st.shape[0], st.shape[1]
-            with Pool(1, nh, n, device=dev) as pool:
+            with Pool(1, nh, n, device=dev, out_dtype=out_dtype) as pool:
                 pool.states.zero_()
                 o = pool.prefill(0, torch.arange(n, dtype=torch.int32, device=dev),
                                  torch.as_tensor(cu, device=dev), *ins,
                                  max_seqlen=int(np.max(np.diff(cu))))
                 status = pool.device_status()
-                o, S = o.cpu().numpy(), pool.states[:, 0].cpu().numpy()
+                o, S = o.float().cpu().numpy(), pool.states[:, 0].cpu().numpy()
             slices_o = oracle.rel_err_segments(o, o_ref, cu, floor_frac=1e-2)
             tol = 2e-2
+        if out_dtype == "bf16":
+            tol += 2.0 ** -8
         out[item[0]] = {"o_normwise": float(f"{oracle.rel_err(o, o_ref):.3e}"),
                         "o_worst_slice": float(f"{float(np.max(slices_o)):.3e}"),
                         "o_elem_median": float(f"{float(np.median(oracle.elementwise_rel(o, o_ref))):.3e}"),
@@ -893,8 +907,7 @@ def run_ours(args):
                 "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
                 "peak_source": peaks["source"] + " (hbm copy)",
                 "bytes_per_launch": wk.phase_bytes[dom], "ms_per_launch": round(dom_ms, 4),
-                "traffic": profiled_traffic(dom, args.workload)
-                if getattr(wk, "state_dtype", "f32") == "f32" else None,
+                "traffic": profiled_traffic(dom, args.workload) if _default_dtypes(wk) else None,
                 "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)"}
     phases = {}
     for n in wk.phases:
@@ -927,13 +940,14 @@ def run_ours(args):
     extra = {}
     if "decode" in phase_ms:
         rows = wk.phase_bytes["decode"]
-        per_row = wk.H * (2 * getattr(wk, "state_head_bytes", HEAD_BYTES_STATE) + wk.N * 2 * 6 + wk.N * 4)
+        per_row = wk.H * (2 * getattr(wk, "state_head_bytes", HEAD_BYTES_STATE) + wk.N * 2 * 6
+                          + wk.N * getattr(wk, "out_elem_bytes", 4))
         n_slot_steps = rows // per_row
         extra["decode"] = {"slot_steps_per_s": round(n_slot_steps / (phase_ms["decode"] / 1e3), 1),
                            "GB_per_s": phases["decode"]["GB_per_s"],
                            "hbm_frac": phases["decode"]["hbm_frac"],
                            "traffic": profiled_traffic("decode", args.workload)
-                           if getattr(wk, "state_dtype", "f32") == "f32" else None}
+                           if _default_dtypes(wk) else None}
     if "verify" in phase_ms:
         extra["verify"] = {"slot_token_steps_per_s": round(wk.tokens_per_step
                                                            / (phase_ms["verify"] / 1e3), 1),
@@ -947,6 +961,7 @@ def run_ours(args):
 
     cfg = wk.config()
     state_dtype = getattr(wk, "state_dtype", "f32")
+    out_dtype = getattr(wk, "out_dtype", "f32")
 
     unit = getattr(wk, "unit", "tokens/s")
 
@@ -959,8 +974,7 @@ def run_ours(args):
         cpu_base = cpu_baseline(wk, target_seconds=8.0)
 
     targets = None
-    if (args.workload == "mixed" and world == 1 and not args.no_targets
-            and getattr(wk, "state_dtype", "f32") == "f32"):
+    if (args.workload == "mixed" and world == 1 and not args.no_targets and _default_dtypes(wk)):
         del wk  # free the mixed step's pool before the next workloads are built
         torch.cuda.empty_cache()
         targets = run_targets(torch, device, args, peaks)
@@ -985,7 +999,8 @@ def run_ours(args):
                        "to bf16); decode arithmetic and outputs float32; inputs bf16"
                        if state_dtype == "bf16" else
                        "state, decode arithmetic and outputs float32; prefill contractions "
-                       "bf16 tensor-core operands with float32 accumulation; inputs bf16"),
+                       "bf16 tensor-core operands with float32 accumulation; inputs bf16")
+                      + ("; outputs rounded to bf16 as stored" if out_dtype == "bf16" else ""),
     }
     if world > 1:
         torch.distributed.destroy_process_group()
@@ -1179,7 +1194,7 @@ def cpu_baseline(wk, target_seconds=12.0, parity=True):
            "cores": threads, "kind": "oracle", "seconds": round(t, 2),
            "sample": sample["desc"]}
     if parity:
-        out["parity_on_sample"] = gpu_parity(work, refs)
+        out["parity_on_sample"] = gpu_parity(work, refs, getattr(wk, "out_dtype", "f32"))
     return out
 
 
@@ -1222,6 +1237,7 @@ def _shapes_only(args):
     s = S()
     s.state_dtype = args.state_dtype
     s.state_head_bytes = HEAD_BYTES_STATE // (2 if args.state_dtype == "bf16" else 1)
+    s.out_dtype = args.out_dtype if args.workload == "mixed" else "f32"
     if args.workload == "mixed":
         plan = wl.mixed_plan()
         s.H, s.N = wl.MIXED.H, wl.MIXED.N

@@ -28,8 +28,8 @@
  *                  the larger table, rounded up to 256 bytes)
  *
  * Token inputs are packed [rows][n_heads][head_size] (row = batch entry for
- * decode, token for prefill), contiguous, float32 or bf16; outputs o are
- * float32 with the same shape.
+ * decode, token for prefill), contiguous, float32 or bf16; outputs o have
+ * the same shape, float32 (or bf16, see out_dtype).
  *
  * Conventions for every call.
  *   - All pointers named *_dev and every tensor argument are device pointers
@@ -127,6 +127,12 @@ typedef struct {
                             and every checkpoint, and at a checkpoint the carry
                             continues from the rounded value, so that resuming from
                             a checkpoint still reproduces the uninterrupted run. */
+    int32_t out_dtype;   /* WKV7_F32 (0, the default when zero-initialised): every
+                            recurrence call writes o in float32.  WKV7_BF16: o in
+                            bf16, the float32 readout rounded to nearest even (the
+                            states and everything else are unchanged; the method
+                            fixes no output precision, and the float32 paths'
+                            1e-4 contract holds only for float32 o). */
 } wkv7_pool_desc;
 
 /* ---------------------------------------------------------------- pool ---- */
@@ -253,7 +259,10 @@ wkv7_status wkv7_slot_resume(wkv7_pool *pool, const void *host_src, size_t host_
 
 /* Every call in this section reads its inputs and writes o with vector loads
  * and stores, so the six input bases and o must be 16-byte aligned; a base
- * that is not is reported as UNSUPPORTED before any launch. */
+ * that is not is reported as UNSUPPORTED before any launch.  o holds float32
+ * elements, or bf16 ones on a pool created with out_dtype = WKV7_BF16 (each
+ * the float32 readout rounded to nearest even); the shapes below count
+ * elements either way. */
 
 /* decode: one token for each of n slots at one layer -- the per-token
  * recurrence of RWKV-X Architecture, "WKV-7 Kernel (Generalized Delta Rule)"
@@ -262,14 +271,14 @@ wkv7_status wkv7_slot_resume(wkv7_pool *pool, const void *host_src, size_t host_
  * RWKV, GDN and Mamba hybrids" ("The allocation unit wkvm changes").  For b < n and every
  * head h, the state at (slot_ids_dev[b], layer, h) takes one step of the
  * recurrence with inputs x[b][h][:] (x = r, w, k, v, a, b; [n][n_heads][64],
- * dtype in_dtype) and o[b][h][:] (float32) receives the readout.  The state is
+ * dtype in_dtype) and o[b][h][:] receives the readout.  The state is
  * read once and written once.  Errors: INVALID_ARG (including n > n_slots),
  * UNSUPPORTED (a misaligned base), CUDA.  Device: WKV7_DEV_BAD_SLOT for an out-of-range id (that
  * row's state and o are untouched). */
 wkv7_status wkv7_decode_step(wkv7_pool *pool, int32_t layer, const int32_t *slot_ids_dev,
                              int32_t n, wkv7_dtype in_dtype, const void *r, const void *w,
                              const void *k, const void *v, const void *a, const void *b,
-                             float *o, cudaStream_t stream);
+                             void *o, cudaStream_t stream);
 
 /* decode_multi: n_tokens (K >= 1) consecutive tokens for each of n slots at
  * one layer, the verify pass of speculative decoding on state slots (the
@@ -292,7 +301,7 @@ wkv7_status wkv7_decode_step(wkv7_pool *pool, int32_t layer, const int32_t *slot
 wkv7_status wkv7_decode_multi(wkv7_pool *pool, int32_t layer, const int32_t *slot_ids_dev,
                               int32_t n, int32_t n_tokens, wkv7_dtype in_dtype, const void *r,
                               const void *w, const void *k, const void *v, const void *a,
-                              const void *b, float *o, const int32_t *step_snap_ids_dev,
+                              const void *b, void *o, const int32_t *step_snap_ids_dev,
                               cudaStream_t stream);
 
 /* prefill: n_seqs sequences packed back to back (RWKV-X Architecture, "What
@@ -300,7 +309,7 @@ wkv7_status wkv7_decode_multi(wkv7_pool *pool, int32_t layer, const int32_t *slo
  * tokens cu_seqlens_dev[s] .. cu_seqlens_dev[s+1]-1 of the packed inputs
  * [total_tokens][n_heads][64] (bf16) and starts from the state at
  * (slot_ids_dev[s], layer); the slot receives the state after its last token
- * and o[t][h][:] (float32) the readout of every token.  The result equals
+ * and o[t][h][:] the readout of every token.  The result equals
  * the token-by-token recurrence up to rounding; it is computed in chunks of
  * 64 tokens anchored at each sequence's first token, with bf16 tensor-core
  * operands and a float32 state carried between chunks.  A (sequence, head)
@@ -319,7 +328,7 @@ wkv7_status wkv7_prefill(wkv7_pool *pool, int32_t layer, const int32_t *slot_ids
                          const int32_t *cu_seqlens_dev, int32_t n_seqs, int32_t total_tokens,
                          int32_t max_seqlen, wkv7_dtype in_dtype, const void *r,
                          const void *w, const void *k, const void *v, const void *a,
-                         const void *b, float *o, cudaStream_t stream);
+                         const void *b, void *o, cudaStream_t stream);
 
 /* prefill_sequential: the same contract as wkv7_prefill, computed token by
  * token in float32 on the CUDA cores (no chunking, no tensor cores; accepts
@@ -330,7 +339,7 @@ wkv7_status wkv7_prefill_sequential(wkv7_pool *pool, int32_t layer,
                                     int32_t total_tokens, int32_t max_seqlen,
                                     wkv7_dtype in_dtype, const void *r, const void *w,
                                     const void *k, const void *v, const void *a,
-                                    const void *b, float *o, cudaStream_t stream);
+                                    const void *b, void *o, cudaStream_t stream);
 
 /* prefill_checkpointed: wkv7_prefill (sequential == 0) or
  * wkv7_prefill_sequential (sequential != 0) that also keeps the state at
@@ -356,7 +365,7 @@ wkv7_status wkv7_prefill_checkpointed(wkv7_pool *pool, int32_t layer, const int3
                                       int32_t total_tokens, int32_t max_seqlen,
                                       wkv7_dtype in_dtype, const void *r, const void *w,
                                       const void *k, const void *v, const void *a,
-                                      const void *b, float *o, const int32_t *cu_ckpt_dev,
+                                      const void *b, void *o, const int32_t *cu_ckpt_dev,
                                       const int32_t *ckpt_snap_ids_dev, int32_t sequential,
                                       cudaStream_t stream);
 

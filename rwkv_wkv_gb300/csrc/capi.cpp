@@ -79,7 +79,8 @@ struct IdTable {
 
 bool desc_valid(const wkv7_pool_desc *d) {
     return d && d->n_layers >= 1 && d->n_heads >= 1 && d->head_size >= 1 && d->n_slots >= 1 &&
-           d->n_snapshots >= 0 && (d->state_dtype == WKV7_F32 || d->state_dtype == WKV7_BF16);
+           d->n_snapshots >= 0 && (d->state_dtype == WKV7_F32 || d->state_dtype == WKV7_BF16) &&
+           (d->out_dtype == WKV7_F32 || d->out_dtype == WKV7_BF16);
 }
 
 size_t state_elem_bytes(const wkv7_pool_desc *d) { return d->state_dtype == WKV7_BF16 ? 2 : 4; }
@@ -118,6 +119,7 @@ struct wkv7_pool {
     uint32_t *marks = nullptr;  // id-validation bitmap (scratch of wkv7_validate_ids)
     long long slot_floats = 0;  // slot bytes / 4: the unit of the byte-copy verbs
     bool state_bf16 = false;
+    bool out_bf16 = false;  // o written in bf16
     std::mutex mu;
     IdTable slots;
     IdTable snapshots;
@@ -139,7 +141,7 @@ wkv7::LayerView layer_view(wkv7_pool *p, int32_t layer) {
 bool dtype_valid(wkv7_dtype d) { return d == WKV7_F32 || d == WKV7_BF16; }
 
 bool inputs_present(const void *r, const void *w, const void *k, const void *v, const void *a,
-                    const void *b, const float *o) {
+                    const void *b, const void *o) {
     return r && w && k && v && a && b && o;
 }
 
@@ -147,7 +149,7 @@ bool inputs_present(const void *r, const void *w, const void *k, const void *v, 
 // accesses (the chunked prefill's tensor maps also need 16-byte bases); every
 // access offset is a multiple of 16 bytes from its base.
 bool inputs_aligned(const void *r, const void *w, const void *k, const void *v, const void *a,
-                    const void *b, const float *o) {
+                    const void *b, const void *o) {
     const void *x[7] = {r, w, k, v, a, b, o};
     for (const void *p : x)
         if (reinterpret_cast<uintptr_t>(p) % 16 != 0) return false;
@@ -206,6 +208,7 @@ wkv7_status wkv7_pool_create(const wkv7_pool_desc *desc, wkv7_pool **out) {
     p->states = reinterpret_cast<float *>(p->base + kHeaderBytes);
     p->slot_floats = static_cast<long long>(slot_bytes_of(desc) / sizeof(float));
     p->state_bf16 = desc->state_dtype == WKV7_BF16;
+    p->out_bf16 = desc->out_dtype == WKV7_BF16;
     p->snaps = p->states + static_cast<size_t>(p->slot_floats) * static_cast<size_t>(desc->n_slots);
     p->marks = reinterpret_cast<uint32_t *>(
         p->base + kHeaderBytes +
@@ -422,7 +425,7 @@ wkv7_status wkv7_slot_resume(wkv7_pool *pool, const void *host_src, size_t host_
 wkv7_status wkv7_decode_step(wkv7_pool *pool, int32_t layer, const int32_t *slot_ids_dev,
                              int32_t n, wkv7_dtype in_dtype, const void *r, const void *w,
                              const void *k, const void *v, const void *a, const void *b,
-                             float *o, cudaStream_t stream) {
+                             void *o, cudaStream_t stream) {
     if (!pool || layer < 0 || layer >= pool->desc.n_layers || n < 0) return WKV7_ERR_INVALID_ARG;
     if (!dtype_valid(in_dtype)) return WKV7_ERR_INVALID_ARG;
     if (n > pool->desc.n_slots) return WKV7_ERR_INVALID_ARG;
@@ -433,7 +436,7 @@ wkv7_status wkv7_decode_step(wkv7_pool *pool, int32_t layer, const int32_t *slot
     da.lv = layer_view(pool, layer);
     da.slot_ids = slot_ids_dev;
     da.n = n;
-    da.in = {r, w, k, v, a, b, in_dtype == WKV7_BF16, o};
+    da.in = {r, w, k, v, a, b, in_dtype == WKV7_BF16, o, pool->out_bf16};
     da.state_bf16 = pool->state_bf16;
     int launches = 0;
     cudaError_t e = wkv7::launch_decode(da, stream, &launches);
@@ -443,7 +446,7 @@ wkv7_status wkv7_decode_step(wkv7_pool *pool, int32_t layer, const int32_t *slot
 wkv7_status wkv7_decode_multi(wkv7_pool *pool, int32_t layer, const int32_t *slot_ids_dev,
                               int32_t n, int32_t n_tokens, wkv7_dtype in_dtype, const void *r,
                               const void *w, const void *k, const void *v, const void *a,
-                              const void *b, float *o, const int32_t *step_snap_ids_dev,
+                              const void *b, void *o, const int32_t *step_snap_ids_dev,
                               cudaStream_t stream) {
     if (!pool || layer < 0 || layer >= pool->desc.n_layers || n < 0 || n_tokens < 1)
         return WKV7_ERR_INVALID_ARG;
@@ -459,7 +462,7 @@ wkv7_status wkv7_decode_multi(wkv7_pool *pool, int32_t layer, const int32_t *slo
     da.slot_ids = slot_ids_dev;
     da.n = n;
     da.n_tok = n_tokens;
-    da.in = {r, w, k, v, a, b, in_dtype == WKV7_BF16, o};
+    da.in = {r, w, k, v, a, b, in_dtype == WKV7_BF16, o, pool->out_bf16};
     da.snaps = pool->snaps;
     da.n_snaps = pool->desc.n_snapshots;
     da.step_snap_ids = step_snap_ids_dev;
@@ -473,7 +476,7 @@ static wkv7_status prefill_common(wkv7_pool *pool, int32_t layer, const int32_t 
                                   const int32_t *cu_seqlens_dev, int32_t n_seqs,
                                   int32_t total_tokens, int32_t max_seqlen, wkv7_dtype in_dtype,
                                   const void *r, const void *w, const void *k, const void *v,
-                                  const void *a, const void *b, float *o, cudaStream_t stream,
+                                  const void *a, const void *b, void *o, cudaStream_t stream,
                                   bool chunked, const int32_t *cu_ckpt_dev = nullptr,
                                   const int32_t *ckpt_snap_ids_dev = nullptr) {
     if (!pool || layer < 0 || layer >= pool->desc.n_layers) return WKV7_ERR_INVALID_ARG;
@@ -493,7 +496,7 @@ static wkv7_status prefill_common(wkv7_pool *pool, int32_t layer, const int32_t 
     pa.n_seqs = n_seqs;
     pa.total_tokens = total_tokens;
     pa.max_seqlen = max_seqlen;
-    pa.in = {r, w, k, v, a, b, in_dtype == WKV7_BF16, o};
+    pa.in = {r, w, k, v, a, b, in_dtype == WKV7_BF16, o, pool->out_bf16};
     pa.ck = {pool->snaps, pool->desc.n_snapshots, cu_ckpt_dev, ckpt_snap_ids_dev};
     pa.state_bf16 = pool->state_bf16;
     const bool force_timeout = g_test_wait_timeout.load(std::memory_order_relaxed) != 0;
@@ -508,7 +511,7 @@ static wkv7_status prefill_common(wkv7_pool *pool, int32_t layer, const int32_t 
 wkv7_status wkv7_prefill(wkv7_pool *pool, int32_t layer, const int32_t *slot_ids_dev,
                          const int32_t *cu_seqlens_dev, int32_t n_seqs, int32_t total_tokens,
                          int32_t max_seqlen, wkv7_dtype in_dtype, const void *r, const void *w,
-                         const void *k, const void *v, const void *a, const void *b, float *o,
+                         const void *k, const void *v, const void *a, const void *b, void *o,
                          cudaStream_t stream) {
     return prefill_common(pool, layer, slot_ids_dev, cu_seqlens_dev, n_seqs, total_tokens,
                           max_seqlen, in_dtype, r, w, k, v, a, b, o, stream, true);
@@ -519,7 +522,7 @@ wkv7_status wkv7_prefill_sequential(wkv7_pool *pool, int32_t layer, const int32_
                                     int32_t total_tokens, int32_t max_seqlen,
                                     wkv7_dtype in_dtype, const void *r, const void *w,
                                     const void *k, const void *v, const void *a, const void *b,
-                                    float *o, cudaStream_t stream) {
+                                    void *o, cudaStream_t stream) {
     return prefill_common(pool, layer, slot_ids_dev, cu_seqlens_dev, n_seqs, total_tokens,
                           max_seqlen, in_dtype, r, w, k, v, a, b, o, stream, false);
 }
@@ -529,7 +532,7 @@ wkv7_status wkv7_prefill_checkpointed(wkv7_pool *pool, int32_t layer, const int3
                                       int32_t total_tokens, int32_t max_seqlen,
                                       wkv7_dtype in_dtype, const void *r, const void *w,
                                       const void *k, const void *v, const void *a, const void *b,
-                                      float *o, const int32_t *cu_ckpt_dev,
+                                      void *o, const int32_t *cu_ckpt_dev,
                                       const int32_t *ckpt_snap_ids_dev, int32_t sequential,
                                       cudaStream_t stream) {
     if (!pool) return WKV7_ERR_INVALID_ARG;

@@ -89,7 +89,7 @@ __global__ void __launch_bounds__(256) decode_kernel(DecodeArgs p) {
     for (int m = 0; m < 4; ++m)
         __stcs(reinterpret_cast<float4 *>(S + (row0 + 16 * m) * kHeadSize + c), s[m]);
     const float ou = reduce_scatter4(os, tid & 15);  // row ((tid >> 2) & 3)'s readout
-    if ((tid & 3) == 0) p.in.o[io + row0 + 16 * ((tid >> 2) & 3)] = ou;
+    if ((tid & 3) == 0) store_out(p.in.o, p.in.o_bf16, io + row0 + 16 * ((tid >> 2) & 3), ou);
 }
 
 // Decode over a pool whose states are stored in bf16 (half the bytes of the
@@ -188,7 +188,7 @@ __global__ void __launch_bounds__(kBf16Threads) decode_bf16state_kernel(DecodeAr
         for (int m = 0; m < kBf16Rows; ++m) os[m] += __shfl_xor_sync(0xffffffffu, os[m], off);
     if ((tid & 7) == 0) {
 #pragma unroll
-        for (int m = 0; m < kBf16Rows; ++m) p.in.o[io + row0 + kBf16RowStep * m] = os[m];
+        for (int m = 0; m < kBf16Rows; ++m) store_out(p.in.o, p.in.o_bf16, io + row0 + kBf16RowStep * m, os[m]);
     }
 }
 

@@ -152,7 +152,7 @@ __global__ void __launch_bounds__(256, (SNAPS && SBF16) ? 4 : 5) decode_multi_ke
                 }
             }
             const float ou = reduce_scatter4(os, tid & 15);  // row ((tid >> 2) & 3)'s readout
-            if ((tid & 3) == 0) p.in.o[io_of(k) + row0 + 16 * ((tid >> 2) & 3)] = ou;
+            if ((tid & 3) == 0) store_out(p.in.o, p.in.o_bf16, io_of(k) + row0 + 16 * ((tid >> 2) & 3), ou);
         }
     }
 #pragma unroll

@@ -98,6 +98,22 @@ __device__ __forceinline__ void st_global_v8(float *p, const float *v) {
                  : "memory");
 }
 
+// Eight 32-bit words to global memory in one 32-byte store; p must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8_b32(uint32_t *p, const uint32_t *v) {
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(v[0]), "r"(v[1]),
+                 "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+
+// One output element o[idx]: float32, or rounded to bf16 (nearest even) when the
+// pool's out_dtype is bf16.
+__device__ __forceinline__ void store_out(void *o, bool o_bf16, size_t idx, float v) {
+    if (o_bf16)
+        reinterpret_cast<__nv_bfloat16 *>(o)[idx] = __float2bfloat16_rn(v);
+    else
+        reinterpret_cast<float *>(o)[idx] = v;
+}
+
 // Programmatic dependent launch.  A kernel launched with launch_pdl lets the next
 // kernel in its stream start launching once all of its CTAs have begun
 // (launch_dependents), and itself waits for everything before it in the stream

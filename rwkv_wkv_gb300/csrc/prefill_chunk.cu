@@ -361,8 +361,9 @@ __device__ __noinline__ void prefill_unit_token_by_token(const PrefillArgs &p, i
     prefill_seq_unit<true, SBF16>(p, h, t0, t1, ck0, s_off, st);
 }
 
-// SBF16: the pool stores its states in bf16 (see the store paths of the readback).
-template <bool SBF16>
+// SBF16: the pool stores its states in bf16 (see the store paths of the readback);
+// OBF16: o is written in bf16 (p.in.o_bf16).
+template <bool SBF16, bool OBF16>
 __global__ void __launch_bounds__(kThreads, 2)
     prefill_chunk_kernel(const PrefillArgs p, const __grid_constant__ InputMaps maps) {
     extern __shared__ uint8_t smem_raw[];
@@ -480,8 +481,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int cpart = 32 * (warp >> 2);      // this thread's 32-column part of each 64-column group
 
     const int n_chunks = (len + kL - 1) / kL;
-    // Every output row starts a multiple of 128 bytes past o (which the host
-    // checks is 16-byte aligned), so o's own alignment decides the store width.
+    // Every output row starts a multiple of 128 bytes (64 for bf16 o) past o, which
+    // the host checks is 16-byte aligned, so o's own alignment decides the store width.
     const bool o_v8 = (reinterpret_cast<uintptr_t>(p.in.o) & 31u) == 0;
     uint32_t ph_mma = 0, ph_in = 0, ph_g5 = 0;
     bool g5_pending = false;
@@ -498,8 +499,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         tmem_ld_wait();
         if (row >= 64) {  // O row t' -> o[otc0 + t'][h][cpart ..]
             const int tq = row - 64;
-            float *dst = p.in.o + (static_cast<size_t>(otc0 + tq) * H + h) * kHeadSize + cpart;
-            if (tq < oLc) {  // 128 bytes per thread: 32-byte stores when o allows them
+            const size_t oi = (static_cast<size_t>(otc0 + tq) * H + h) * kHeadSize + cpart;
+            if (tq < oLc && !OBF16) {  // 128 bytes per thread: 32-byte stores when o allows them
+                float *dst = static_cast<float *>(p.in.o) + oi;
                 if (o_v8) {
 #pragma unroll
                     for (int q = 0; q < 4; ++q) st_global_v8(dst + 8 * q, v + 8 * q);
@@ -508,6 +510,19 @@ __global__ void __launch_bounds__(kThreads, 2)
                     for (int q = 0; q < 8; ++q)
                         reinterpret_cast<float4 *>(dst)[q] =
                             make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                }
+            } else if (OBF16 && tq < oLc) {  // bf16 o: 64 bytes per thread, rounded to nearest even
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) pk[e] = pack_bf16(v[2 * e], v[2 * e + 1]);
+                uint32_t *dst = reinterpret_cast<uint32_t *>(static_cast<__nv_bfloat16 *>(p.in.o) + oi);
+                if (o_v8) {
+                    st_global_v8_b32(dst, pk);
+                    st_global_v8_b32(dst + 8, pk + 8);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        reinterpret_cast<uint4 *>(dst)[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
                 }
             }
         } else {  // S_L^T row j (values i of this thread's part)
@@ -1098,7 +1113,10 @@ cudaError_t launch_prefill_chunked(const PrefillArgs &a, cudaStream_t s, int *la
     for (int x = 0; x < 6; ++x)
         if (!encode_input_map(&maps.m[x], src[x], a.lv.n_heads, a.total_tokens))
             return cudaErrorInvalidValue;
-    auto kernel = a.state_bf16 ? prefill_chunk_kernel<true> : prefill_chunk_kernel<false>;
+    void (*const kernels[4])(const PrefillArgs, const InputMaps) = {
+        prefill_chunk_kernel<false, false>, prefill_chunk_kernel<false, true>,
+        prefill_chunk_kernel<true, false>, prefill_chunk_kernel<true, true>};
+    auto kernel = kernels[(a.state_bf16 ? 2 : 0) | (a.in.o_bf16 ? 1 : 0)];
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     const unsigned ny = static_cast<unsigned>(a.n_seqs) < kGridY ? static_cast<unsigned>(a.n_seqs) : kGridY;

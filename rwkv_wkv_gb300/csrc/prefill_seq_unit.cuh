@@ -103,7 +103,7 @@ __device__ __forceinline__ void prefill_seq_unit(const PrefillArgs &p, int h, in
             float osum = (op[0] + op[1]) + (op[2] + op[3]);
             osum += __shfl_xor_sync(0xffffffffu, osum, 1);
             osum += __shfl_xor_sync(0xffffffffu, osum, 2);
-            if (q == 0) p.in.o[(static_cast<size_t>(tb + tau) * H + h) * kHeadSize + i] = osum;
+            if (q == 0) store_out(p.in.o, p.in.o_bf16, (static_cast<size_t>(tb + tau) * H + h) * kHeadSize + i, osum);
         }
         const int done = tb + n_tok - t0;  // tokens of the sequence consumed so far
         if (p.ck.cu_ckpt && n_tok == kSeqTile && (done & 63) == 0) {  // a 64-token boundary

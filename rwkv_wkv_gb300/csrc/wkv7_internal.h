@@ -23,7 +23,8 @@ struct LayerView {
 struct TokenInputs {
     const void *r, *w, *k, *v, *a, *b;
     bool bf16;
-    float *o;
+    void *o;      // float32, or bf16 when o_bf16
+    bool o_bf16;  // the pool's out_dtype: o rounded to bf16 (nearest even)
 };
 
 struct DecodeArgs {

@@ -42,7 +42,8 @@ class PoolDesc(ctypes.Structure):
     _fields_ = [("n_layers", ctypes.c_int32), ("n_heads", ctypes.c_int32),
                 ("head_size", ctypes.c_int32), ("n_slots", ctypes.c_int32),
                 ("n_snapshots", ctypes.c_int32), ("device_buffer", ctypes.c_void_p),
-                ("buffer_bytes", ctypes.c_size_t), ("state_dtype", ctypes.c_int32)]
+                ("buffer_bytes", ctypes.c_size_t), ("state_dtype", ctypes.c_int32),
+                ("out_dtype", ctypes.c_int32)]
 
 
 # name -> (restype, argtypes)
@@ -150,11 +151,13 @@ class Pool:
     States live in one torch-allocated device buffer: ``states`` is a float32
     (or, with state_dtype="bf16", bfloat16) view [n_slots, n_layers, n_heads,
     64, 64] and ``snapshots`` the same for the parked copies (S[i][j]: i =
-    value row, j = key column).
+    value row, j = key column).  Outputs o are float32, or bfloat16 with
+    out_dtype="bf16" (the float32 readout rounded to nearest even).
     """
 
     def __init__(self, n_layers: int, n_heads: int, n_slots: int, n_snapshots: int = 0,
-                 head_size: int = HEAD_SIZE, device=None, state_dtype: str = "f32"):
+                 head_size: int = HEAD_SIZE, device=None, state_dtype: str = "f32",
+                 out_dtype: str = "f32"):
         self._lib = load_library()
         self.device = torch.device("cuda", torch.cuda.current_device()) if device is None \
             else torch.device(device)
@@ -162,9 +165,12 @@ class Pool:
         self.n_slots, self.n_snapshots = n_slots, n_snapshots
         if state_dtype not in ("f32", "bf16"):
             raise ValueError("state_dtype must be 'f32' or 'bf16'")
-        self.state_dtype = state_dtype
+        if out_dtype not in ("f32", "bf16"):
+            raise ValueError("out_dtype must be 'f32' or 'bf16'")
+        self.state_dtype, self.out_dtype = state_dtype, out_dtype
+        self.o_torch_dtype = torch.bfloat16 if out_dtype == "bf16" else torch.float32
         desc = PoolDesc(n_layers, n_heads, head_size, n_slots, n_snapshots, None, 0,
-                        BF16 if state_dtype == "bf16" else F32)
+                        BF16 if state_dtype == "bf16" else F32, BF16 if out_dtype == "bf16" else F32)
         nbytes = self._lib.wkv7_pool_required_bytes(ctypes.byref(desc))
         if nbytes == 0:
             raise Wkv7Error(1, "Pool", "invalid description")
@@ -304,11 +310,11 @@ class Pool:
 
     def _out(self, o, rows):
         if o is None:
-            return torch.empty(rows, self.n_heads, self.head_size, dtype=torch.float32,
+            return torch.empty(rows, self.n_heads, self.head_size, dtype=self.o_torch_dtype,
                                device=self.device)
-        if (o.dtype != torch.float32 or o.device != self.device or not o.is_contiguous()
+        if (o.dtype != self.o_torch_dtype or o.device != self.device or not o.is_contiguous()
                 or tuple(o.shape) != (rows, self.n_heads, self.head_size)):
-            raise ValueError("o must be a contiguous float32 [rows, n_heads, 64] tensor")
+            raise ValueError(f"o must be a contiguous {self.o_torch_dtype} [rows, n_heads, 64] tensor")
         return o
 
     def decode_step(self, layer: int, slot_ids: torch.Tensor, r, w, k, v, a, b, o=None,
@@ -324,7 +330,7 @@ class Pool:
     def decode_multi(self, layer: int, slot_ids: torch.Tensor, r, w, k, v, a, b, o=None,
                      step_snap_ids: torch.Tensor | None = None, stream=None) -> torch.Tensor:
         """K consecutive tokens per slot: inputs [n, K, n_heads, 64] (one dtype), o the
-        same shape in float32; with step_snap_ids ([n, K] device int32) the state after
+        same shape in the pool's output dtype; with step_snap_ids ([n, K] device int32) the state after
         every token also goes to those snapshot ids (this layer)."""
         n = slot_ids.numel()
         if r.dim() != 4 or r.shape[0] != n:
@@ -334,7 +340,7 @@ class Pool:
                                       tuple(x.shape[:2]) == (n, K) else x
                                       for x in (r, w, k, v, a, b)), n * K)
         if o is None:
-            o = torch.empty(n, K, self.n_heads, self.head_size, dtype=torch.float32,
+            o = torch.empty(n, K, self.n_heads, self.head_size, dtype=self.o_torch_dtype,
                             device=self.device)
         self._out(o.reshape(n * K, *o.shape[2:]) if o.dim() == 4 else o, n * K)
         snaps = None

@@ -51,10 +51,10 @@ def test_version_and_strings(lib):
 
 
 def _desc(**kw):
-    d = dict(n_layers=2, n_heads=3, head_size=64, n_slots=8, n_snapshots=4, state_dtype=0)
+    d = dict(n_layers=2, n_heads=3, head_size=64, n_slots=8, n_snapshots=4, state_dtype=0, out_dtype=0)
     d.update(kw)
     return wkv7.PoolDesc(d["n_layers"], d["n_heads"], d["head_size"], d["n_slots"],
-                         d["n_snapshots"], None, 0, d["state_dtype"])
+                         d["n_snapshots"], None, 0, d["state_dtype"], d["out_dtype"])
 
 
 def _fake_pool(lib, **kw):
@@ -250,5 +250,29 @@ def test_bf16_state_pool(lib):
         assert lib.wkv7_decode_multi(h, 0, x, 1, 0, 1, *ins, x, None, None) == 1
         desc = wkv7.PoolDesc()
         assert lib.wkv7_pool_get_desc(h, ctypes.byref(desc)) == 0 and desc.state_dtype == 1
+    finally:
+        lib.wkv7_pool_destroy(h)
+
+
+def test_bf16_output_pool(lib):
+    """out_dtype: float32 (0) or bf16 (1), nothing else; it changes no byte count
+    and every recurrence call is offered on such a pool."""
+    base = lib.wkv7_pool_required_bytes(ctypes.byref(_desc()))
+    assert lib.wkv7_pool_required_bytes(ctypes.byref(_desc(out_dtype=1))) == base
+    assert lib.wkv7_pool_required_bytes(ctypes.byref(_desc(out_dtype=2))) == 0
+    assert lib.wkv7_pool_required_bytes(ctypes.byref(_desc(out_dtype=-1))) == 0
+    st, h = _fake_pool(lib, out_dtype=1)
+    assert st == 0
+    x = ctypes.c_void_p(FAKE_DEVICE_ADDR)
+    ins = [x] * 6
+    try:
+        assert lib.wkv7_prefill(h, 0, x, x, 0, 0, 0, 1, *ins, x, None) == 0
+        assert lib.wkv7_decode_step(h, 0, x, 0, 1, *ins, x, None) == 0
+        assert lib.wkv7_decode_multi(h, 0, x, 0, 2, 1, *ins, x, None, None) == 0
+        # o is checked like every other base: missing -> INVALID_ARG, misaligned -> UNSUPPORTED
+        assert lib.wkv7_decode_step(h, 0, x, 1, 1, *ins, None, None) == 1
+        assert lib.wkv7_decode_step(h, 0, x, 1, 1, *ins, ctypes.c_void_p(FAKE_DEVICE_ADDR + 2), None) == 7
+        desc = wkv7.PoolDesc()
+        assert lib.wkv7_pool_get_desc(h, ctypes.byref(desc)) == 0 and desc.out_dtype == 1
     finally:
         lib.wkv7_pool_destroy(h)
