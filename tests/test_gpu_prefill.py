@@ -352,3 +352,24 @@ def test_sequential_prefill_float32_inputs(state_dtype):
     if state_dtype == "bf16":
         assert torch.equal(runs["bf16"][0], runs["f32"][0])
         assert torch.equal(runs["bf16"][1], runs["f32"][1].to(torch.bfloat16))
+
+
+def test_long_sequence_error_does_not_grow_with_length():
+    """One 65,536-token sequence (1,024 chunks), 2 heads, from N(0, 0.1) start
+    states: the chunked path's float32 carry with the bf16 hi/lo state split
+    keeps the error of the last 4,096 tokens' outputs and of the final state
+    within the tolerance, and not far above the first 4,096 tokens' error."""
+    H, N, T = 2, 64, 65536
+    cu = wl.cu_seqlens([T])
+    ins = wl.token_inputs(31, "long", T, H, N, dtype="bf16")
+    S0 = wl.slot_states(31, "long/s0", [0], 1, H, N)[:, 0]
+    with Pool(1, H, 1) as pool:
+        pool.states[:, 0] = torch.from_numpy(S0).cuda()
+        o_gpu, code = _run(pool, [0], cu, ins, sequential=False)
+        assert code == 0
+        S_gpu = pool.states[:, 0].cpu().numpy()
+    o_ref, S_ref = oracle.prefill(S0.astype(np.float64), cu, *host_inputs(ins), n_threads=2)
+    head = rel(o_gpu[:4096], o_ref[:4096])
+    tail = rel(o_gpu[-4096:], o_ref[-4096:])
+    assert tail < PREFILL_TOL and rel(S_gpu, S_ref) < PREFILL_TOL, (head, tail)
+    assert tail < 4 * max(head, 1e-3), (head, tail)
