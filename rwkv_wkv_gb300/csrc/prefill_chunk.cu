@@ -277,7 +277,9 @@ __device__ __forceinline__ void block_frag_store(float *D, const float (&acc)[2]
 // ragged tail of the grid is short.  The grid is (head, rank) with the rank
 // split over y and z.
 // Every CTA derives the same order from cu_seqlens; `work` is 1.1 KB of shared
-// memory.  Returns the sequence of the given rank.
+// memory.  Returns the sequence of the given rank.  Up to 256 sequences, one
+// thread per sequence counts those ordered before it (a few hundred cycles);
+// beyond, a histogram of the keys and two CTA-wide scans.
 constexpr int kMaxRankedSeqs = 4096;
 constexpr unsigned kGridY = 65535;
 
@@ -313,6 +315,24 @@ __device__ __noinline__ int seq_of_rank(const int *cu, int n, int rank, int *wor
     if (n == 1) return 0;
     int *hist = work, *sums = work + 256, *found = work + 264;
     const int tid = threadIdx.x;
+    if (n <= kThreads) {  // one thread per sequence: its rank is the number ordered before it
+        int *key = work;
+        const int mine = tid < n ? chunk_key(cu, tid) : 0;
+        if (tid < n) key[tid] = mine;
+        __syncthreads();
+        if (tid < n) {
+            int r = 0;
+            for (int q = 0; q < n; ++q) {
+                const int kq = key[q];
+                r += (kq < mine) | ((kq == mine) & (q < tid));
+            }
+            if (r == rank) found[0] = tid;
+        }
+        __syncthreads();
+        const int seq = found[0];
+        __syncthreads();  // the work area is reused by the caller
+        return seq;
+    }
     hist[tid] = 0;
     __syncthreads();
     for (int q = tid; q < n; q += kThreads) atomicAdd(&hist[chunk_key(cu, q)], 1);
@@ -462,14 +482,19 @@ __global__ void __launch_bounds__(kThreads, 2)
             else
                 xs[q] = __ldcg(S + (i0 + q) * kHeadSize + j);
         }
+        uint32_t hw[8], lw[8];  // values i0 + 2e, i0 + 2e + 1: bf16 hi and the bf16 of the remainder
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
-            const int i = i0 + q;
-            const float x = xs[q];
-            const __nv_bfloat16 hb = __float2bfloat16_rn(x);
-            *reinterpret_cast<__nv_bfloat16 *>(base + OFF_SHI + sw128_off(j, i)) = hb;
-            *reinterpret_cast<__nv_bfloat16 *>(base + OFF_SLO + sw128_off(j, i)) =
-                __float2bfloat16_rn(x - __bfloat162float(hb));
+        for (int e = 0; e < 8; ++e) {
+            hw[e] = pack_bf16(xs[2 * e], xs[2 * e + 1]);
+            lw[e] = pack_bf16(xs[2 * e] - bf16_lo(hw[e]), xs[2 * e + 1] - bf16_hi(hw[e]));
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t off = sw128_off(j, i0 + 8 * h);
+            *reinterpret_cast<uint4 *>(base + OFF_SHI + off) =
+                make_uint4(hw[4 * h], hw[4 * h + 1], hw[4 * h + 2], hw[4 * h + 3]);
+            *reinterpret_cast<uint4 *>(base + OFF_SLO + off) =
+                make_uint4(lw[4 * h], lw[4 * h + 1], lw[4 * h + 2], lw[4 * h + 3]);
         }
     }
     tc_fence_before();
