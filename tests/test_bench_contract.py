@@ -44,3 +44,17 @@ def test_reference_arm_has_no_host_copy_reference_for_hibernate():
     assert out.returncode == 0, out.stderr[-2000:]
     d = json.loads([ln for ln in out.stdout.splitlines() if ln.strip().startswith("{")][-1])
     assert d["impl"] == "reference" and "unavailable" in d
+
+
+def test_output_dtype_reaches_both_arms_configs():
+    """--out-dtype names the mixed step's output dtype in the config both arms print
+    (the GPU arm's Mixed.config and the reference arm's shapes-only copy share it)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    for od in ("f32", "bf16"):
+        args = bench.parse_args(["--impl", "reference", "--out-dtype", od])
+        cfg = bench._shapes_only(args).config()
+        assert cfg["output_dtype"] == od
+        assert cfg["workload"].endswith("; bf16 outputs") == (od == "bf16")
+    args = bench.parse_args(["--impl", "reference", "--workload", "decode12", "--out-dtype", "bf16"])
+    assert bench._shapes_only(args).config()["output_dtype"] == "f32"  # mixed step only
